@@ -1,0 +1,192 @@
+/*
+ * nvfp4kv.h -- C ABI of the NVFP4 paged KV cache library (libnvfp4kv.so).
+ *
+ * The library implements the three cache paths of "Accelerating Long-Context
+ * and Agentic Inference with NVFP4 KV Cache" (section A2) on one GB300 GPU
+ * (sm_103a), as hand-written CUDA:
+ *
+ *   nvfp4_kv_quantize_append      -- new K/V written into the paged cache
+ *                                    (path 1 "initial prefill" writes its
+ *                                    FP8/BF16 KV this way; path 2 appends the
+ *                                    new chunk this way).
+ *   nvfp4_paged_decode_attention  -- path 3 "decode": the kernel reads packed
+ *                                    4-bit values and block scales, dequantises
+ *                                    them on chip (Fig. 3) and never writes
+ *                                    dequantised KV back to HBM.
+ *   nvfp4_prefix_dequant          -- path 2 "chunked prefill / extend": the
+ *                                    cached prefix is expanded into a reusable
+ *                                    workspace shared across layers.
+ *
+ * Format (section A3 and Fig. 1): each run of 16 consecutive values along
+ * head_dim is one block with an FP8 E4M3 scale; values are 4-bit E2M1; an
+ * FP32 tensor scale multiplies everything (fixed at 1.0 on the page, A7).
+ * 16 values take 8 bytes + 1 scale byte, (8 + 1) / 16 = 0.5625 of FP8
+ * (section A2, storage ratio formula).  An FP8 E4M3 cache (the page's
+ * fp8_e4m3 baseline, A4) is supported for comparison.
+ *
+ * Conventions for every call:
+ *   - All buffers are caller-owned DEVICE memory unless stated otherwise.  The
+ *     library never allocates device memory; calls that need scratch take a
+ *     caller-sized workspace.
+ *   - Calls are asynchronous on `stream` (NULL = legacy default stream) and do
+ *     not synchronise.  Arguments are validated on the host before any launch;
+ *     a rejected call launches nothing and returns a negative status.
+ *   - Indices a call reads from device memory (slot mapping, block table
+ *     entries, lengths) are range-checked on the device.  An out-of-range index
+ *     is skipped (never dereferenced) and recorded in a per-device error word
+ *     that nvfp4kv_check_device_errors() reports.  No kernel traps or asserts.
+ *   - head_dim is 128.  page_size P is 16, 32, 64 or 128 tokens.
+ *
+ * Pool layout, one slab per (page, kv_head), slabs ordered page-major:
+ *   pool = uint8[num_pages][num_kv_heads][slab_bytes]
+ *   NVFP4 slab (144 * P bytes):
+ *     K codes  uint8[P][64]  byte i of row t = element 2i (low nibble) and
+ *                            element 2i+1 (high nibble) of token row t
+ *     K scales uint8[P][8]   E4M3 scale of block j (elements 16j..16j+15)
+ *     V codes  uint8[P][64]  as K codes
+ *     V scales uint8[8][P]   block-major: scale of block j of row t at [j][t]
+ *   FP8 slab (256 * P bytes):  K uint8[P][128] | V uint8[P][128] (E4M3 codes)
+ *   Token position t of a sequence is row t % P of page block_table[t / P].
+ *   A nibble is an E2M1 code: bit 3 sign, bits 2..0 magnitude index into
+ *   {0, 0.5, 1, 1.5, 2, 3, 4, 6}.
+ */
+#ifndef NVFP4KV_H
+#define NVFP4KV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes. */
+typedef enum {
+    NVFP4KV_OK = 0,
+    NVFP4KV_EINVAL = -1,        /* a pointer, size, shape or alignment is invalid */
+    NVFP4KV_EUNSUPPORTED = -2,  /* valid request outside what this build implements */
+    NVFP4KV_ECUDA = -3,         /* a CUDA runtime call or kernel launch failed */
+    NVFP4KV_EDEVICE_CHECK = -4  /* a kernel found an out-of-range index (see conventions) */
+} nvfp4kv_status;
+
+typedef enum {
+    NVFP4KV_DTYPE_NVFP4 = 0,    /* E2M1 values + E4M3 scale per 16 */
+    NVFP4KV_DTYPE_FP8_E4M3 = 1  /* one E4M3 code per value */
+} nvfp4kv_dtype;
+
+/* Describes a caller-owned page pool.  The library reads it, never frees it. */
+typedef struct {
+    void *pool;             /* device, uint8[num_pages][num_kv_heads][slab_bytes], 256-byte aligned */
+    int64_t num_pages;      /* >= 1 */
+    int32_t page_size;      /* P: 16, 32, 64 or 128 tokens */
+    int32_t num_kv_heads;   /* >= 1 */
+    int32_t head_dim;       /* must be 128 */
+    int32_t dtype;          /* nvfp4kv_dtype */
+    float k_global_scale;   /* FP32 tensor scale of K, > 0 and finite (1.0 on the page) */
+    float v_global_scale;   /* FP32 tensor scale of V, > 0 and finite */
+} nvfp4kv_cache;
+
+/* Bytes of one (page, kv_head) slab: 144*P (NVFP4) or 256*P (FP8); 0 if the
+ * descriptor is invalid. */
+size_t nvfp4kv_slab_bytes(const nvfp4kv_cache *cache);
+
+/* Bytes of the whole pool (num_pages * num_kv_heads * slab); 0 if invalid. */
+size_t nvfp4kv_pool_bytes(const nvfp4kv_cache *cache);
+
+/*
+ * Quantise BF16 K and V rows and write them into the pool.
+ * Source: section A2, path 1 (KV quantised to NVFP4 and written to the
+ * persistent cache) and path 2 (the new chunk's KV quantised and appended).
+ *
+ *   k, v          device BF16 [num_tokens][token_stride]; the row of kv head h
+ *                 is elements h*128 .. h*128+127 of the token.  16-byte aligned.
+ *   token_stride  elements between consecutive tokens; >= num_kv_heads*128 and
+ *                 a multiple of 8.
+ *   slot_mapping  device int64 [num_tokens]: slot = page * P + row.  A negative
+ *                 slot skips the token; a slot >= num_pages * P is skipped and
+ *                 flagged in the device error word.
+ * Per block of 16 values x_i (g = the tensor scale of K or V):
+ *   scale  = E4M3(amax_i |x_i| / (6 g)),  round to nearest even, saturating;
+ *   code_i = E2M1(x_i / (scale g)),       round to nearest even, saturating;
+ *            a block whose scale is 0 stores signed zeros.
+ * The quotients are formed in FP32 (for g = 1 this equals exact rounding).
+ * FP8 pools store E4M3(x_i / g) per value.  Two tokens writing the same slot
+ * in one call is a caller error (the result is one of the two rows).
+ * num_tokens == 0 is a no-op.
+ */
+int nvfp4_kv_quantize_append(const nvfp4kv_cache *cache, const void *k, const void *v, int64_t num_tokens,
+                             int64_t token_stride, const int64_t *slot_mapping, cudaStream_t stream);
+
+/* Workspace bytes nvfp4_paged_decode_attention needs for this shape and
+ * num_splits on the current device (0 if the arguments are invalid). */
+size_t nvfp4kv_decode_workspace_bytes(const nvfp4kv_cache *cache, int batch, int num_q_heads, int num_splits);
+
+/* Number of work partitions an auto-split (num_splits = 0) call uses on the
+ * current device for this cache. */
+int nvfp4kv_decode_auto_splits(const nvfp4kv_cache *cache, int num_q_heads);
+
+/*
+ * Paged GQA decode attention over the cache, one query token per sequence.
+ * Source: section A2, path 3 and Fig. 3 (packed K/V tiles and block scales
+ * staged in shared memory, unpacked in registers, scaled, matrix products on
+ * the dequantised values, tensor scales applied as product scaling).
+ *
+ *   q            device BF16 [batch][num_q_heads][128], 16-byte aligned
+ *   block_table  device int32 [batch][max_pages_per_seq]; only the first
+ *                ceil(seq_lens[b] / P) entries of row b are read
+ *   seq_lens     device int32 [batch]; 0 <= seq_lens[b] <= max_pages_per_seq*P
+ *                (a larger value is clamped and flagged)
+ *   out          device BF16 [batch][num_q_heads][128], 16-byte aligned
+ *   workspace    device, >= nvfp4kv_decode_workspace_bytes(...) bytes,
+ *                256-byte aligned; holds split-KV partials and the work plan
+ *   num_splits   number of work partitions the KV range is cut into (each
+ *                becomes one CTA; partials are merged by a log-sum-exp
+ *                reduction kernel); 0 = auto, a multiple of the SM count.
+ * Query head h attends KV head h / G, G = num_q_heads / num_kv_heads <= 16.
+ *   out[b][h] = sum_t softmax_t(sm_scale * g_K * q_h . k_t) * g_V * v_t
+ * over t < seq_lens[b], with k_t, v_t the dequantised cache rows.  A sequence
+ * of length 0 yields zeros.
+ */
+int nvfp4_paged_decode_attention(const nvfp4kv_cache *cache, const void *q, int batch, int num_q_heads,
+                                 const int32_t *block_table, int max_pages_per_seq, const int32_t *seq_lens,
+                                 float sm_scale, void *out, void *workspace, size_t workspace_bytes, int num_splits,
+                                 cudaStream_t stream);
+
+/*
+ * Dequantise cached prefixes into a contiguous BF16 workspace.
+ * Source: section A2, path 2 (cached prefix entries gathered, dequantised into
+ * a layer-shared workspace that the new chunk's KV joins before attention).
+ * The page writes an FP8 workspace; this library writes BF16, which holds
+ * every dequantised NVFP4 value exactly (at most 5 significant bits).
+ *
+ *   block_table     device int32 [num_reqs][max_pages_per_seq]
+ *   prefix_lens     device int32 [num_reqs]
+ *   cu_prefix_lens  device int32 [num_reqs + 1], cu[0] = 0, cu[r+1] = cu[r] + prefix_lens[r]
+ *   total_prefix_tokens  host copy of cu[num_reqs] (sizes the launch)
+ *   k_ws, v_ws      device BF16 [total_prefix_tokens][num_kv_heads][128],
+ *                   16-byte aligned; row cu[r] + t receives prefix token t of
+ *                   request r:  value = e2m1 * e4m3 * g, rounded to BF16
+ *                   (exact for g = 1).
+ */
+int nvfp4_prefix_dequant(const nvfp4kv_cache *cache, const int32_t *block_table, int max_pages_per_seq,
+                         const int32_t *prefix_lens, const int32_t *cu_prefix_lens, int num_reqs,
+                         int64_t total_prefix_tokens, void *k_ws, void *v_ws, cudaStream_t stream);
+
+/* Synchronises `stream`, then reads and clears the current device's error
+ * word.  Returns NVFP4KV_OK, NVFP4KV_EDEVICE_CHECK (some kernel skipped an
+ * out-of-range index since the last check) or NVFP4KV_ECUDA. */
+int nvfp4kv_check_device_errors(cudaStream_t stream);
+
+/* Static description of a status code. */
+const char *nvfp4kv_status_string(int status);
+
+/* Library ABI version (major * 100 + minor). */
+int nvfp4kv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NVFP4KV_H */

@@ -32,7 +32,8 @@
  *   KV head h / G (G = query heads per KV head).
  *
  * Pool layout (one slab per (page, kv_head), slabs ordered page-major):
- *   NVFP4: K codes [P][64] | K scales [P][8] | V codes [P][64] | V scales [P][8]
+ *   NVFP4: K codes [P][64] | K scales [P][8] | V codes [P][64] | V scales [8][P]
+ *          (K scales row-major, V scales block-major: block j of row t at [j][t])
  *   FP8  : K codes [P][128] | V codes [P][128]
  * Token t of a sequence lives in page block_table[t / P] at row t % P.
  *
@@ -219,10 +220,12 @@ static uint8_t *codes_row(const pool_t *p, uint8_t *slab, int which, int row)
     if (p->dtype == ORACLE_DTYPE_NVFP4) return slab + (which ? 72 * P : 0) + row * 64;
     return slab + (which ? 128 * P : 0) + row * 128;
 }
-static uint8_t *scales_row(const pool_t *p, uint8_t *slab, int which, int row)
+/* Scale byte of block `blk` of row `row`: K scales are [P][8], V scales [8][P]. */
+static uint8_t *scale_ptr(const pool_t *p, uint8_t *slab, int which, int row, int blk)
 {
     int P = p->page_size;
-    return slab + (which ? 136 * P : 64 * P) + row * 8;
+    if (which == 0) return slab + 64 * P + row * 8 + blk;
+    return slab + 136 * P + blk * P + row;
 }
 
 /* Dequantise one head_dim row of K or V into out[128] (double). */
@@ -232,11 +235,10 @@ static void dequant_row(const pool_t *p, int64_t page, int kv, int which, int ro
     uint8_t *c = codes_row(p, slab, which, row);
     float g = which ? p->gv : p->gk;
     if (p->dtype == ORACLE_DTYPE_NVFP4) {
-        uint8_t *s = scales_row(p, slab, which, row);
         for (int d = 0; d < HEAD_DIM; d++) {
             uint8_t byte = c[d / 2];
             uint8_t code = (d % 2 == 0) ? (byte & 15) : (byte >> 4);
-            out[d] = nvfp4_dequant(code, s[d / BLOCK], g);
+            out[d] = nvfp4_dequant(code, *scale_ptr(p, slab, which, row, d / BLOCK), g);
         }
     } else {
         for (int d = 0; d < HEAD_DIM; d++) out[d] = oracle_e4m3_value(c[d]) * (double)g;
@@ -254,10 +256,9 @@ static int store_row(const pool_t *p, int64_t page, int kv, int which, int row, 
     uint8_t *c = codes_row(p, slab, which, row);
     float g = which ? p->gv : p->gk;
     if (p->dtype == ORACLE_DTYPE_NVFP4) {
-        uint8_t *s = scales_row(p, slab, which, row);
         for (int b = 0; b < HEAD_DIM / BLOCK; b++) {
             uint8_t codes[BLOCK];
-            int rc = oracle_quantize_block16(x + b * BLOCK, g, codes, &s[b]);
+            int rc = oracle_quantize_block16(x + b * BLOCK, g, codes, scale_ptr(p, slab, which, row, b));
             if (rc) return rc;
             for (int i = 0; i < BLOCK / 2; i++)
                 c[b * 8 + i] = (uint8_t)(codes[2 * i] | (codes[2 * i + 1] << 4));

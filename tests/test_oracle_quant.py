@@ -126,8 +126,15 @@ def test_non_finite_input_rejected():
 
 def _layout_offsets(P):
     """The cache's documented layout: K codes [P][64], K scales [P][8],
-    V codes [P][64], V scales [P][8] per (page, kv_head) slab."""
+    V codes [P][64], V scales [8][P] (block-major) per (page, kv_head) slab."""
     return {"kq": 0, "ks": 64 * P, "vq": 72 * P, "vs": 136 * P}
+
+
+def _scale_index(P, name, row, blk):
+    off = _layout_offsets(P)
+    if name == "k":
+        return off["ks"] + row * 8 + blk
+    return off["vs"] + blk * P + row
 
 
 @pytest.mark.parametrize("P", [16, 64])
@@ -151,7 +158,7 @@ def test_append_places_rows_at_documented_offsets(P):
             slab = pool.data[page, h]
             for name, src in (("k", k[t, h]), ("v", v[t, h])):
                 q = slab[off[name + "q"] + row * 64: off[name + "q"] + row * 64 + 64]
-                s = slab[off[name + "s"] + row * 8: off[name + "s"] + row * 8 + 8]
+                s = [slab[_scale_index(P, name, row, j)] for j in range(8)]
                 vals = np.empty(128)
                 for d in range(128):
                     code = (q[d // 2] >> (4 * (d % 2))) & 15
@@ -166,7 +173,7 @@ def test_append_places_rows_at_documented_offsets(P):
                 slab = pool.data[page, h]
                 for name in ("k", "v"):
                     assert np.all(slab[off[name + "q"] + row * 64: off[name + "q"] + row * 64 + 64] == 0xAB)
-                    assert np.all(slab[off[name + "s"] + row * 8: off[name + "s"] + row * 8 + 8] == 0xAB)
+                    assert all(slab[_scale_index(P, name, row, j)] == 0xAB for j in range(8))
 
 
 def test_append_rejects_out_of_range_slot():
