@@ -1,0 +1,488 @@
+#!/usr/bin/env python
+"""Benchmark of the NVFP4 paged KV cache decode step on GB300.
+
+Workload (one GPU; N GPUs run N independent replicas): batch 64, every
+sequence 32,768 cached tokens, 64 query heads over 8 KV heads (GQA 8),
+head_dim 128, 64-token pages under a randomly permuted block table, K/V/Q
+drawn N(0,1) -- the 32K iso-concurrency shape of "Accelerating Long-Context
+and Agentic Inference with NVFP4 KV Cache" (A4, decode performance).
+
+One step = the whole hot path of a decode step: quantise-append of the new
+token of every sequence (64 tokens x 8 KV heads) into the paged cache, then
+paged GQA decode attention over all 32,768 tokens (plan, decode, split
+reduction).  The cache (2.42 GB) is far larger than L2, so no flush is needed
+between steps.
+
+value = HBM GB/s on algorithmic bytes (packed KV + scales + block table + Q +
+out, plus the append's BF16 reads and packed writes) / device time per step.
+roofline = the decode kernel alone, timed with CUDA events recorded around its
+launch on the launching stream, against the measured HBM copy bandwidth.
+
+`--impl reference` times the CPU oracle (fp64, all host cores) on a bounded
+sample of the same workload and prints the same JSON line with
+"impl": "reference".
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "NVFP4 paged decode-attn: HBM GB/s (% of GB300 peak), KV-tokens/s, µs/step"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=1000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-comparisons", action="store_true")
+    p.add_argument("--num-splits", type=int, default=0)
+    return p.parse_args()
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def peak_hbm():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def decode_bytes(batch, seq_len, hq, hkv, max_pages, dtype_bytes_per_token_head):
+    """Algorithmic bytes of one decode call: KV (+ scales) + block table + Q + out."""
+    kv = batch * seq_len * hkv * dtype_bytes_per_token_head
+    return kv + batch * max_pages * 4 + 2 * batch * hq * 128 * 2 + batch * 4
+
+
+def append_bytes(tokens, hkv, packed_bytes_per_token_head):
+    """Algorithmic bytes of one quantise-append: BF16 K/V in, packed rows out, slots."""
+    return tokens * hkv * 2 * 128 * 2 + tokens * hkv * packed_bytes_per_token_head + tokens * 8
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons in the background."""
+
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, gpu_id):
+        self.samples = []
+        self.proc = None
+        try:
+            cmd = ["nvidia-smi", "--query-gpu=" + ",".join(self.FIELDS), "--format=csv,noheader,nounits",
+                   "-lms", "50"]
+            if gpu_id:
+                cmd += ["-i", gpu_id]
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        rows = [s for (t, s) in self.samples if t0 <= t <= t1 and len(s) == len(self.FIELDS)]
+        note = "samples inside the timed region"
+        if not rows:  # timed region shorter than the sampling period: take the nearest samples
+            near = sorted(self.samples, key=lambda ts: min(abs(ts[0] - t0), abs(ts[0] - t1)))
+            rows = [s for (_, s) in near[:3] if len(s) == len(self.FIELDS)]
+            note = "nearest samples (timed region shorter than the 50 ms sampling period)"
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "note": "nvidia-smi unavailable"}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = sorted(v for v in (num(r[0]) for r in rows) if v is not None)
+        mx = [v for v in (num(r[1]) for r in rows) if v is not None]
+        reasons = set()
+        for r in rows:
+            for name, val in zip(["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"],
+                                 r[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(rows), "note": note}
+
+
+def decode_kernel_traffic():
+    """DRAM bytes per decode-kernel launch from the committed ncu summary, if it
+    was taken on the current kernel source (else None)."""
+    src = os.path.join(ROOT, "nvfp4_quantised_paged_gb300", "csrc", "decode_attention.cu")
+    summ = os.path.join(ROOT, "profiles", "decode_kernel_dram.txt")
+    try:
+        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        kv = {}
+        for line in open(summ):
+            if ":" in line and not line.startswith("#"):
+                k, v = line.split(":", 1)
+                kv[k.strip()] = v.strip()
+        if kv.get("kernel_source_sha256_16") == h:
+            return float(kv["dram_bytes_per_launch_full_size"])
+    except Exception:
+        pass
+    return None
+
+
+def init_dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+        return world, rank, local, dist
+    return 1, 0, 0, None
+
+
+def max_over_ranks(dist, x):
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+# ----------------------------------------------------------------------------- CPU oracle leg
+
+def oracle_decode_sample(w, nseq, seed_device="cpu"):
+    """Builds the oracle's own pool for the first `nseq` sequences of the
+    workload (untimed) and returns a callable running one oracle decode over
+    them, plus the algorithmic bytes that call covers."""
+    import numpy as np
+    import torch
+
+    import oracle
+
+    seqs = list(range(nseq))
+    pages = sorted({int(p) for b in seqs for p in w.block_table[b].tolist() if p >= 0})
+    remap = {p: i for i, p in enumerate(pages)}
+    bt = w.block_table[seqs].clone()
+    bt = torch.tensor([[remap[int(p)] if p >= 0 else -1 for p in row] for row in bt.tolist()], dtype=torch.int32)
+    pool = oracle.OraclePool(len(pages), w.page_size, w.num_kv_heads)
+
+    def bits(t):
+        return t.contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+
+    for b in seqs:
+        k, v = w.seq_kv(b, seed_device)
+        t = torch.arange(int(w.seq_lens[b]))
+        slots = bt[b].to(torch.int64)[t // w.page_size] * w.page_size + t % w.page_size
+        oracle.quantize_append(pool, bits(k), bits(v), slots.numpy())
+    q = bits(w.q(seed_device)[:nseq])
+    sl = w.seq_lens[:nseq].numpy()
+    cores = os.cpu_count() or 1
+
+    def run():
+        return oracle.decode_attention(pool, q, bt.numpy(), sl, w.sm_scale, nthreads=cores)
+
+    nbytes = decode_bytes(nseq, int(w.seq_lens[0]), w.num_q_heads, w.num_kv_heads, w.max_pages, 144)
+    return run, nbytes, cores
+
+
+def cpu_baseline(w, seed_device):
+    cores = os.cpu_count() or 1
+    nseq = max(1, min(w.batch, math.ceil(cores / w.num_kv_heads)))
+    run, nbytes, cores = oracle_decode_sample(w, nseq, seed_device)
+    run()  # warm
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        run()
+        reps += 1
+        if time.perf_counter() - t0 > 10.0:
+            break
+    dt = (time.perf_counter() - t0) / reps
+    return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": "%d of %d sequences (%d (seq, kv_head) units of %d tokens), fp64 decode over the oracle's "
+                      "own NVFP4 pool, %d repetitions" % (nseq, w.batch, nseq * w.num_kv_heads,
+                                                          int(w.seq_lens[0]), reps),
+            "ms_per_sample": dt * 1e3}
+
+
+def run_reference(args):
+    import workloads
+    world, rank, local, dist = init_dist()
+    if rank != 0:
+        return
+    w = workloads.decode_32k()
+    cores = os.cpu_count() or 1
+    nseq = max(1, min(w.batch, math.ceil(cores / w.num_kv_heads)))
+    run, nbytes, cores = oracle_decode_sample(w, nseq, "cpu")
+    for _ in range(max(0, args.warmup)):
+        run()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        run()
+    dt = (time.perf_counter() - t0) / max(1, args.steps)
+    value = nbytes / dt / 1e9
+    sample = "%d of %d sequences x %d KV heads per step (%d tokens each), fp64 oracle decode on %d host threads" % (
+        nseq, w.batch, w.num_kv_heads, int(w.seq_lens[0]), cores)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "sample": sample},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- GPU leg
+
+def fill_cache(m, w, cache, device):
+    for b in range(w.batch):
+        k, v = w.seq_kv(b, device)
+        m.quantize_append(cache, k, v, w.slots(b).to(device))
+        del k, v
+
+
+def time_decode_only(m, w, dtype, device, steps, warmup):
+    """Decode-kernel time (µs) for workload w over a cache of `dtype` (used for the
+    FP8 byte-ratio comparison and the long-context workload)."""
+    import torch
+    cache = m.PagedCache(w.num_pages, w.page_size, w.num_kv_heads, dtype=dtype, device=device)
+    fill_cache(m, w, cache, device)
+    q = w.q(device)
+    bt, sl = w.block_table.to(device), w.seq_lens.to(device)
+    ws = m.alloc_decode_workspace(cache, w.batch, w.num_q_heads)
+    out = torch.empty_like(q)
+    for _ in range(warmup):
+        m.paged_decode_attention(cache, q, bt, sl, w.sm_scale, out=out, workspace=ws)
+    before = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    after = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    m.profile_decode(before, after)
+    torch.cuda.synchronize()
+    for _ in range(steps):
+        m.paged_decode_attention(cache, q, bt, sl, w.sm_scale, out=out, workspace=ws)
+    torch.cuda.synchronize()
+    m.profile_decode([], [])
+    assert m.check_device_errors() == 0
+    us = sum(b.elapsed_time(a) for b, a in zip(before, after)) / steps * 1e3
+    del cache
+    torch.cuda.empty_cache()
+    return us
+
+
+def time_append(m, device, steps, warmup):
+    import torch
+
+    import workloads
+    w = workloads.append_65k()
+    cache = m.PagedCache(w.num_pages, w.page_size, w.num_kv_heads, device=device)
+    k, v = w.kv(device)
+    slots = w.slot_mapping().to(device)
+    for _ in range(warmup):
+        m.quantize_append(cache, k, v, slots)
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    s.record()
+    for _ in range(steps):
+        m.quantize_append(cache, k, v, slots)
+    e.record()
+    torch.cuda.synchronize()
+    us = s.elapsed_time(e) / steps * 1e3
+    nbytes = append_bytes(w.num_tokens, w.num_kv_heads, 144)
+    return {"workload": w.name, "us_per_call": us, "gb_per_s": nbytes / us / 1e3, "algorithmic_bytes": nbytes,
+            "note": "inputs 268 MB > L2 is false (129 MB L2 holds part): back-to-back calls"}
+
+
+def run_ours(args):
+    import torch
+
+    import nvfp4_quantised_paged_gb300 as m
+    import workloads
+
+    world, rank, local, dist = init_dist()
+    torch.cuda.set_device(local)
+    device = "cuda:%d" % local
+    w = workloads.decode_32k()
+    B, S, Hq, Hkv, P = w.batch, int(w.seq_lens[0]), w.num_q_heads, w.num_kv_heads, w.page_size
+
+    cache = m.PagedCache(w.num_pages, P, Hkv, device=device)
+    fill_cache(m, w, cache, device)
+    q = w.q(device)
+    bt, sl = w.block_table.to(device), w.seq_lens.to(device)
+    # the step's new token of every sequence goes to position S-1
+    g = torch.Generator(device=device)
+    g.manual_seed(4242)
+    new_k = torch.randn((B, Hkv, 128), generator=g, device=device).to(torch.bfloat16)
+    new_v = torch.randn((B, Hkv, 128), generator=g, device=device).to(torch.bfloat16)
+    new_slots = torch.cat([w.slots(b, S - 1, S) for b in range(B)]).to(device)
+    ws = m.alloc_decode_workspace(cache, B, Hq, args.num_splits)
+    out = torch.empty_like(q)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        m.quantize_append(cache, new_k, new_v, new_slots)
+        m.paged_decode_attention(cache, q, bt, sl, w.sm_scale, out=out, workspace=ws, num_splits=args.num_splits)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    assert m.check_device_errors() == 0
+
+    K = args.steps
+    before = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    after = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(local).uuid)
+    except Exception:
+        pass
+    sampler = ClockSampler(uuid)
+    time.sleep(0.3)
+    m.profile_decode(before, after)
+    barrier(dist)
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    ev0.record(stream)
+    for _ in range(K):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    barrier(dist)
+    m.profile_decode([], [])
+    time.sleep(0.1)
+    sampler.stop()
+    assert m.check_device_errors() == 0
+    ms_step = max_over_ranks(dist, ev0.elapsed_time(ev1) / K)
+    dec_us = max_over_ranks(dist, sum(b.elapsed_time(a) for b, a in zip(before, after)) / K * 1e3)
+
+    dbytes = decode_bytes(B, S, Hq, Hkv, w.max_pages, 144)
+    abytes = append_bytes(B, Hkv, 144)
+    step_bytes = dbytes + abytes
+    value = world * step_bytes / (ms_step * 1e-3) / 1e9
+    kv_tokens_per_s = world * B * S / (ms_step * 1e-3)
+
+    # ---- end to end through the public API with host buffers
+    q_h = q.cpu().pin_memory()
+    k_h, v_h = new_k.cpu().pin_memory(), new_v.cpu().pin_memory()
+    s_h = new_slots.cpu().pin_memory()
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    q_d, k_d, v_d, s_d = torch.empty_like(q), torch.empty_like(new_k), torch.empty_like(new_v), torch.empty_like(new_slots)
+
+    def e2e_step():
+        q_d.copy_(q_h, non_blocking=True)
+        k_d.copy_(k_h, non_blocking=True)
+        v_d.copy_(v_h, non_blocking=True)
+        s_d.copy_(s_h, non_blocking=True)
+        m.quantize_append(cache, k_d, v_d, s_d)
+        m.paged_decode_attention(cache, q_d, bt, sl, w.sm_scale, out=out, workspace=ws, num_splits=args.num_splits)
+        out_h.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    barrier(dist)
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    for _ in range(K):
+        e2e_step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(dist, ev0.elapsed_time(ev1) / K)
+    h2d = q.numel() * 2 + new_k.numel() * 2 * 2 + new_slots.numel() * 8
+    d2h = out.numel() * 2
+
+    peak, peak_kind = peak_hbm()
+    achieved = dbytes / (dec_us * 1e-6) / 1e9
+    traffic = decode_kernel_traffic()
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f16xf16->f32", "data": "synthetic",
+        "config": {"workload": w.name, "batch": B, "seq_len": S, "num_q_heads": Hq, "num_kv_heads": Hkv,
+                   "head_dim": 128, "page_size": P, "kv_cache": "nvfp4 (e2m1 + e4m3 per 16, tensor scale 1.0)",
+                   "step": "quantize-append of 1 new token per sequence + paged decode attention",
+                   "l2": "inputs larger than L2 (2.42 GB cache vs 129 MB L2), no flush",
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "num_splits": args.num_splits or m.decode_auto_splits(cache, Hq)},
+        "us_per_step": ms_step * 1e3, "kv_tokens_per_s": kv_tokens_per_s,
+        "pct_of_nominal_8tbps": 100.0 * (value / world) / NOMINAL_HBM_GBS,
+        "pct_of_measured_hbm": 100.0 * (value / world) / peak,
+        "algorithmic_bytes_per_step": step_bytes,
+        "e2e": {"value": world * step_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": 4 * K,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic, "peak_kind": peak_kind,
+                     "kernel": "decode_kernel<nvfp4>", "us_per_launch": dec_us,
+                     "algorithmic_bytes_per_launch": dbytes},
+        "clocks": sampler.summary(t_wall0, t_wall1),
+    }
+
+    if not args.no_comparisons and rank == 0:
+        comp = {}
+        del cache
+        torch.cuda.empty_cache()
+        fp8_us = time_decode_only(m, w, 1, device, 100, 5)
+        comp["fp8_e4m3_cache_same_workload"] = {
+            "decode_us": fp8_us, "nvfp4_decode_us": dec_us, "nvfp4_over_fp8_time": dec_us / fp8_us,
+            "fp8_gb_per_s": decode_bytes(B, S, Hq, Hkv, w.max_pages, 256) / fp8_us / 1e3,
+            "kv_byte_ratio": 144 / 256}
+        w4 = workloads.decode_1m()
+        us4 = time_decode_only(m, w4, 0, device, 50, 5)
+        b4 = decode_bytes(w4.batch, int(w4.seq_lens[0]), w4.num_q_heads, w4.num_kv_heads, w4.max_pages, 144)
+        comp["decode_1m"] = {"workload": w4.name, "decode_us": us4, "gb_per_s": b4 / us4 / 1e3,
+                             "pct_of_measured_hbm": 100.0 * b4 / us4 / 1e3 / peak,
+                             "kv_tokens_per_s": 2 * 1048576 / (us4 * 1e-6)}
+        comp["append_65k"] = time_append(m, device, 50, 5)
+        line["comparisons"] = comp
+
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, device)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

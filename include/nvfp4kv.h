@@ -58,6 +58,12 @@
 
 #include <cuda_runtime_api.h>
 
+#if defined(__GNUC__)
+#define NVFP4KV_API __attribute__((visibility("default")))
+#else
+#define NVFP4KV_API
+#endif
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -90,10 +96,10 @@ typedef struct {
 
 /* Bytes of one (page, kv_head) slab: 144*P (NVFP4) or 256*P (FP8); 0 if the
  * descriptor is invalid. */
-size_t nvfp4kv_slab_bytes(const nvfp4kv_cache *cache);
+NVFP4KV_API size_t nvfp4kv_slab_bytes(const nvfp4kv_cache *cache);
 
 /* Bytes of the whole pool (num_pages * num_kv_heads * slab); 0 if invalid. */
-size_t nvfp4kv_pool_bytes(const nvfp4kv_cache *cache);
+NVFP4KV_API size_t nvfp4kv_pool_bytes(const nvfp4kv_cache *cache);
 
 /*
  * Quantise BF16 K and V rows and write them into the pool.
@@ -116,16 +122,16 @@ size_t nvfp4kv_pool_bytes(const nvfp4kv_cache *cache);
  * in one call is a caller error (the result is one of the two rows).
  * num_tokens == 0 is a no-op.
  */
-int nvfp4_kv_quantize_append(const nvfp4kv_cache *cache, const void *k, const void *v, int64_t num_tokens,
+NVFP4KV_API int nvfp4_kv_quantize_append(const nvfp4kv_cache *cache, const void *k, const void *v, int64_t num_tokens,
                              int64_t token_stride, const int64_t *slot_mapping, cudaStream_t stream);
 
 /* Workspace bytes nvfp4_paged_decode_attention needs for this shape and
  * num_splits on the current device (0 if the arguments are invalid). */
-size_t nvfp4kv_decode_workspace_bytes(const nvfp4kv_cache *cache, int batch, int num_q_heads, int num_splits);
+NVFP4KV_API size_t nvfp4kv_decode_workspace_bytes(const nvfp4kv_cache *cache, int batch, int num_q_heads, int num_splits);
 
 /* Number of work partitions an auto-split (num_splits = 0) call uses on the
  * current device for this cache. */
-int nvfp4kv_decode_auto_splits(const nvfp4kv_cache *cache, int num_q_heads);
+NVFP4KV_API int nvfp4kv_decode_auto_splits(const nvfp4kv_cache *cache, int num_q_heads);
 
 /*
  * Paged GQA decode attention over the cache, one query token per sequence.
@@ -149,7 +155,7 @@ int nvfp4kv_decode_auto_splits(const nvfp4kv_cache *cache, int num_q_heads);
  * over t < seq_lens[b], with k_t, v_t the dequantised cache rows.  A sequence
  * of length 0 yields zeros.
  */
-int nvfp4_paged_decode_attention(const nvfp4kv_cache *cache, const void *q, int batch, int num_q_heads,
+NVFP4KV_API int nvfp4_paged_decode_attention(const nvfp4kv_cache *cache, const void *q, int batch, int num_q_heads,
                                  const int32_t *block_table, int max_pages_per_seq, const int32_t *seq_lens,
                                  float sm_scale, void *out, void *workspace, size_t workspace_bytes, int num_splits,
                                  cudaStream_t stream);
@@ -170,20 +176,28 @@ int nvfp4_paged_decode_attention(const nvfp4kv_cache *cache, const void *q, int 
  *                   request r:  value = e2m1 * e4m3 * g, rounded to BF16
  *                   (exact for g = 1).
  */
-int nvfp4_prefix_dequant(const nvfp4kv_cache *cache, const int32_t *block_table, int max_pages_per_seq,
+NVFP4KV_API int nvfp4_prefix_dequant(const nvfp4kv_cache *cache, const int32_t *block_table, int max_pages_per_seq,
                          const int32_t *prefix_lens, const int32_t *cu_prefix_lens, int num_reqs,
                          int64_t total_prefix_tokens, void *k_ws, void *v_ws, cudaStream_t stream);
 
 /* Synchronises `stream`, then reads and clears the current device's error
  * word.  Returns NVFP4KV_OK, NVFP4KV_EDEVICE_CHECK (some kernel skipped an
  * out-of-range index since the last check) or NVFP4KV_ECUDA. */
-int nvfp4kv_check_device_errors(cudaStream_t stream);
+NVFP4KV_API int nvfp4kv_check_device_errors(cudaStream_t stream);
+
+/* Benchmark hook: while enabled, the i-th nvfp4_paged_decode_attention call
+ * records before[i % count] on its stream immediately before launching the
+ * decode kernel and after[i % count] immediately after it, so the caller can
+ * time that kernel alone with cudaEventElapsedTime.  The events are created
+ * and owned by the caller; count = 0 (or NULL arrays) disables the hook and
+ * resets i.  Process-wide and not thread-safe: for benchmarks only. */
+NVFP4KV_API int nvfp4kv_profile_decode(const cudaEvent_t *before, const cudaEvent_t *after, int count);
 
 /* Static description of a status code. */
-const char *nvfp4kv_status_string(int status);
+NVFP4KV_API const char *nvfp4kv_status_string(int status);
 
 /* Library ABI version (major * 100 + minor). */
-int nvfp4kv_version(void);
+NVFP4KV_API int nvfp4kv_version(void);
 
 #ifdef __cplusplus
 }

@@ -1,0 +1,888 @@
+// decode_attention.cu -- paged GQA decode attention that dequantises the cache on chip.
+//
+// Source: "Accelerating Long-Context and Agentic Inference with NVFP4 KV
+// Cache", section A2, path 3 and Fig. 3: packed K/V tiles and their E4M3 block
+// scales are staged in shared memory, unpacked to 16-bit floats in registers,
+// multiplied by the scales with packed multiplies, and fed to the matrix
+// products; the FP32 tensor scales are applied as scaling of those products.
+// Dequantised KV never goes back to HBM.
+//
+// GB300 design (not the page's SM120 kernel):
+//   * Work split.  The KV of every (sequence, kv_head) pair is cut into
+//     64-token chunks; all chunks of all pairs form one flat range that is cut
+//     into `grid` equal contiguous pieces, one per CTA (grid = SM count x
+//     resident CTAs for an auto split).  A CTA therefore streams an equal
+//     number of bytes whatever the mix of sequence lengths.  A pair covered by
+//     one CTA gets its output written directly; a pair spread over several CTAs
+//     leaves one (max, sum, acc) partial per CTA, merged by a separate
+//     log-sum-exp reduction kernel.
+//   * Staging.  One thread issues 1-D bulk (TMA) copies of each 64-token chunk
+//     (9,216 bytes for NVFP4) into a 4-stage shared-memory ring, completion
+//     tracked by mbarriers; every wait is bounded and reports a timeout in the
+//     device error word instead of spinning forever.
+//   * Tensor cores on the real contraction only: per warp and 16 tokens,
+//     S^T (16 tokens x 8 query heads of the group) = K Q^T and
+//     O^T (128 dims x 8 heads) += V^T P^T with mma.sync m16n8k16, FP16 inputs
+//     and FP32 accumulation.  Tokens sit on the M dimension, so a GQA group of
+//     up to 8 heads fills N = 8 with no padding; groups of 9-16 use two N tiles.
+//   * Unpack.  ptxas for sm_103a accepts cvt.rn.f16x2.e2m1x2 (not the BF16
+//     form), so values are unpacked to FP16.  Every e2m1 x e4m3 product is an
+//     FP16 normal with <= 6 significant bits, so the scaled values are exact.
+//     Q is converted to FP16 after a per-head power-of-two pre-scale (exact for
+//     every element above 2^-29 of the head's largest), undone in the score scale.
+//   * V operand order.  The P.V product needs, per register, two consecutive
+//     tokens of one channel; the cache stores two consecutive channels of one
+//     token per byte.  Two lop3/shift pairs per 8 bytes swap nibbles between
+//     the two tokens before the conversion, and the V scales (stored
+//     block-major) arrive as the matching token pair.
+//   * Softmax in base 2 with a lazily updated running max: the accumulators are
+//     rescaled only when some score exceeds the running max by more than 2^8,
+//     so most tiles skip the cross-lane max and the rescale.
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace nvfp4kv {
+
+namespace {
+
+constexpr int kWarps = 4;
+constexpr int kThreads = 32 * kWarps;
+constexpr int kStages = 4;
+constexpr int kChunk = 64;                 // tokens per pipeline stage
+constexpr uint32_t kWaitLimit = 1u << 24;  // polls before a wait gives up (>= ~1 s)
+constexpr float kRescaleLog2 = 8.0f;
+constexpr float kNegInf = -__builtin_huge_valf();
+
+template <int DTYPE>
+struct Layout;
+template <>
+struct Layout<NVFP4KV_DTYPE_NVFP4> {  // canonical 64-token stage
+    static constexpr int kStageBytes = 9216;
+    static constexpr int kKq = 0, kKs = 4096, kVq = 4608, kVs = 8704;
+};
+template <>
+struct Layout<NVFP4KV_DTYPE_FP8_E4M3> {
+    static constexpr int kStageBytes = 16384;
+    static constexpr int kKq = 0, kVq = 8192;
+};
+
+template <int DTYPE, int NT>
+struct Smem {
+    static constexpr int kStageBytes = Layout<DTYPE>::kStageBytes;
+    static constexpr int kMergeO = kStages * kStageBytes;                 // float [kWarps][NT*8][128]
+    static constexpr int kMergeML = kMergeO + kWarps * NT * 8 * 128 * 4;  // float2 [kWarps][NT*8]
+    static constexpr int kBars = kMergeML + kWarps * NT * 8 * 8;          // u64 full[kStages], empty[kStages]
+    static constexpr int kFlags = kBars + 2 * kStages * 8;                // int valid[kStages], abort
+    static constexpr int kTotal = kFlags + (kStages + 4) * 4;
+};
+
+struct DecodeArgs {
+    const uint8_t *pool;
+    int64_t num_pages;
+    int P, log2P;
+    int Hkv, G, Hq, B, max_pages;
+    int64_t slab;
+    const uint4 *q;
+    const int32_t *block_table;
+    const int32_t *seq_lens;
+    const int64_t *chunk_prefix;  // [B + 1], chunks of 64 tokens per sequence (exclusive scan)
+    float score_log2;             // sm_scale * g_K * log2(e)
+    float gv;
+    __nv_bfloat16 *out;
+    float *part_acc;  // [slots][G][128]
+    float2 *part_ml;  // [slots][G]
+    int grid;
+    unsigned *err;
+};
+
+__device__ __forceinline__ int clamp_len(int32_t n, int64_t cap) {
+    if (n < 0) return 0;
+    return (int64_t)n > cap ? (int)cap : n;
+}
+
+struct Cursor {
+    int b, kv, n;
+    int64_t chunk, nchunks;
+};
+
+__device__ __forceinline__ void cursor_load_seq(Cursor &cu, const DecodeArgs &a) {
+    cu.nchunks = a.chunk_prefix[cu.b + 1] - a.chunk_prefix[cu.b];
+    cu.n = clamp_len(a.seq_lens[cu.b], (int64_t)a.max_pages * a.P);
+}
+
+__device__ __forceinline__ void cursor_advance(Cursor &cu, const DecodeArgs &a) {
+    if (++cu.chunk < cu.nchunks) return;
+    cu.chunk = 0;
+    if (++cu.kv < a.Hkv) return;
+    cu.kv = 0;
+    do {
+        ++cu.b;
+    } while (cu.b < a.B && a.chunk_prefix[cu.b + 1] == a.chunk_prefix[cu.b]);
+    if (cu.b < a.B) cursor_load_seq(cu, a);
+}
+
+// Block-table entries of the pages behind the stage at `cu` (-2 = not needed).
+__device__ __forceinline__ void load_pages(const DecodeArgs &a, const Cursor &cu, int32_t (&pg)[4]) {
+    const int32_t *row = a.block_table + (int64_t)cu.b * a.max_pages;
+    const int64_t tok0 = cu.chunk * kChunk;
+    if (a.P >= kChunk) {
+        pg[0] = __ldg(row + (tok0 >> a.log2P));
+        pg[1] = pg[2] = pg[3] = -2;
+    } else {
+        const int np = kChunk >> a.log2P;
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+            const int64_t t = tok0 + ((int64_t)j << a.log2P);
+            pg[j] = (j < np && t < cu.n) ? __ldg(row + (t >> a.log2P)) : -2;
+        }
+    }
+}
+
+// Producer: stage `cu` into `stage` (thread 0 only).
+template <int DTYPE>
+__device__ __forceinline__ void issue_stage(const DecodeArgs &a, const Cursor &cu, const int32_t (&pg)[4],
+                                            uint8_t *stage, uint64_t *full, int *valid) {
+    bool ok = true;
+#pragma unroll
+    for (int j = 0; j < 4; j++)
+        if (pg[j] != -2 && (pg[j] < 0 || (int64_t)pg[j] >= a.num_pages)) ok = false;
+    if (!ok) {
+        flag_error(a.err, kErrPage);
+        *valid = 0;
+        mbar_arrive(full);
+        return;
+    }
+    *valid = 1;
+    const int P = a.P;
+    if (P == kChunk) {
+        const uint8_t *src = a.pool + ((int64_t)pg[0] * a.Hkv + cu.kv) * a.slab;
+        mbar_arrive_expect_tx(full, (uint32_t)a.slab);
+        bulk_g2s(stage, src, (uint32_t)a.slab, full);
+        return;
+    }
+    if (DTYPE == NVFP4KV_DTYPE_NVFP4) {
+        using L = Layout<NVFP4KV_DTYPE_NVFP4>;
+        if (P > kChunk) {  // P = 128: half a page
+            const int h = (int)(cu.chunk & 1);
+            const uint8_t *s = a.pool + ((int64_t)pg[0] * a.Hkv + cu.kv) * a.slab;
+            mbar_arrive_expect_tx(full, L::kStageBytes);
+            bulk_g2s(stage + L::kKq, s + h * 4096, 4096, full);
+            bulk_g2s(stage + L::kKs, s + 64 * P + h * 512, 512, full);
+            bulk_g2s(stage + L::kVq, s + 72 * P + h * 4096, 4096, full);
+#pragma unroll
+            for (int j = 0; j < 8; j++) bulk_g2s(stage + L::kVs + j * 64, s + 136 * P + j * P + h * 64, 64, full);
+        } else {  // P = 16 or 32: 64 / P pages
+            const int np = kChunk / P;
+            uint32_t bytes = 0;
+            for (int j = 0; j < np; j++)
+                if (pg[j] >= 0) bytes += 144u * P;
+            mbar_arrive_expect_tx(full, bytes);
+            for (int j = 0; j < np; j++) {
+                if (pg[j] < 0) continue;
+                const uint8_t *s = a.pool + ((int64_t)pg[j] * a.Hkv + cu.kv) * a.slab;
+                bulk_g2s(stage + L::kKq + j * 64 * P, s, 64 * P, full);
+                bulk_g2s(stage + L::kKs + j * 8 * P, s + 64 * P, 8 * P, full);
+                bulk_g2s(stage + L::kVq + j * 64 * P, s + 72 * P, 64 * P, full);
+                bulk_g2s(stage + L::kVs + j * 8 * P, s + 136 * P, 8 * P, full);
+            }
+        }
+    } else {
+        using L = Layout<NVFP4KV_DTYPE_FP8_E4M3>;
+        if (P > kChunk) {
+            const int h = (int)(cu.chunk & 1);
+            const uint8_t *s = a.pool + ((int64_t)pg[0] * a.Hkv + cu.kv) * a.slab;
+            mbar_arrive_expect_tx(full, L::kStageBytes);
+            bulk_g2s(stage + L::kKq, s + h * 8192, 8192, full);
+            bulk_g2s(stage + L::kVq, s + 128 * P + h * 8192, 8192, full);
+        } else {
+            const int np = kChunk / P;
+            uint32_t bytes = 0;
+            for (int j = 0; j < np; j++)
+                if (pg[j] >= 0) bytes += 256u * P;
+            mbar_arrive_expect_tx(full, bytes);
+            for (int j = 0; j < np; j++) {
+                if (pg[j] < 0) continue;
+                const uint8_t *s = a.pool + ((int64_t)pg[j] * a.Hkv + cu.kv) * a.slab;
+                bulk_g2s(stage + L::kKq + j * 128 * P, s, 128 * P, full);
+                bulk_g2s(stage + L::kVq + j * 128 * P, s + 128 * P, 128 * P, full);
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// Q fragments of one (sequence, kv_head): lane (g, c) holds head nt*8+g,
+// channels 32c .. 32c+31 as the B operand of the 8 k-steps (k-step j covers
+// channels 32c+4j .. 32c+4j+3 of every lane c); fac = score scale per head of
+// the lane's S columns (heads nt*8 + 2c, +1), including the undo of the
+// power-of-two pre-scale.
+template <int NT>
+__device__ __forceinline__ void load_q(const DecodeArgs &a, int b, int kv, int lane, uint32_t (&qf)[NT][8][2],
+                                       float (&fac)[NT][2]) {
+    const int g = lane >> 2, c = lane & 3;
+#pragma unroll
+    for (int nt = 0; nt < NT; nt++) {
+        const int head = nt * 8 + g;
+        uint32_t w[16];
+        if (head < a.G) {
+            const uint4 *src = a.q + ((int64_t)b * a.Hq + (int64_t)kv * a.G + head) * (kHeadDim / 8) + c * 4;
+#pragma unroll
+            for (int k = 0; k < 4; k++) {
+                const uint4 v = __ldg(src + k);
+                w[4 * k] = v.x;
+                w[4 * k + 1] = v.y;
+                w[4 * k + 2] = v.z;
+                w[4 * k + 3] = v.w;
+            }
+        } else {
+#pragma unroll
+            for (int k = 0; k < 16; k++) w[k] = 0u;
+        }
+        uint32_t m = 0;
+#pragma unroll
+        for (int k = 0; k < 16; k++) m = __vmaxu2(m, w[k] & 0x7fff7fffu);
+        m = max(m >> 16, m & 0xffffu);
+        m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
+        m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
+        // pre-scale 2^kq puts the head's largest |q| in [2^14, 2^15)
+        int kq = 0;
+        if (m != 0) {
+            const int e = (int)((m >> 7) & 0xff) - 127;  // exponent of the BF16 amax (subnormal -> -127)
+            kq = min(126, max(-126, 14 - e));
+        }
+        const float s = __uint_as_float((uint32_t)(kq + 127) << 23);
+#pragma unroll
+        for (int j = 0; j < 8; j++) {
+            qf[nt][j][0] = f32x2_to_f16x2(bf16_hi(w[2 * j]) * s, bf16_lo(w[2 * j]) * s);
+            qf[nt][j][1] = f32x2_to_f16x2(bf16_hi(w[2 * j + 1]) * s, bf16_lo(w[2 * j + 1]) * s);
+        }
+        const int kq0 = __shfl_sync(0xffffffffu, kq, 8 * c);
+        const int kq1 = __shfl_sync(0xffffffffu, kq, 8 * c + 4);
+        fac[nt][0] = a.score_log2 * __uint_as_float((uint32_t)(127 - kq0) << 23);
+        fac[nt][1] = a.score_log2 * __uint_as_float((uint32_t)(127 - kq1) << 23);
+    }
+}
+
+// Online softmax on one 16-token S^T tile (rows g, g+8 of the lane; columns =
+// heads nt*8+2c, +1), then the P^T operand for the P.V product.
+template <int NT>
+__device__ __forceinline__ void softmax_tile(float (&s)[NT][4], int g, int vt, const float (&fac)[NT][2],
+                                             float (&m_run)[NT][2], float (&l_run)[NT][2], float (&o)[NT][8][4],
+                                             uint32_t (&pb)[NT][2]) {
+    bool need = false;
+#pragma unroll
+    for (int nt = 0; nt < NT; nt++) {
+        s[nt][0] *= fac[nt][0];
+        s[nt][1] *= fac[nt][1];
+        s[nt][2] *= fac[nt][0];
+        s[nt][3] *= fac[nt][1];
+        if (vt < 16) {
+            if (g >= vt) s[nt][0] = s[nt][1] = kNegInf;
+            if (g + 8 >= vt) s[nt][2] = s[nt][3] = kNegInf;
+        }
+        need |= fmaxf(s[nt][0], s[nt][2]) > m_run[nt][0] + kRescaleLog2;
+        need |= fmaxf(s[nt][1], s[nt][3]) > m_run[nt][1] + kRescaleLog2;
+    }
+    if (__any_sync(0xffffffffu, need)) {
+#pragma unroll
+        for (int nt = 0; nt < NT; nt++) {
+            float t0 = fmaxf(s[nt][0], s[nt][2]), t1 = fmaxf(s[nt][1], s[nt][3]);
+#pragma unroll
+            for (int x = 4; x < 32; x <<= 1) {
+                t0 = fmaxf(t0, __shfl_xor_sync(0xffffffffu, t0, x));
+                t1 = fmaxf(t1, __shfl_xor_sync(0xffffffffu, t1, x));
+            }
+            const float n0 = fmaxf(m_run[nt][0], t0), n1 = fmaxf(m_run[nt][1], t1);
+            const float a0 = ex2(m_run[nt][0] - n0), a1 = ex2(m_run[nt][1] - n1);
+            m_run[nt][0] = n0;
+            m_run[nt][1] = n1;
+            l_run[nt][0] *= a0;
+            l_run[nt][1] *= a1;
+#pragma unroll
+            for (int i = 0; i < 8; i++) {
+                o[nt][i][0] *= a0;
+                o[nt][i][1] *= a1;
+                o[nt][i][2] *= a0;
+                o[nt][i][3] *= a1;
+            }
+        }
+    }
+#pragma unroll
+    for (int nt = 0; nt < NT; nt++) {
+        const float p0 = ex2(s[nt][0] - m_run[nt][0]), p1 = ex2(s[nt][1] - m_run[nt][1]);
+        const float p2 = ex2(s[nt][2] - m_run[nt][0]), p3 = ex2(s[nt][3] - m_run[nt][1]);
+        l_run[nt][0] += p0 + p2;
+        l_run[nt][1] += p1 + p3;
+        pb[nt][0] = movmatrix_trans(f32x2_to_f16x2(p1, p0));
+        pb[nt][1] = movmatrix_trans(f32x2_to_f16x2(p3, p2));
+    }
+}
+
+// One warp, one 16-token tile of an NVFP4 stage.  vt = valid rows (1..16).
+template <int NT>
+__device__ __forceinline__ void tile_nvfp4(const uint8_t *st, int r0, int vt, int log2Pc, int lane,
+                                           const uint32_t (&qf)[NT][8][2], const float (&fac)[NT][2],
+                                           float (&m_run)[NT][2], float (&l_run)[NT][2], float (&o)[NT][8][4]) {
+    using L = Layout<NVFP4KV_DTYPE_NVFP4>;
+    const int g = lane >> 2, c = lane & 3;
+    // ---- S^T = K Q^T.  Lane loads channels 32c..32c+31 (16 bytes) of rows g, g+8.
+    const uint4 kA = *reinterpret_cast<const uint4 *>(st + L::kKq + (r0 + g) * 64 + 16 * c);
+    const uint4 kB = *reinterpret_cast<const uint4 *>(st + L::kKq + (r0 + g + 8) * 64 + 16 * c);
+    const uint32_t sA = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t *>(st + L::kKs + (r0 + g) * 8 + 2 * c));
+    const uint32_t sB =
+        e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t *>(st + L::kKs + (r0 + g + 8) * 8 + 2 * c));
+    const uint32_t sA_lo = __byte_perm(sA, 0, 0x1010), sA_hi = __byte_perm(sA, 0, 0x3232);
+    const uint32_t sB_lo = __byte_perm(sB, 0, 0x1010), sB_hi = __byte_perm(sB, 0, 0x3232);
+    const uint32_t kAw[4] = {kA.x, kA.y, kA.z, kA.w}, kBw[4] = {kB.x, kB.y, kB.z, kB.w};
+    float sacc[2][NT][4];
+#pragma unroll
+    for (int x = 0; x < 2; x++)
+#pragma unroll
+        for (int nt = 0; nt < NT; nt++)
+#pragma unroll
+            for (int e = 0; e < 4; e++) sacc[x][nt][e] = 0.f;
+#pragma unroll
+    for (int m = 0; m < 4; m++) {  // word m = bytes 4m..4m+3 = k-steps 2m, 2m+1; block 2c + (m >= 2)
+        uint32_t fa[4], fb[4];
+        e2m1x8_to_f16x2x4(kAw[m], fa[0], fa[1], fa[2], fa[3]);
+        e2m1x8_to_f16x2x4(kBw[m], fb[0], fb[1], fb[2], fb[3]);
+        const uint32_t sa = m < 2 ? sA_lo : sA_hi, sb = m < 2 ? sB_lo : sB_hi;
+#pragma unroll
+        for (int e = 0; e < 4; e++) {
+            fa[e] = hmul2(fa[e], sa);
+            fb[e] = hmul2(fb[e], sb);
+        }
+#pragma unroll
+        for (int nt = 0; nt < NT; nt++) {
+            mma_f16_16816(sacc[0][nt], fa[0], fb[0], fa[1], fb[1], qf[nt][2 * m][0], qf[nt][2 * m][1]);
+            mma_f16_16816(sacc[1][nt], fa[2], fb[2], fa[3], fb[3], qf[nt][2 * m + 1][0], qf[nt][2 * m + 1][1]);
+        }
+    }
+    float s[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; nt++)
+#pragma unroll
+        for (int e = 0; e < 4; e++) s[nt][e] = sacc[0][nt][e] + sacc[1][nt][e];
+    uint32_t pb[NT][2];
+    softmax_tile<NT>(s, g, vt, fac, m_run, l_run, o, pb);
+
+    // ---- O^T += V^T P^T.  Lane owns channels 16g..16g+15 (block g) of tokens 2c, 2c+1, 2c+8, 2c+9.
+    const int t0 = r0 + 2 * c;
+    uint2 v0 = *reinterpret_cast<const uint2 *>(st + L::kVq + t0 * 64 + 8 * g);
+    uint2 v1 = *reinterpret_cast<const uint2 *>(st + L::kVq + (t0 + 1) * 64 + 8 * g);
+    uint2 v2 = *reinterpret_cast<const uint2 *>(st + L::kVq + (t0 + 8) * 64 + 8 * g);
+    uint2 v3 = *reinterpret_cast<const uint2 *>(st + L::kVq + (t0 + 9) * 64 + 8 * g);
+    const int Pc = 1 << log2Pc;
+    auto vs_off = [&](int row) { return L::kVs + ((row >> log2Pc) << (log2Pc + 3)) + g * Pc + (row & (Pc - 1)); };
+    uint32_t vs01 = *reinterpret_cast<const uint16_t *>(st + vs_off(t0));
+    uint32_t vs23 = *reinterpret_cast<const uint16_t *>(st + vs_off(t0 + 8));
+    if (vt < 16) {  // rows past the sequence end may hold stale bytes: zero codes and scales
+        const int j = 2 * c;
+        if (j >= vt) { v0 = make_uint2(0, 0); vs01 &= 0xff00u; }
+        if (j + 1 >= vt) { v1 = make_uint2(0, 0); vs01 &= 0x00ffu; }
+        if (j + 8 >= vt) { v2 = make_uint2(0, 0); vs23 &= 0xff00u; }
+        if (j + 9 >= vt) { v3 = make_uint2(0, 0); vs23 &= 0x00ffu; }
+    }
+    const uint32_t sv01 = e4m3x2_to_f16x2(vs01), sv23 = e4m3x2_to_f16x2(vs23);
+    // swap nibbles so each byte holds (token a, token b) of one channel
+    const uint32_t M = 0x0f0f0f0fu;
+    const uint32_t E[4] = {(v0.x & M) | ((v1.x & M) << 4), (v0.y & M) | ((v1.y & M) << 4),
+                           (v2.x & M) | ((v3.x & M) << 4), (v2.y & M) | ((v3.y & M) << 4)};
+    const uint32_t O[4] = {((v0.x >> 4) & M) | (v1.x & ~M), ((v0.y >> 4) & M) | (v1.y & ~M),
+                           ((v2.x >> 4) & M) | (v3.x & ~M), ((v2.y >> 4) & M) | (v3.y & ~M)};
+#pragma unroll
+    for (int half = 0; half < 2; half++) {  // m-tiles 4*half .. 4*half+3
+        uint32_t e01[4], o01[4], e23[4], o23[4];
+        e2m1x8_to_f16x2x4(E[half], e01[0], e01[1], e01[2], e01[3]);
+        e2m1x8_to_f16x2x4(O[half], o01[0], o01[1], o01[2], o01[3]);
+        e2m1x8_to_f16x2x4(E[2 + half], e23[0], e23[1], e23[2], e23[3]);
+        e2m1x8_to_f16x2x4(O[2 + half], o23[0], o23[1], o23[2], o23[3]);
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            const int i = 4 * half + q;  // m-tile i: rows g -> channel 16g+2i, g+8 -> 16g+2i+1
+            const uint32_t A0 = hmul2(e01[q], sv01), A1 = hmul2(o01[q], sv01);
+            const uint32_t A2 = hmul2(e23[q], sv23), A3 = hmul2(o23[q], sv23);
+#pragma unroll
+            for (int nt = 0; nt < NT; nt++) mma_f16_16816(o[nt][i], A0, A1, A2, A3, pb[nt][0], pb[nt][1]);
+        }
+    }
+}
+
+// One warp, one 16-token tile of an FP8 stage.
+template <int NT>
+__device__ __forceinline__ void tile_fp8(const uint8_t *st, int r0, int vt, int lane, const uint32_t (&qf)[NT][8][2],
+                                         const float (&fac)[NT][2], float (&m_run)[NT][2], float (&l_run)[NT][2],
+                                         float (&o)[NT][8][4]) {
+    using L = Layout<NVFP4KV_DTYPE_FP8_E4M3>;
+    const int g = lane >> 2, c = lane & 3;
+    uint32_t kA[8], kB[8];
+    {
+        const uint4 *pa = reinterpret_cast<const uint4 *>(st + L::kKq + (r0 + g) * 128 + 32 * c);
+        const uint4 *pbk = reinterpret_cast<const uint4 *>(st + L::kKq + (r0 + g + 8) * 128 + 32 * c);
+        const uint4 a0 = pa[0], a1 = pa[1], b0 = pbk[0], b1 = pbk[1];
+        kA[0] = a0.x; kA[1] = a0.y; kA[2] = a0.z; kA[3] = a0.w; kA[4] = a1.x; kA[5] = a1.y; kA[6] = a1.z; kA[7] = a1.w;
+        kB[0] = b0.x; kB[1] = b0.y; kB[2] = b0.z; kB[3] = b0.w; kB[4] = b1.x; kB[5] = b1.y; kB[6] = b1.z; kB[7] = b1.w;
+    }
+    float sacc[2][NT][4];
+#pragma unroll
+    for (int x = 0; x < 2; x++)
+#pragma unroll
+        for (int nt = 0; nt < NT; nt++)
+#pragma unroll
+            for (int e = 0; e < 4; e++) sacc[x][nt][e] = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; j++) {  // word j = channels 32c+4j .. +3
+        const uint32_t A0 = e4m3x2_to_f16x2(kA[j] & 0xffffu), A2 = e4m3x2_to_f16x2(kA[j] >> 16);
+        const uint32_t A1 = e4m3x2_to_f16x2(kB[j] & 0xffffu), A3 = e4m3x2_to_f16x2(kB[j] >> 16);
+#pragma unroll
+        for (int nt = 0; nt < NT; nt++) mma_f16_16816(sacc[j & 1][nt], A0, A1, A2, A3, qf[nt][j][0], qf[nt][j][1]);
+    }
+    float s[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; nt++)
+#pragma unroll
+        for (int e = 0; e < 4; e++) s[nt][e] = sacc[0][nt][e] + sacc[1][nt][e];
+    uint32_t pb[NT][2];
+    softmax_tile<NT>(s, g, vt, fac, m_run, l_run, o, pb);
+
+    // V: lane owns channels 16g..16g+15 (16 bytes) of tokens 2c, 2c+1, 2c+8, 2c+9.
+    const int t0 = r0 + 2 * c;
+    uint4 v[4];
+    v[0] = *reinterpret_cast<const uint4 *>(st + L::kVq + t0 * 128 + 16 * g);
+    v[1] = *reinterpret_cast<const uint4 *>(st + L::kVq + (t0 + 1) * 128 + 16 * g);
+    v[2] = *reinterpret_cast<const uint4 *>(st + L::kVq + (t0 + 8) * 128 + 16 * g);
+    v[3] = *reinterpret_cast<const uint4 *>(st + L::kVq + (t0 + 9) * 128 + 16 * g);
+    if (vt < 16) {
+        const int rel[4] = {2 * c, 2 * c + 1, 2 * c + 8, 2 * c + 9};
+#pragma unroll
+        for (int k = 0; k < 4; k++)
+            if (rel[k] >= vt) v[k] = make_uint4(0, 0, 0, 0);
+    }
+    const uint32_t w0[4] = {v[0].x, v[0].y, v[0].z, v[0].w}, w1[4] = {v[1].x, v[1].y, v[1].z, v[1].w};
+    const uint32_t w2[4] = {v[2].x, v[2].y, v[2].z, v[2].w}, w3[4] = {v[3].x, v[3].y, v[3].z, v[3].w};
+#pragma unroll
+    for (int i = 0; i < 8; i++) {  // m-tile i: channels 16g+2i (row g), 16g+2i+1 (row g+8)
+        const uint32_t sel = (i & 1) ? 0x7362u : 0x5140u;
+        const uint32_t x01 = __byte_perm(w0[i >> 1], w1[i >> 1], sel);  // [t0 ch_e, t1 ch_e, t0 ch_o, t1 ch_o]
+        const uint32_t x23 = __byte_perm(w2[i >> 1], w3[i >> 1], sel);
+        const uint32_t A0 = e4m3x2_to_f16x2(x01 & 0xffffu), A1 = e4m3x2_to_f16x2(x01 >> 16);
+        const uint32_t A2 = e4m3x2_to_f16x2(x23 & 0xffffu), A3 = e4m3x2_to_f16x2(x23 >> 16);
+#pragma unroll
+        for (int nt = 0; nt < NT; nt++) mma_f16_16816(o[nt][i], A0, A1, A2, A3, pb[nt][0], pb[nt][1]);
+    }
+}
+
+__device__ __forceinline__ void named_barrier_sync() { asm volatile("bar.sync 1, %0;" ::"r"(kThreads) : "memory"); }
+
+template <int DTYPE, int NT>
+__global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : 2) decode_kernel(DecodeArgs a) {
+    using S = Smem<DTYPE, NT>;
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+    const int64_t U = (int64_t)a.Hkv * a.chunk_prefix[a.B];
+    const int64_t c = blockIdx.x;
+    const int64_t u0 = c * U / a.grid, u1 = (c + 1) * U / a.grid;
+    if (u0 >= u1) return;
+    const int64_t nstages = u1 - u0;
+
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + S::kBars);
+    uint64_t *empty = full + kStages;
+    int *valid = reinterpret_cast<int *>(smem + S::kFlags);
+    volatile int *abort_flag = valid + kStages;
+    float *merge_o = reinterpret_cast<float *>(smem + S::kMergeO);
+    float2 *merge_ml = reinterpret_cast<float2 *>(smem + S::kMergeML);
+
+    if (tid == 0) {
+        for (int s = 0; s < kStages; s++) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kWarps);
+            valid[s] = 0;
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    // Locate the first unit: the last sequence b whose first unit is <= u0.
+    Cursor cc;
+    {
+        int lo = 0, hi = a.B - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if ((int64_t)a.Hkv * a.chunk_prefix[mid] <= u0) lo = mid;
+            else hi = mid - 1;
+        }
+        cc.b = lo;
+        cursor_load_seq(cc, a);
+        const int64_t rem = u0 - (int64_t)a.Hkv * a.chunk_prefix[lo];
+        cc.kv = (int)(rem / cc.nchunks);
+        cc.chunk = rem - (int64_t)cc.kv * cc.nchunks;
+    }
+
+    // Producer state (thread 0): cursor of the next stage to issue and its pages.
+    Cursor pc = cc;
+    int32_t pg[4] = {-2, -2, -2, -2};
+    int64_t issued = 0;
+    if (tid == 0) {
+        load_pages(a, pc, pg);
+        const int64_t first = nstages < kStages ? nstages : kStages;
+        for (int64_t s = 0; s < first; s++) {
+            issue_stage<DTYPE>(a, pc, pg, smem + s * S::kStageBytes, &full[s], &valid[s]);
+            issued++;
+            cursor_advance(pc, a);
+            if (issued < nstages) load_pages(a, pc, pg);
+        }
+    }
+
+    const int log2Pc = a.log2P < 6 ? a.log2P : 6;
+    uint32_t qf[NT][8][2];
+    float fac[NT][2], m_run[NT][2], l_run[NT][2], o[NT][8][4];
+    bool fresh = true;
+
+    for (int64_t i = 0; i < nstages; i++) {
+        // refill the slot freed by stage i-1 with stage i-1+kStages
+        if (tid == 0 && i >= 1 && issued < nstages && !*abort_flag) {
+            const int64_t sp = i - 1;
+            const int slot = (int)(sp % kStages);
+            if (mbar_wait_bounded(&empty[slot], (uint32_t)((sp / kStages) & 1), kWaitLimit, abort_flag)) {
+                issue_stage<DTYPE>(a, pc, pg, smem + slot * S::kStageBytes, &full[slot], &valid[slot]);
+                issued++;
+                cursor_advance(pc, a);
+                if (issued < nstages) load_pages(a, pc, pg);
+            } else if (!*abort_flag) {
+                *abort_flag = 1;
+                flag_error(a.err, kErrTimeout);
+            }
+        }
+        if (fresh) {
+            load_q<NT>(a, cc.b, cc.kv, lane, qf, fac);
+#pragma unroll
+            for (int nt = 0; nt < NT; nt++) {
+                m_run[nt][0] = m_run[nt][1] = kNegInf;
+                l_run[nt][0] = l_run[nt][1] = 0.f;
+#pragma unroll
+                for (int k = 0; k < 8; k++) o[nt][k][0] = o[nt][k][1] = o[nt][k][2] = o[nt][k][3] = 0.f;
+            }
+            fresh = false;
+        }
+        const int slot = (int)(i % kStages);
+        bool ok = mbar_wait_bounded(&full[slot], (uint32_t)((i / kStages) & 1), kWaitLimit, abort_flag);
+        if (!ok && lane == 0 && !*abort_flag) {
+            *abort_flag = 1;
+            flag_error(a.err, kErrTimeout);
+        }
+        if (ok && valid[slot]) {
+            const int64_t left = (int64_t)cc.n - cc.chunk * kChunk - 16 * warp;
+            if (left > 0) {
+                const int vt = left < 16 ? (int)left : 16;
+                const uint8_t *st = smem + slot * S::kStageBytes;
+                if (DTYPE == NVFP4KV_DTYPE_NVFP4)
+                    tile_nvfp4<NT>(st, 16 * warp, vt, log2Pc, lane, qf, fac, m_run, l_run, o);
+                else
+                    tile_fp8<NT>(st, 16 * warp, vt, lane, qf, fac, m_run, l_run, o);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);
+
+        // end of this pair's segment inside the CTA?
+        Cursor nx = cc;
+        cursor_advance(nx, a);
+        const bool seg_end = (i + 1 == nstages) || nx.b != cc.b || nx.kv != cc.kv;
+        if (seg_end) {
+            const int g = lane >> 2, cq = lane & 3;
+#pragma unroll
+            for (int nt = 0; nt < NT; nt++) {
+#pragma unroll
+                for (int k = 0; k < 2; k++) {
+                    float l = l_run[nt][k];
+                    l += __shfl_xor_sync(0xffffffffu, l, 4);
+                    l += __shfl_xor_sync(0xffffffffu, l, 8);
+                    l += __shfl_xor_sync(0xffffffffu, l, 16);
+                    if (g == 0) merge_ml[warp * NT * 8 + nt * 8 + 2 * cq + k] = make_float2(m_run[nt][k], l);
+                }
+#pragma unroll
+                for (int k = 0; k < 8; k++) {
+                    float *base = merge_o + (warp * NT * 8 + nt * 8 + 2 * cq) * kHeadDim + 16 * g + 2 * k;
+                    base[0] = o[nt][k][0];
+                    base[kHeadDim] = o[nt][k][1];
+                    base[1] = o[nt][k][2];
+                    base[kHeadDim + 1] = o[nt][k][3];
+                }
+            }
+            named_barrier_sync();
+            const int64_t off_p = (int64_t)a.Hkv * a.chunk_prefix[cc.b] + (int64_t)cc.kv * cc.nchunks;
+            const bool single = off_p >= u0 && off_p + cc.nchunks <= u1;
+            const int64_t slot_id = c + (int64_t)cc.b * a.Hkv + cc.kv;
+            for (int idx = tid; idx < a.G * kHeadDim; idx += kThreads) {
+                const int h = idx >> 7, d = idx & (kHeadDim - 1);
+                float mx = kNegInf;
+#pragma unroll
+                for (int w = 0; w < kWarps; w++) mx = fmaxf(mx, merge_ml[w * NT * 8 + h].x);
+                float L = 0.f, acc = 0.f;
+                if (mx != kNegInf) {
+#pragma unroll
+                    for (int w = 0; w < kWarps; w++) {
+                        const float2 ml = merge_ml[w * NT * 8 + h];
+                        const float f = ex2(ml.x - mx);
+                        L += f * ml.y;
+                        acc += f * merge_o[(w * NT * 8 + h) * kHeadDim + d];
+                    }
+                }
+                if (single) {
+                    const float y = L > 0.f ? acc / L * a.gv : 0.f;
+                    a.out[((int64_t)cc.b * a.Hq + (int64_t)cc.kv * a.G + h) * kHeadDim + d] = __float2bfloat16_rn(y);
+                } else {
+                    a.part_acc[(slot_id * a.G + h) * kHeadDim + d] = acc;
+                    if (d == 0) a.part_ml[slot_id * a.G + h] = make_float2(mx, L);
+                }
+            }
+            named_barrier_sync();
+            fresh = true;
+        }
+        cc = nx;
+    }
+
+    // No copy may still be writing shared memory when the CTA exits.
+    if (tid == 0 && *abort_flag) {
+        for (int s = 0; s < kStages; s++) {
+            // stages s, s + kStages, ... were issued; wait for the last one issued into slot s
+            if (issued > s) {
+                const int64_t last = s + ((issued - 1 - s) / kStages) * kStages;
+                mbar_wait_bounded(&full[s], (uint32_t)((last / kStages) & 1), kWaitLimit, nullptr);
+            }
+        }
+    }
+}
+
+// Plan: chunk_prefix[b] = sum over b' < b of ceil(len(b') / 64); one CTA.
+__global__ void __launch_bounds__(1024) plan_kernel(const int32_t *seq_lens, int B, int64_t max_tokens,
+                                                    int64_t *prefix, unsigned *err) {
+    __shared__ int64_t warp_sums[32];
+    const int tid = threadIdx.x;
+    const int per = (B + 1023) / 1024;
+    const int lo = min(B, tid * per), hi = min(B, lo + per);
+    int64_t local = 0;
+    for (int b = lo; b < hi; b++) {
+        const int32_t n = seq_lens[b];
+        if (n < 0 || (int64_t)n > max_tokens) flag_error(err, kErrSeqLen);
+        const int64_t m = n < 0 ? 0 : ((int64_t)n > max_tokens ? max_tokens : n);
+        local += (m + kChunk - 1) / kChunk;
+    }
+    // block-wide exclusive scan of `local`
+    const int lane = tid & 31, warp = tid >> 5;
+    int64_t incl = local;
+#pragma unroll
+    for (int x = 1; x < 32; x <<= 1) {
+        const int64_t y = __shfl_up_sync(0xffffffffu, incl, x);
+        if (lane >= x) incl += y;
+    }
+    if (lane == 31) warp_sums[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int64_t v = warp_sums[lane];
+#pragma unroll
+        for (int x = 1; x < 32; x <<= 1) {
+            const int64_t y = __shfl_up_sync(0xffffffffu, v, x);
+            if (lane >= x) v += y;
+        }
+        warp_sums[lane] = v;  // inclusive over warps
+    }
+    __syncthreads();
+    int64_t run = incl - local + (warp > 0 ? warp_sums[warp - 1] : 0);
+    for (int b = lo; b < hi; b++) {
+        prefix[b] = run;
+        const int32_t n = seq_lens[b];
+        const int64_t m = n < 0 ? 0 : ((int64_t)n > max_tokens ? max_tokens : n);
+        run += (m + kChunk - 1) / kChunk;
+    }
+    if (tid == 1023) prefix[B] = warp_sums[31];
+}
+
+struct ReduceArgs {
+    int B, Hq, Hkv, G, grid;
+    const int64_t *chunk_prefix;
+    const float *part_acc;
+    const float2 *part_ml;
+    float gv;
+    __nv_bfloat16 *out;
+};
+
+// Log-sum-exp merge of the split partials: one warp per (sequence, query head).
+__global__ void __launch_bounds__(256) reduce_kernel(ReduceArgs a) {
+    const int lane = threadIdx.x & 31;
+    const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (row >= (int64_t)a.B * a.Hq) return;
+    const int b = (int)(row / a.Hq), h = (int)(row % a.Hq);
+    const int kv = h / a.G, hh = h % a.G;
+    const int64_t nch = a.chunk_prefix[b + 1] - a.chunk_prefix[b];
+    uint2 *dst = reinterpret_cast<uint2 *>(a.out + row * kHeadDim) + lane;
+    if (nch == 0) {
+        *dst = make_uint2(0u, 0u);
+        return;
+    }
+    const int64_t U = (int64_t)a.Hkv * a.chunk_prefix[a.B];
+    const int64_t off = (int64_t)a.Hkv * a.chunk_prefix[b] + (int64_t)kv * nch;
+    const int64_t c0 = ((off + 1) * a.grid - 1) / U;
+    const int64_t c1 = ((off + nch) * a.grid - 1) / U;
+    if (c0 == c1) return;  // written by the decode kernel
+    const int64_t p = (int64_t)b * a.Hkv + kv;
+    // CTAs with an empty range (possible when grid > U) wrote no partial
+    auto empty_cta = [&](int64_t cc) { return cc * U / a.grid == (cc + 1) * U / a.grid; };
+    float mx = kNegInf;
+    for (int64_t cc = c0; cc <= c1; cc++)
+        if (!empty_cta(cc)) mx = fmaxf(mx, a.part_ml[(cc + p) * a.G + hh].x);
+    float L = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
+    if (mx != kNegInf) {
+        for (int64_t cc = c0; cc <= c1; cc++) {
+            if (empty_cta(cc)) continue;
+            const float2 ml = a.part_ml[(cc + p) * a.G + hh];
+            const float f = ex2(ml.x - mx);
+            L += f * ml.y;
+            const float4 v = reinterpret_cast<const float4 *>(a.part_acc + ((cc + p) * a.G + hh) * kHeadDim)[lane];
+            acc[0] += f * v.x;
+            acc[1] += f * v.y;
+            acc[2] += f * v.z;
+            acc[3] += f * v.w;
+        }
+    }
+    const float inv = L > 0.f ? a.gv / L : 0.f;
+    const __nv_bfloat162 lo2 = __floats2bfloat162_rn(acc[0] * inv, acc[1] * inv);
+    const __nv_bfloat162 hi2 = __floats2bfloat162_rn(acc[2] * inv, acc[3] * inv);
+    *dst = make_uint2(*reinterpret_cast<const uint32_t *>(&lo2), *reinterpret_cast<const uint32_t *>(&hi2));
+}
+
+template <int DTYPE, int NT>
+const void *kernel_fn() {
+    return reinterpret_cast<const void *>(&decode_kernel<DTYPE, NT>);
+}
+
+const void *select_kernel(int dtype, int nt, int *smem_bytes) {
+    if (dtype == NVFP4KV_DTYPE_NVFP4) {
+        if (nt == 1) { *smem_bytes = Smem<0, 1>::kTotal; return kernel_fn<0, 1>(); }
+        *smem_bytes = Smem<0, 2>::kTotal;
+        return kernel_fn<0, 2>();
+    }
+    if (nt == 1) { *smem_bytes = Smem<1, 1>::kTotal; return kernel_fn<1, 1>(); }
+    *smem_bytes = Smem<1, 2>::kTotal;
+    return kernel_fn<1, 2>();
+}
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+int g_auto_grid[kMaxDevices][2][2];   // [device][dtype][nt-1], 0 = unknown
+bool g_attr_set[kMaxDevices][2][2];
+
+cudaError_t prepare_kernel(int dtype, int nt, int *grid_out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_mu);
+    int smem = 0;
+    const void *fn = select_kernel(dtype, nt, &smem);
+    if (!g_attr_set[dev][dtype][nt - 1]) {
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        g_attr_set[dev][dtype][nt - 1] = true;
+    }
+    if (!g_auto_grid[dev][dtype][nt - 1]) {
+        int sms = 0, per_sm = 0;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThreads, smem);
+        if (e != cudaSuccess) return e;
+        g_auto_grid[dev][dtype][nt - 1] = sms * (per_sm > 0 ? per_sm : 1);
+    }
+    if (grid_out) *grid_out = g_auto_grid[dev][dtype][nt - 1];
+    return cudaSuccess;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+}  // namespace
+
+int decode_auto_grid(const nvfp4kv_cache &c, int group, cudaError_t *status) {
+    int grid = 0;
+    cudaError_t e = prepare_kernel(c.dtype, group <= 8 ? 1 : 2, &grid);
+    if (status) *status = e;
+    return e == cudaSuccess ? grid : 0;
+}
+
+size_t decode_workspace_bytes(const nvfp4kv_cache &c, int batch, int num_q_heads, int grid) {
+    const int G = num_q_heads / c.num_kv_heads;
+    const size_t slots = (size_t)grid + (size_t)batch * c.num_kv_heads;
+    return align256(sizeof(int64_t) * ((size_t)batch + 1)) + align256(sizeof(float2) * slots * G) +
+           sizeof(float) * slots * G * kHeadDim;
+}
+
+cudaError_t launch_decode(const nvfp4kv_cache &c, const void *q, int batch, int num_q_heads,
+                          const int32_t *block_table, int max_pages, const int32_t *seq_lens, float sm_scale,
+                          void *out, void *workspace, int grid, unsigned *err, cudaStream_t stream,
+                          cudaEvent_t before, cudaEvent_t after) {
+    const int G = num_q_heads / c.num_kv_heads;
+    const int nt = G <= 8 ? 1 : 2;
+    cudaError_t e = prepare_kernel(c.dtype, nt, nullptr);
+    if (e != cudaSuccess) return e;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    const size_t slots = (size_t)grid + (size_t)batch * c.num_kv_heads;
+    int64_t *prefix = reinterpret_cast<int64_t *>(ws);
+    float2 *part_ml = reinterpret_cast<float2 *>(ws + align256(sizeof(int64_t) * ((size_t)batch + 1)));
+    float *part_acc = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(part_ml) + align256(sizeof(float2) * slots * G));
+
+    plan_kernel<<<1, 1024, 0, stream>>>(seq_lens, batch, (int64_t)max_pages * c.page_size, prefix, err);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+
+    DecodeArgs a;
+    a.pool = static_cast<const uint8_t *>(c.pool);
+    a.num_pages = c.num_pages;
+    a.P = c.page_size;
+    a.log2P = __builtin_ctz((unsigned)c.page_size);
+    a.Hkv = c.num_kv_heads;
+    a.G = G;
+    a.Hq = num_q_heads;
+    a.B = batch;
+    a.max_pages = max_pages;
+    a.slab = (int64_t)(c.dtype == NVFP4KV_DTYPE_NVFP4 ? 144 : 256) * c.page_size;
+    a.q = static_cast<const uint4 *>(q);
+    a.block_table = block_table;
+    a.seq_lens = seq_lens;
+    a.chunk_prefix = prefix;
+    a.score_log2 = (float)((double)sm_scale * (double)c.k_global_scale * 1.4426950408889634);
+    a.gv = c.v_global_scale;
+    a.out = static_cast<__nv_bfloat16 *>(out);
+    a.part_acc = part_acc;
+    a.part_ml = part_ml;
+    a.grid = grid;
+    a.err = err;
+    int smem = 0;
+    const void *fn = select_kernel(c.dtype, nt, &smem);
+    void *args[] = {&a};
+    if (before && (e = cudaEventRecord(before, stream)) != cudaSuccess) return e;
+    e = cudaLaunchKernel(fn, dim3((unsigned)grid), dim3(kThreads), args, (size_t)smem, stream);
+    if (e != cudaSuccess) return e;
+    if (after && (e = cudaEventRecord(after, stream)) != cudaSuccess) return e;
+
+    ReduceArgs r;
+    r.B = batch;
+    r.Hq = num_q_heads;
+    r.Hkv = c.num_kv_heads;
+    r.G = G;
+    r.grid = grid;
+    r.chunk_prefix = prefix;
+    r.part_acc = part_acc;
+    r.part_ml = part_ml;
+    r.gv = c.v_global_scale;
+    r.out = static_cast<__nv_bfloat16 *>(out);
+    const int64_t rows = (int64_t)batch * num_q_heads;
+    reduce_kernel<<<(unsigned)ceil_div64(rows, 8), 256, 0, stream>>>(r);
+    return cudaGetLastError();
+}
+
+}  // namespace nvfp4kv

@@ -1,0 +1,32 @@
+// kernels.h -- internal launchers of the NVFP4 KV cache kernels (not part of the C ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "nvfp4kv.h"
+
+namespace nvfp4kv {
+
+cudaError_t launch_quantize_append(const nvfp4kv_cache &c, const void *k, const void *v, int64_t num_tokens,
+                                   int64_t token_stride, const int64_t *slot_mapping, unsigned *err,
+                                   cudaStream_t stream);
+
+cudaError_t launch_prefix_dequant(const nvfp4kv_cache &c, const int32_t *block_table, int max_pages,
+                                  const int32_t *prefix_lens, const int32_t *cu, int num_reqs, int64_t total,
+                                  void *k_ws, void *v_ws, unsigned *err, cudaStream_t stream);
+
+// Number of decode CTAs an auto split uses (SM count x resident CTAs per SM).
+int decode_auto_grid(const nvfp4kv_cache &c, int group, cudaError_t *status);
+
+// Workspace bytes for a decode call with `grid` CTAs.
+size_t decode_workspace_bytes(const nvfp4kv_cache &c, int batch, int num_q_heads, int grid);
+
+// before / after: optional events recorded around the decode kernel launch.
+cudaError_t launch_decode(const nvfp4kv_cache &c, const void *q, int batch, int num_q_heads,
+                          const int32_t *block_table, int max_pages, const int32_t *seq_lens, float sm_scale,
+                          void *out, void *workspace, int grid, unsigned *err, cudaStream_t stream,
+                          cudaEvent_t before, cudaEvent_t after);
+
+}  // namespace nvfp4kv

@@ -1,0 +1,123 @@
+"""CPU checks of the C ABI: the library builds, loads, exports every symbol the
+header declares, reports the documented layout sizes, and rejects invalid
+arguments on the host (no GPU needed: rejected calls launch nothing)."""
+
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "nvfp4kv.h")
+
+
+def _lib_path():
+    import __graft_entry__
+    return __graft_entry__._cuda_build_module().build()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return re.findall(r"^NVFP4KV_API\s+[\w\s\*]*?\b(nvfp4\w+)\s*\(", text, flags=re.M)
+
+
+def test_header_declares_the_three_paths():
+    names = declared_functions()
+    for n in ("nvfp4_kv_quantize_append", "nvfp4_paged_decode_attention", "nvfp4_prefix_dequant"):
+        assert n in names
+    assert len(names) == len(set(names)) >= 10
+
+
+def test_library_exports_every_declared_symbol():
+    path = _lib_path()
+    out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True, check=True).stdout
+    exported = {ln.split()[-1] for ln in out.splitlines() if " T " in ln}
+    for n in declared_functions():
+        assert n in exported, n
+    # nothing else leaks out of the library
+    assert exported == set(declared_functions())
+    lib = ctypes.CDLL(path)
+    for n in declared_functions():
+        assert hasattr(lib, n)
+
+
+@pytest.fixture(scope="module")
+def m():
+    _lib_path()
+    import nvfp4_quantised_paged_gb300 as mod
+    return mod
+
+
+def test_binding_exports_match_header(m):
+    assert set(m.EXPORTED_SYMBOLS) == set(declared_functions())
+
+
+def test_slab_sizes_and_byte_ratio(m):
+    for P in (16, 32, 64, 128):
+        nv, f8 = m.slab_bytes(m.DTYPE_NVFP4, P), m.slab_bytes(m.DTYPE_FP8_E4M3, P)
+        assert nv == 144 * P and f8 == 256 * P and nv / f8 == 0.5625
+    for bad in (8, 48, 256):
+        with pytest.raises(m.NVFP4KVError):
+            m.slab_bytes(m.DTYPE_NVFP4, bad)
+
+
+def _desc(m, **kw):
+    d = dict(pool=4096, num_pages=4, page_size=16, num_kv_heads=2, head_dim=128, dtype=0, k_global_scale=1.0,
+             v_global_scale=1.0)
+    d.update(kw)
+    return m._CacheDesc(d["pool"], d["num_pages"], d["page_size"], d["num_kv_heads"], d["head_dim"], d["dtype"],
+                        d["k_global_scale"], d["v_global_scale"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(head_dim=64), -2), (dict(page_size=48), -2), (dict(dtype=7), -2), (dict(num_kv_heads=0), -1),
+    (dict(k_global_scale=0.0), -1), (dict(v_global_scale=float("inf")), -1), (dict(pool=4097), -1),
+    (dict(pool=0), -1), (dict(num_pages=0), -1),
+])
+def test_invalid_cache_descriptors_are_rejected_before_any_launch(m, kw, status):
+    lib = m.library()
+    d = _desc(m, **kw)
+    P = ctypes.c_void_p
+    rc = lib.nvfp4_kv_quantize_append(ctypes.byref(d), P(4096), P(4096), 1, 256, P(4096), None)
+    assert rc == status
+    rc = lib.nvfp4_paged_decode_attention(ctypes.byref(d), P(4096), 1, 2, P(4096), 1, P(4096), 0.1, P(4096),
+                                          P(4096), 1 << 20, 0, None)
+    assert rc == status
+    rc = lib.nvfp4_prefix_dequant(ctypes.byref(d), P(4096), 1, P(4096), P(4096), 1, 16, P(4096), P(4096), None)
+    assert rc == status
+
+
+def test_invalid_call_arguments_are_rejected(m):
+    lib = m.library()
+    d = ctypes.byref(_desc(m))
+    P = ctypes.c_void_p
+    # append: stride too small, stride not a multiple of 8, misaligned k, null slot mapping, negative count
+    assert lib.nvfp4_kv_quantize_append(d, P(4096), P(4096), 1, 128, P(4096), None) == -1
+    assert lib.nvfp4_kv_quantize_append(d, P(4096), P(4096), 1, 260, P(4096), None) == -1
+    assert lib.nvfp4_kv_quantize_append(d, P(4098), P(4096), 1, 256, P(4096), None) == -1
+    assert lib.nvfp4_kv_quantize_append(d, P(4096), P(4096), 1, 256, None, None) == -1
+    assert lib.nvfp4_kv_quantize_append(d, P(4096), P(4096), -1, 256, P(4096), None) == -1
+    assert lib.nvfp4_kv_quantize_append(d, None, None, 0, 256, None, None) == 0  # empty call is a no-op
+    # decode: heads not a multiple of kv heads, group > 16, misaligned workspace, bad sm_scale, empty batch
+    assert lib.nvfp4_paged_decode_attention(d, P(4096), 1, 3, P(4096), 1, P(4096), 0.1, P(4096), P(4096), 1 << 20,
+                                            0, None) == -1
+    assert lib.nvfp4_paged_decode_attention(d, P(4096), 1, 34, P(4096), 1, P(4096), 0.1, P(4096), P(4096), 1 << 20,
+                                            0, None) == -2
+    assert lib.nvfp4_paged_decode_attention(d, P(4096), 1, 2, P(4096), 1, P(4096), 0.1, P(4096), P(4100), 1 << 20,
+                                            1, None) == -1
+    assert lib.nvfp4_paged_decode_attention(d, P(4096), 1, 2, P(4096), 1, P(4096), float("nan"), P(4096),
+                                            P(4096), 1 << 20, 1, None) == -1
+    assert lib.nvfp4_paged_decode_attention(d, None, 0, 2, None, 1, None, 0.1, None, None, 0, 0, None) == 0
+    # prefix dequant: misaligned workspace, negative total, nothing to do
+    assert lib.nvfp4_prefix_dequant(d, P(4096), 1, P(4096), P(4096), 1, 16, P(4098), P(4096), None) == -1
+    assert lib.nvfp4_prefix_dequant(d, P(4096), 1, P(4096), P(4096), 1, -1, P(4096), P(4096), None) == -1
+    assert lib.nvfp4_prefix_dequant(d, None, 1, None, None, 0, 0, None, None, None) == 0
+
+
+def test_status_strings(m):
+    lib = m.library()
+    for s in (0, -1, -2, -3, -4):
+        assert lib.nvfp4kv_status_string(s)
+    assert lib.nvfp4kv_version() >= 100

@@ -1,0 +1,111 @@
+"""GPU parity of paged decode attention against the fp64 oracle (max-abs 2e-2,
+rel-L2 3e-3), over page sizes, GQA group sizes (1, 4, 5, 8, 16), ragged and
+empty sequences, split counts, the FP8 comparison cache, tensor scales, and
+the tiny-decode workload; plus error reporting for bad block-table entries."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from gpu_common import bits, check_attention, decode_both, fill_both
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def m():
+    import nvfp4_quantised_paged_gb300 as mod
+    return mod
+
+
+def test_tiny_decode_workload(m):
+    w = workloads.tiny_decode()
+    cache, pool = fill_both(w, m)
+    assert np.array_equal(cache.pool.cpu().numpy(), pool.data)
+    for splits in (0, 1, 2, 9):
+        out, ref = decode_both(w, m, cache, pool, num_splits=splits)
+        check_attention(out, ref, "tiny splits=%d" % splits)
+
+
+@pytest.mark.parametrize("P", [16, 32, 64, 128])
+@pytest.mark.parametrize("Hq,Hkv", [(8, 8), (16, 4), (40, 8), (64, 8), (32, 2)])
+def test_decode_page_sizes_and_groups(m, P, Hq, Hkv):
+    lens = [1, 63, 64, 65, 300, 1000, 0, 129]
+    w = workloads.make_decode("t", 31 + P + Hq, lens, Hq, Hkv, P, recipe=workloads.ValueRecipe(outlier_p=0.01))
+    cache, pool = fill_both(w, m)
+    out, ref = decode_both(w, m, cache, pool)
+    check_attention(out, ref, "P=%d Hq=%d Hkv=%d" % (P, Hq, Hkv))
+    assert not out[6].float().abs().sum().item()   # empty sequence -> zeros
+
+
+@pytest.mark.parametrize("splits", [1, 3, 7, 64, 500])
+def test_split_count_does_not_change_the_result_beyond_tolerance(m, splits):
+    w = workloads.make_decode("s", 5, [4000, 2500, 31, 1], 16, 2, 64)
+    cache, pool = fill_both(w, m)
+    out, ref = decode_both(w, m, cache, pool, num_splits=splits)
+    check_attention(out, ref, "splits=%d" % splits)
+
+
+def test_channel_outliers_long_sequence(m):
+    w = workloads.make_decode("c", 6, [20000, 7], 40, 8, 64, recipe=workloads.ValueRecipe(channel_lognormal=True))
+    cache, pool = fill_both(w, m)
+    out, ref = decode_both(w, m, cache, pool)
+    check_attention(out, ref, "channel outliers")
+
+
+def test_shared_prefix_pages(m):
+    w = workloads.make_decode("p", 8, [3300, 5000, 3201, 4000], 32, 8, 64, shared_prefix_tokens=3200)
+    cache, pool = fill_both(w, m)
+    out, ref = decode_both(w, m, cache, pool)
+    check_attention(out, ref, "shared prefix")
+
+
+@pytest.mark.parametrize("P", [16, 64, 128])
+def test_fp8_cache_decode(m, P):
+    w = workloads.make_decode("f", 9 + P, [1, 100, 2000, 64], 32, 4, P)
+    cache, pool = fill_both(w, m, dtype=1)
+    assert np.array_equal(cache.pool.cpu().numpy(), pool.data)
+    out, ref = decode_both(w, m, cache, pool)
+    check_attention(out, ref, "fp8 P=%d" % P)
+
+
+def test_tensor_scales_and_custom_sm_scale(m):
+    w = workloads.make_decode("g", 10, [700, 33], 16, 2, 32)
+    cache, pool = fill_both(w, m, gk=0.75, gv=3.0)
+    q = w.q("cuda")
+    out = m.paged_decode_attention(cache, q, w.block_table.cuda(), w.seq_lens.cuda(), sm_scale=0.3)
+    ref = oracle.decode_attention(pool, bits(q), w.block_table.numpy(), w.seq_lens.numpy(), 0.3)
+    check_attention(out, ref, "tensor scales")
+
+
+def test_large_query_values(m):
+    """Q far outside FP16 range is pre-scaled by a power of two per head."""
+    w = workloads.make_decode("q", 11, [500], 8, 1, 16)
+    cache, pool = fill_both(w, m)
+    q = (w.q("cuda").float() * 3.0e5).to(torch.bfloat16)
+    q[0, 3] = (q[0, 3].float() * 1e-30).to(torch.bfloat16)
+    out = m.paged_decode_attention(cache, q, w.block_table.cuda(), w.seq_lens.cuda(), sm_scale=1e-6)
+    ref = oracle.decode_attention(pool, bits(q), w.block_table.numpy(), w.seq_lens.numpy(), 1e-6)
+    check_attention(out, ref, "large q")
+
+
+def test_bad_block_table_entry_is_reported_not_read(m):
+    w = workloads.make_decode("bad", 12, [200, 300], 8, 2, 16)
+    cache, pool = fill_both(w, m)
+    bt = w.block_table.clone()
+    bt[1, 3] = w.num_pages + 1000     # out of range: the kernel must skip it and flag it
+    bt[0, 2] = -7
+    out = m.paged_decode_attention(cache, w.q("cuda"), bt.cuda(), w.seq_lens.cuda())
+    assert m.check_device_errors() == -4
+    assert m.check_device_errors() == 0
+    assert torch.isfinite(out.float()).all()
+
+
+def test_seq_len_beyond_table_is_clamped_and_reported(m):
+    w = workloads.make_decode("len", 13, [40], 4, 1, 16)
+    cache, pool = fill_both(w, m)
+    sl = torch.tensor([10_000], dtype=torch.int32, device="cuda")
+    m.paged_decode_attention(cache, w.q("cuda"), w.block_table.cuda(), sl)
+    assert m.check_device_errors() == -4
