@@ -160,6 +160,34 @@ NVFP4KV_API int nvfp4_paged_decode_attention(const nvfp4kv_cache *cache, const v
                                  float sm_scale, void *out, void *workspace, size_t workspace_bytes, int num_splits,
                                  cudaStream_t stream);
 
+/* Size of the library's static scratch array used by
+ * nvfp4_paged_decode_attention_noalloc (16 MiB on every GPU that loads the
+ * library, held until the process exits). */
+#define NVFP4KV_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/*
+ * Paged decode attention for callers that cannot allocate device memory (a
+ * host framework that owns every allocation, or a latency-critical path where
+ * cudaMalloc's possible device synchronisation is not acceptable).  No
+ * counterpart on the page: it is nvfp4_paged_decode_attention with the
+ * workspace taken from a static __device__ array of the library instead of
+ * the caller; arguments and results are the same, minus the workspace.
+ *   - Allocates nothing (no cudaMalloc, cudaFree or allocating library call).
+ *   - Needs nvfp4kv_decode_workspace_bytes(cache, batch, num_q_heads,
+ *     num_splits) <= NVFP4KV_NOALLOC_SCRATCH_BYTES; a larger request returns
+ *     NVFP4KV_EUNSUPPORTED and launches nothing.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture.
+ *   - Every call shares the one array, which keeps the last call's contents:
+ *     calls that overlap on the GPU (e.g. on unordered streams) race.  No part
+ *     of the array needs to start at zero.
+ */
+NVFP4KV_API int nvfp4_paged_decode_attention_noalloc(const nvfp4kv_cache *cache, const void *q, int batch,
+                                                     int num_q_heads, const int32_t *block_table,
+                                                     int max_pages_per_seq, const int32_t *seq_lens, float sm_scale,
+                                                     void *out, int num_splits, cudaStream_t stream);
+
 /*
  * Dequantise cached prefixes into a contiguous BF16 workspace.
  * Source: section A2, path 2 (cached prefix entries gathered, dequantised into

@@ -65,6 +65,7 @@ def _load_library():
         "nvfp4_prefix_dequant": (i32, [D, P, i32, P, P, i32, i64, P, P, P]),
         "nvfp4kv_check_device_errors": (i32, [P]),
         "nvfp4kv_profile_decode": (i32, [P, P, i32]),
+        "nvfp4_paged_decode_attention_noalloc": (i32, [D, P, i32, i32, P, i32, P, f32, P, i32, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -78,7 +79,9 @@ _lib = _load_library()
 EXPORTED_SYMBOLS = ("nvfp4kv_version", "nvfp4kv_status_string", "nvfp4kv_slab_bytes", "nvfp4kv_pool_bytes",
                     "nvfp4_kv_quantize_append", "nvfp4kv_decode_workspace_bytes", "nvfp4kv_decode_auto_splits",
                     "nvfp4_paged_decode_attention", "nvfp4_prefix_dequant", "nvfp4kv_check_device_errors",
-                    "nvfp4kv_profile_decode")
+                    "nvfp4kv_profile_decode", "nvfp4_paged_decode_attention_noalloc")
+
+NOALLOC_SCRATCH_BYTES = 16 << 20  # NVFP4KV_NOALLOC_SCRATCH_BYTES of the header
 
 
 def library():
@@ -206,6 +209,29 @@ def paged_decode_attention(cache: PagedCache, q: torch.Tensor, block_table: torc
                                            _ptr(seq_lens), float(sm_scale), _ptr(out), _ptr(workspace),
                                            workspace.numel(), int(num_splits), _stream(stream))
     _check(rc, "nvfp4_paged_decode_attention")
+    return out
+
+
+def paged_decode_attention_noalloc(cache: PagedCache, q: torch.Tensor, block_table: torch.Tensor,
+                                   seq_lens: torch.Tensor, sm_scale: Optional[float] = None,
+                                   out: Optional[torch.Tensor] = None, num_splits: int = 0,
+                                   stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """Same as paged_decode_attention, with the split scratch taken from the
+    library's static device array instead of a workspace, for callers that
+    cannot allocate device memory.  `out` must then be provided by the caller
+    too (passing None allocates it here, through torch)."""
+    _require(q, "q", torch.bfloat16)
+    _require(block_table, "block_table", torch.int32)
+    _require(seq_lens, "seq_lens", torch.int32)
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(HEAD_DIM)
+    if out is None:
+        out = torch.empty_like(q)
+    _require(out, "out", torch.bfloat16)
+    rc = _lib.nvfp4_paged_decode_attention_noalloc(cache.desc, _ptr(q), int(q.shape[0]), int(q.shape[1]),
+                                                   _ptr(block_table), int(block_table.shape[1]), _ptr(seq_lens),
+                                                   float(sm_scale), _ptr(out), int(num_splits), _stream(stream))
+    _check(rc, "nvfp4_paged_decode_attention_noalloc")
     return out
 
 
