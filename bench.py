@@ -52,6 +52,8 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-comparisons", action="store_true")
     p.add_argument("--num-splits", type=int, default=0)
+    p.add_argument("--batch", type=int, default=64,
+                   help="sequences of the 32K workload (64 = the benchmark; smaller = a profiling case)")
     return p.parse_args()
 
 
@@ -335,7 +337,8 @@ def run_ours(args):
     world, rank, local, dist = init_dist()
     torch.cuda.set_device(local)
     device = "cuda:%d" % local
-    w = workloads.decode_32k()
+    w = workloads.decode_32k() if args.batch == 64 else workloads.make_decode(
+        "decode b%d s32768 q64kv8 p64" % args.batch, 1003, [32_768] * args.batch, 64, 8, 64)
     B, S, Hq, Hkv, P = w.batch, int(w.seq_lens[0]), w.num_q_heads, w.num_kv_heads, w.page_size
 
     cache = m.PagedCache(w.num_pages, P, Hkv, device=device)

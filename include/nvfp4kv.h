@@ -161,9 +161,9 @@ NVFP4KV_API int nvfp4_paged_decode_attention(const nvfp4kv_cache *cache, const v
                                  cudaStream_t stream);
 
 /* Size of the library's static scratch array used by
- * nvfp4_paged_decode_attention_noalloc (16 MiB on every GPU that loads the
+ * nvfp4_paged_decode_attention_noalloc (64 MiB on every GPU that loads the
  * library, held until the process exits). */
-#define NVFP4KV_NOALLOC_SCRATCH_BYTES (16u << 20)
+#define NVFP4KV_NOALLOC_SCRATCH_BYTES (64u << 20)
 
 /*
  * Paged decode attention for callers that cannot allocate device memory (a

@@ -81,7 +81,7 @@ EXPORTED_SYMBOLS = ("nvfp4kv_version", "nvfp4kv_status_string", "nvfp4kv_slab_by
                     "nvfp4_paged_decode_attention", "nvfp4_prefix_dequant", "nvfp4kv_check_device_errors",
                     "nvfp4kv_profile_decode", "nvfp4_paged_decode_attention_noalloc")
 
-NOALLOC_SCRATCH_BYTES = 16 << 20  # NVFP4KV_NOALLOC_SCRATCH_BYTES of the header
+NOALLOC_SCRATCH_BYTES = 64 << 20  # NVFP4KV_NOALLOC_SCRATCH_BYTES of the header
 
 
 def library():

@@ -49,7 +49,7 @@ namespace {
 
 constexpr int kWarps = 4;
 constexpr int kThreads = 32 * kWarps;
-constexpr int kStages = 4;
+constexpr int kStages = 6;                 // ring depth: ~5 chunks in flight per CTA
 constexpr int kChunk = 64;                 // tokens per pipeline stage
 constexpr uint32_t kWaitLimit = 1u << 24;  // polls before a wait gives up (>= ~1 s)
 constexpr float kRescaleLog2 = 8.0f;
@@ -71,11 +71,9 @@ struct Layout<NVFP4KV_DTYPE_FP8_E4M3> {
 template <int DTYPE, int NT>
 struct Smem {
     static constexpr int kStageBytes = Layout<DTYPE>::kStageBytes;
-    static constexpr int kMergeO = kStages * kStageBytes;                 // float [kWarps][NT*8][128]
-    static constexpr int kMergeML = kMergeO + kWarps * NT * 8 * 128 * 4;  // float2 [kWarps][NT*8]
-    static constexpr int kBars = kMergeML + kWarps * NT * 8 * 8;          // u64 full[kStages], empty[kStages]
-    static constexpr int kFlags = kBars + 2 * kStages * 8;                // int valid[kStages], abort
-    static constexpr int kTotal = kFlags + (kStages + 4) * 4;
+    static constexpr int kBars = kStages * kStageBytes;  // u64 full[kStages]
+    static constexpr int kFlags = kBars + kStages * 8;    // int valid[kStages], done[kStages], issued[kStages], abort
+    static constexpr int kTotal = kFlags + (3 * kStages + 4) * 4;
 };
 
 struct DecodeArgs {
@@ -91,8 +89,8 @@ struct DecodeArgs {
     float score_log2;             // sm_scale * g_K * log2(e)
     float gv;
     __nv_bfloat16 *out;
-    float *part_acc;  // [slots][G][128]
-    float2 *part_ml;  // [slots][G]
+    float *part_acc;  // [slots][kWarps][G][128]
+    float2 *part_ml;  // [slots][kWarps][G]
     int grid;
     unsigned *err;
 };
@@ -102,31 +100,32 @@ __device__ __forceinline__ int clamp_len(int32_t n, int64_t cap) {
     return (int64_t)n > cap ? (int)cap : n;
 }
 
+// A unit of the CTA's range: chunk ch (of nch) of KV head kv of sequence b,
+// whose clamped length is n.
 struct Cursor {
-    int b, kv, n;
-    int64_t chunk, nchunks;
+    int b, kv, ch, nch, n;
 };
 
-__device__ __forceinline__ void cursor_load_seq(Cursor &cu, const DecodeArgs &a) {
-    cu.nchunks = a.chunk_prefix[cu.b + 1] - a.chunk_prefix[cu.b];
+__device__ __forceinline__ void cursor_seq(Cursor &cu, const DecodeArgs &a) {
+    cu.nch = (int)(a.chunk_prefix[cu.b + 1] - a.chunk_prefix[cu.b]);
     cu.n = clamp_len(a.seq_lens[cu.b], (int64_t)a.max_pages * a.P);
 }
 
-__device__ __forceinline__ void cursor_advance(Cursor &cu, const DecodeArgs &a) {
-    if (++cu.chunk < cu.nchunks) return;
-    cu.chunk = 0;
+__device__ __forceinline__ void cursor_next(Cursor &cu, const DecodeArgs &a) {
+    if (++cu.ch < cu.nch) return;
+    cu.ch = 0;
     if (++cu.kv < a.Hkv) return;
     cu.kv = 0;
     do {
         ++cu.b;
     } while (cu.b < a.B && a.chunk_prefix[cu.b + 1] == a.chunk_prefix[cu.b]);
-    if (cu.b < a.B) cursor_load_seq(cu, a);
+    if (cu.b < a.B) cursor_seq(cu, a);
 }
 
 // Block-table entries of the pages behind the stage at `cu` (-2 = not needed).
 __device__ __forceinline__ void load_pages(const DecodeArgs &a, const Cursor &cu, int32_t (&pg)[4]) {
     const int32_t *row = a.block_table + (int64_t)cu.b * a.max_pages;
-    const int64_t tok0 = cu.chunk * kChunk;
+    const int tok0 = cu.ch * kChunk;
     if (a.P >= kChunk) {
         pg[0] = __ldg(row + (tok0 >> a.log2P));
         pg[1] = pg[2] = pg[3] = -2;
@@ -134,7 +133,7 @@ __device__ __forceinline__ void load_pages(const DecodeArgs &a, const Cursor &cu
         const int np = kChunk >> a.log2P;
 #pragma unroll
         for (int j = 0; j < 4; j++) {
-            const int64_t t = tok0 + ((int64_t)j << a.log2P);
+            const int t = tok0 + (j << a.log2P);
             pg[j] = (j < np && t < cu.n) ? __ldg(row + (t >> a.log2P)) : -2;
         }
     }
@@ -165,7 +164,7 @@ __device__ __forceinline__ void issue_stage(const DecodeArgs &a, const Cursor &c
     if (DTYPE == NVFP4KV_DTYPE_NVFP4) {
         using L = Layout<NVFP4KV_DTYPE_NVFP4>;
         if (P > kChunk) {  // P = 128: half a page
-            const int h = (int)(cu.chunk & 1);
+            const int h = cu.ch & 1;
             const uint8_t *s = a.pool + ((int64_t)pg[0] * a.Hkv + cu.kv) * a.slab;
             mbar_arrive_expect_tx(full, L::kStageBytes);
             bulk_g2s(stage + L::kKq, s + h * 4096, 4096, full);
@@ -191,7 +190,7 @@ __device__ __forceinline__ void issue_stage(const DecodeArgs &a, const Cursor &c
     } else {
         using L = Layout<NVFP4KV_DTYPE_FP8_E4M3>;
         if (P > kChunk) {
-            const int h = (int)(cu.chunk & 1);
+            const int h = cu.ch & 1;
             const uint8_t *s = a.pool + ((int64_t)pg[0] * a.Hkv + cu.kv) * a.slab;
             mbar_arrive_expect_tx(full, L::kStageBytes);
             bulk_g2s(stage + L::kKq, s + h * 8192, 8192, full);
@@ -214,6 +213,13 @@ __device__ __forceinline__ void issue_stage(const DecodeArgs &a, const Cursor &c
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// (a & m) | (b & ~m)
+__device__ __forceinline__ uint32_t bitsel(uint32_t m, uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("lop3.b32 %0, %1, %2, %3, 0xE4;" : "=r"(r) : "r"(a), "r"(b), "r"(m));
+    return r;
+}
 
 // Q fragments of one (sequence, kv_head): lane (g, c) holds head nt*8+g,
 // channels 32c .. 32c+31 as the B operand of the 8 k-steps (k-step j covers
@@ -267,56 +273,64 @@ __device__ __forceinline__ void load_q(const DecodeArgs &a, int b, int kv, int l
     }
 }
 
+// Accumulator tile kLTile of o[nt] holds the softmax denominators: it is the
+// product of an all-ones A operand with P^T, so its c0 / c1 are the sums of
+// the tile's probabilities for heads nt*8+2c, +1.
+constexpr int kLTile = 8;
+constexpr uint32_t kOnesF16x2 = 0x3c003c00u;
+
 // Online softmax on one 16-token S^T tile (rows g, g+8 of the lane; columns =
-// heads nt*8+2c, +1), then the P^T operand for the P.V product.
+// heads nt*8+2c, +1), producing the P^T operand of the P.V product.  Scores
+// are in base 2; the running max moves only when a score exceeds it by more
+// than 2^kRescaleLog2, so probabilities stay <= 2^8 (exact enough in FP16).
 template <int NT>
-__device__ __forceinline__ void softmax_tile(float (&s)[NT][4], int g, int vt, const float (&fac)[NT][2],
-                                             float (&m_run)[NT][2], float (&l_run)[NT][2], float (&o)[NT][8][4],
-                                             uint32_t (&pb)[NT][2]) {
+__device__ __forceinline__ void softmax_tile(const float (&s)[NT][4], int g, int vt, const float (&fac)[NT][2],
+                                             float (&m_run)[NT][2], float (&o)[NT][9][4], uint32_t (&pb)[NT][2]) {
+    float x[NT][4];
     bool need = false;
 #pragma unroll
     for (int nt = 0; nt < NT; nt++) {
-        s[nt][0] *= fac[nt][0];
-        s[nt][1] *= fac[nt][1];
-        s[nt][2] *= fac[nt][0];
-        s[nt][3] *= fac[nt][1];
+#pragma unroll
+        for (int e = 0; e < 4; e++) x[nt][e] = fmaf(s[nt][e], fac[nt][e & 1], -m_run[nt][e & 1]);
         if (vt < 16) {
-            if (g >= vt) s[nt][0] = s[nt][1] = kNegInf;
-            if (g + 8 >= vt) s[nt][2] = s[nt][3] = kNegInf;
+            if (g >= vt) x[nt][0] = x[nt][1] = kNegInf;
+            if (g + 8 >= vt) x[nt][2] = x[nt][3] = kNegInf;
         }
-        need |= fmaxf(s[nt][0], s[nt][2]) > m_run[nt][0] + kRescaleLog2;
-        need |= fmaxf(s[nt][1], s[nt][3]) > m_run[nt][1] + kRescaleLog2;
+#pragma unroll
+        for (int e = 0; e < 4; e++) need |= x[nt][e] > kRescaleLog2;  // +inf on the first tile
     }
     if (__any_sync(0xffffffffu, need)) {
 #pragma unroll
         for (int nt = 0; nt < NT; nt++) {
-            float t0 = fmaxf(s[nt][0], s[nt][2]), t1 = fmaxf(s[nt][1], s[nt][3]);
+            float y[4];
 #pragma unroll
-            for (int x = 4; x < 32; x <<= 1) {
-                t0 = fmaxf(t0, __shfl_xor_sync(0xffffffffu, t0, x));
-                t1 = fmaxf(t1, __shfl_xor_sync(0xffffffffu, t1, x));
+            for (int e = 0; e < 4; e++) y[e] = x[nt][e] == kNegInf ? kNegInf : s[nt][e] * fac[nt][e & 1];
+            float t0 = fmaxf(y[0], y[2]), t1 = fmaxf(y[1], y[3]);
+#pragma unroll
+            for (int sh = 4; sh < 32; sh <<= 1) {
+                t0 = fmaxf(t0, __shfl_xor_sync(0xffffffffu, t0, sh));
+                t1 = fmaxf(t1, __shfl_xor_sync(0xffffffffu, t1, sh));
             }
             const float n0 = fmaxf(m_run[nt][0], t0), n1 = fmaxf(m_run[nt][1], t1);
             const float a0 = ex2(m_run[nt][0] - n0), a1 = ex2(m_run[nt][1] - n1);
             m_run[nt][0] = n0;
             m_run[nt][1] = n1;
-            l_run[nt][0] *= a0;
-            l_run[nt][1] *= a1;
 #pragma unroll
-            for (int i = 0; i < 8; i++) {
+            for (int i = 0; i < 9; i++) {
                 o[nt][i][0] *= a0;
                 o[nt][i][1] *= a1;
                 o[nt][i][2] *= a0;
                 o[nt][i][3] *= a1;
             }
+            x[nt][0] = y[0] - n0;
+            x[nt][1] = y[1] - n1;
+            x[nt][2] = y[2] - n0;
+            x[nt][3] = y[3] - n1;
         }
     }
 #pragma unroll
     for (int nt = 0; nt < NT; nt++) {
-        const float p0 = ex2(s[nt][0] - m_run[nt][0]), p1 = ex2(s[nt][1] - m_run[nt][1]);
-        const float p2 = ex2(s[nt][2] - m_run[nt][0]), p3 = ex2(s[nt][3] - m_run[nt][1]);
-        l_run[nt][0] += p0 + p2;
-        l_run[nt][1] += p1 + p3;
+        const float p0 = ex2(x[nt][0]), p1 = ex2(x[nt][1]), p2 = ex2(x[nt][2]), p3 = ex2(x[nt][3]);
         pb[nt][0] = movmatrix_trans(f32x2_to_f16x2(p1, p0));
         pb[nt][1] = movmatrix_trans(f32x2_to_f16x2(p3, p2));
     }
@@ -326,15 +340,16 @@ __device__ __forceinline__ void softmax_tile(float (&s)[NT][4], int g, int vt, c
 template <int NT>
 __device__ __forceinline__ void tile_nvfp4(const uint8_t *st, int r0, int vt, int log2Pc, int lane,
                                            const uint32_t (&qf)[NT][8][2], const float (&fac)[NT][2],
-                                           float (&m_run)[NT][2], float (&l_run)[NT][2], float (&o)[NT][8][4]) {
+                                           float (&m_run)[NT][2], float (&o)[NT][9][4]) {
     using L = Layout<NVFP4KV_DTYPE_NVFP4>;
     const int g = lane >> 2, c = lane & 3;
     // ---- S^T = K Q^T.  Lane loads channels 32c..32c+31 (16 bytes) of rows g, g+8.
-    const uint4 kA = *reinterpret_cast<const uint4 *>(st + L::kKq + (r0 + g) * 64 + 16 * c);
-    const uint4 kB = *reinterpret_cast<const uint4 *>(st + L::kKq + (r0 + g + 8) * 64 + 16 * c);
-    const uint32_t sA = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t *>(st + L::kKs + (r0 + g) * 8 + 2 * c));
-    const uint32_t sB =
-        e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t *>(st + L::kKs + (r0 + g + 8) * 8 + 2 * c));
+    const uint8_t *krow = st + L::kKq + (r0 + g) * 64 + 16 * c;
+    const uint4 kA = *reinterpret_cast<const uint4 *>(krow);
+    const uint4 kB = *reinterpret_cast<const uint4 *>(krow + 8 * 64);
+    const uint8_t *ks = st + L::kKs + (r0 + g) * 8 + 2 * c;
+    const uint32_t sA = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t *>(ks));
+    const uint32_t sB = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t *>(ks + 8 * 8));
     const uint32_t sA_lo = __byte_perm(sA, 0, 0x1010), sA_hi = __byte_perm(sA, 0, 0x3232);
     const uint32_t sB_lo = __byte_perm(sB, 0, 0x1010), sB_hi = __byte_perm(sB, 0, 0x3232);
     const uint32_t kAw[4] = {kA.x, kA.y, kA.z, kA.w}, kBw[4] = {kB.x, kB.y, kB.z, kB.w};
@@ -368,18 +383,21 @@ __device__ __forceinline__ void tile_nvfp4(const uint8_t *st, int r0, int vt, in
 #pragma unroll
         for (int e = 0; e < 4; e++) s[nt][e] = sacc[0][nt][e] + sacc[1][nt][e];
     uint32_t pb[NT][2];
-    softmax_tile<NT>(s, g, vt, fac, m_run, l_run, o, pb);
+    softmax_tile<NT>(s, g, vt, fac, m_run, o, pb);
 
     // ---- O^T += V^T P^T.  Lane owns channels 16g..16g+15 (block g) of tokens 2c, 2c+1, 2c+8, 2c+9.
     const int t0 = r0 + 2 * c;
-    uint2 v0 = *reinterpret_cast<const uint2 *>(st + L::kVq + t0 * 64 + 8 * g);
-    uint2 v1 = *reinterpret_cast<const uint2 *>(st + L::kVq + (t0 + 1) * 64 + 8 * g);
-    uint2 v2 = *reinterpret_cast<const uint2 *>(st + L::kVq + (t0 + 8) * 64 + 8 * g);
-    uint2 v3 = *reinterpret_cast<const uint2 *>(st + L::kVq + (t0 + 9) * 64 + 8 * g);
+    const uint8_t *vrow = st + L::kVq + t0 * 64 + 8 * g;
+    uint2 v0 = *reinterpret_cast<const uint2 *>(vrow);
+    uint2 v1 = *reinterpret_cast<const uint2 *>(vrow + 64);
+    uint2 v2 = *reinterpret_cast<const uint2 *>(vrow + 8 * 64);
+    uint2 v3 = *reinterpret_cast<const uint2 *>(vrow + 9 * 64);
     const int Pc = 1 << log2Pc;
-    auto vs_off = [&](int row) { return L::kVs + ((row >> log2Pc) << (log2Pc + 3)) + g * Pc + (row & (Pc - 1)); };
-    uint32_t vs01 = *reinterpret_cast<const uint16_t *>(st + vs_off(t0));
-    uint32_t vs23 = *reinterpret_cast<const uint16_t *>(st + vs_off(t0 + 8));
+    const uint8_t *vs = st + L::kVs + ((t0 >> log2Pc) << (log2Pc + 3)) + g * Pc + (t0 & (Pc - 1));
+    uint32_t vs01 = *reinterpret_cast<const uint16_t *>(vs);
+    // V scales of rows t0+8, t0+9 (block-major sub-pages of Pc rows)
+    const uint8_t *vs8 = st + L::kVs + (((t0 + 8) >> log2Pc) << (log2Pc + 3)) + g * Pc + ((t0 + 8) & (Pc - 1));
+    uint32_t vs23 = *reinterpret_cast<const uint16_t *>(vs8);
     if (vt < 16) {  // rows past the sequence end may hold stale bytes: zero codes and scales
         const int j = 2 * c;
         if (j >= vt) { v0 = make_uint2(0, 0); vs01 &= 0xff00u; }
@@ -390,10 +408,10 @@ __device__ __forceinline__ void tile_nvfp4(const uint8_t *st, int r0, int vt, in
     const uint32_t sv01 = e4m3x2_to_f16x2(vs01), sv23 = e4m3x2_to_f16x2(vs23);
     // swap nibbles so each byte holds (token a, token b) of one channel
     const uint32_t M = 0x0f0f0f0fu;
-    const uint32_t E[4] = {(v0.x & M) | ((v1.x & M) << 4), (v0.y & M) | ((v1.y & M) << 4),
-                           (v2.x & M) | ((v3.x & M) << 4), (v2.y & M) | ((v3.y & M) << 4)};
-    const uint32_t O[4] = {((v0.x >> 4) & M) | (v1.x & ~M), ((v0.y >> 4) & M) | (v1.y & ~M),
-                           ((v2.x >> 4) & M) | (v3.x & ~M), ((v2.y >> 4) & M) | (v3.y & ~M)};
+    const uint32_t E[4] = {bitsel(M, v0.x, v1.x << 4), bitsel(M, v0.y, v1.y << 4), bitsel(M, v2.x, v3.x << 4),
+                           bitsel(M, v2.y, v3.y << 4)};
+    const uint32_t O[4] = {bitsel(M, v0.x >> 4, v1.x), bitsel(M, v0.y >> 4, v1.y), bitsel(M, v2.x >> 4, v3.x),
+                           bitsel(M, v2.y >> 4, v3.y)};
 #pragma unroll
     for (int half = 0; half < 2; half++) {  // m-tiles 4*half .. 4*half+3
         uint32_t e01[4], o01[4], e23[4], o23[4];
@@ -410,13 +428,15 @@ __device__ __forceinline__ void tile_nvfp4(const uint8_t *st, int r0, int vt, in
             for (int nt = 0; nt < NT; nt++) mma_f16_16816(o[nt][i], A0, A1, A2, A3, pb[nt][0], pb[nt][1]);
         }
     }
+#pragma unroll
+    for (int nt = 0; nt < NT; nt++)
+        mma_f16_16816(o[nt][kLTile], kOnesF16x2, kOnesF16x2, kOnesF16x2, kOnesF16x2, pb[nt][0], pb[nt][1]);
 }
 
 // One warp, one 16-token tile of an FP8 stage.
 template <int NT>
 __device__ __forceinline__ void tile_fp8(const uint8_t *st, int r0, int vt, int lane, const uint32_t (&qf)[NT][8][2],
-                                         const float (&fac)[NT][2], float (&m_run)[NT][2], float (&l_run)[NT][2],
-                                         float (&o)[NT][8][4]) {
+                                         const float (&fac)[NT][2], float (&m_run)[NT][2], float (&o)[NT][9][4]) {
     using L = Layout<NVFP4KV_DTYPE_FP8_E4M3>;
     const int g = lane >> 2, c = lane & 3;
     uint32_t kA[8], kB[8];
@@ -447,7 +467,7 @@ __device__ __forceinline__ void tile_fp8(const uint8_t *st, int r0, int vt, int 
 #pragma unroll
         for (int e = 0; e < 4; e++) s[nt][e] = sacc[0][nt][e] + sacc[1][nt][e];
     uint32_t pb[NT][2];
-    softmax_tile<NT>(s, g, vt, fac, m_run, l_run, o, pb);
+    softmax_tile<NT>(s, g, vt, fac, m_run, o, pb);
 
     // V: lane owns channels 16g..16g+15 (16 bytes) of tokens 2c, 2c+1, 2c+8, 2c+9.
     const int t0 = r0 + 2 * c;
@@ -474,9 +494,25 @@ __device__ __forceinline__ void tile_fp8(const uint8_t *st, int r0, int vt, int 
 #pragma unroll
         for (int nt = 0; nt < NT; nt++) mma_f16_16816(o[nt][i], A0, A1, A2, A3, pb[nt][0], pb[nt][1]);
     }
+#pragma unroll
+    for (int nt = 0; nt < NT; nt++)
+        mma_f16_16816(o[nt][kLTile], kOnesF16x2, kOnesF16x2, kOnesF16x2, kOnesF16x2, pb[nt][0], pb[nt][1]);
 }
 
-__device__ __forceinline__ void named_barrier_sync() { asm volatile("bar.sync 1, %0;" ::"r"(kThreads) : "memory"); }
+// Counts one warp as done with a slot; true for the warp that completes the
+// count (release/acquire at CTA scope: the other warps' reads of the slot
+// happen before the last warp refills it).
+__device__ __forceinline__ bool slot_done_last(int *done) {
+    int old;
+    asm volatile("atom.acq_rel.cta.shared::cta.add.s32 %0, [%1], 1;" : "=r"(old) : "r"(smem_u32(done)) : "memory");
+    return old == kWarps - 1;
+}
+
+// Orders this thread's generic-proxy shared-memory accesses before its
+// following bulk (async-proxy) copies into the same buffer.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
 
 template <int DTYPE, int NT>
 __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : 2) decode_kernel(DecodeArgs a) {
@@ -488,25 +524,13 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : 2) decode_kernel(Decod
     const int64_t c = blockIdx.x;
     const int64_t u0 = c * U / a.grid, u1 = (c + 1) * U / a.grid;
     if (u0 >= u1) return;
-    const int64_t nstages = u1 - u0;
+    const int nstages = (int)(u1 - u0);
 
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + S::kBars);
-    uint64_t *empty = full + kStages;
     int *valid = reinterpret_cast<int *>(smem + S::kFlags);
-    volatile int *abort_flag = valid + kStages;
-    float *merge_o = reinterpret_cast<float *>(smem + S::kMergeO);
-    float2 *merge_ml = reinterpret_cast<float2 *>(smem + S::kMergeML);
-
-    if (tid == 0) {
-        for (int s = 0; s < kStages; s++) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kWarps);
-            valid[s] = 0;
-        }
-        *abort_flag = 0;
-        fence_mbar_init();
-    }
-    __syncthreads();
+    int *done = valid + kStages;
+    int *slot_issued = done + kStages;
+    volatile int *abort_flag = slot_issued + kStages;
 
     // Locate the first unit: the last sequence b whose first unit is <= u0.
     Cursor cc;
@@ -518,144 +542,119 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : 2) decode_kernel(Decod
             else hi = mid - 1;
         }
         cc.b = lo;
-        cursor_load_seq(cc, a);
-        const int64_t rem = u0 - (int64_t)a.Hkv * a.chunk_prefix[lo];
-        cc.kv = (int)(rem / cc.nchunks);
-        cc.chunk = rem - (int64_t)cc.kv * cc.nchunks;
+        cursor_seq(cc, a);
+        const int rem = (int)(u0 - (int64_t)a.Hkv * a.chunk_prefix[lo]);
+        cc.kv = rem / cc.nch;
+        cc.ch = rem - cc.kv * cc.nch;
     }
 
-    // Producer state (thread 0): cursor of the next stage to issue and its pages.
+    // Every warp tracks the unit kStages ahead of the one it consumes: the warp
+    // that finishes a slot last refills it with that unit (lane 0 only).
     Cursor pc = cc;
     int32_t pg[4] = {-2, -2, -2, -2};
-    int64_t issued = 0;
     if (tid == 0) {
-        load_pages(a, pc, pg);
-        const int64_t first = nstages < kStages ? nstages : kStages;
-        for (int64_t s = 0; s < first; s++) {
-            issue_stage<DTYPE>(a, pc, pg, smem + s * S::kStageBytes, &full[s], &valid[s]);
-            issued++;
-            cursor_advance(pc, a);
-            if (issued < nstages) load_pages(a, pc, pg);
+        for (int s = 0; s < kStages; s++) {
+            mbar_init(&full[s], 1);
+            valid[s] = 0;
+            done[s] = 0;
+            slot_issued[s] = 0;
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    {
+        const int first = nstages < kStages ? nstages : kStages;
+        for (int s = 0; s < first; s++) {
+            if (tid == 0) {
+                load_pages(a, pc, pg);
+                issue_stage<DTYPE>(a, pc, pg, smem + s * S::kStageBytes, &full[s], &valid[s]);
+                slot_issued[s] = 1;
+            }
+            cursor_next(pc, a);
         }
     }
 
     const int log2Pc = a.log2P < 6 ? a.log2P : 6;
     uint32_t qf[NT][8][2];
-    float fac[NT][2], m_run[NT][2], l_run[NT][2], o[NT][8][4];
-    bool fresh = true;
+    float fac[NT][2], m_run[NT][2], o[NT][9][4];
+    int seg_left = 0;
 
-    for (int64_t i = 0; i < nstages; i++) {
-        // refill the slot freed by stage i-1 with stage i-1+kStages
-        if (tid == 0 && i >= 1 && issued < nstages && !*abort_flag) {
-            const int64_t sp = i - 1;
-            const int slot = (int)(sp % kStages);
-            if (mbar_wait_bounded(&empty[slot], (uint32_t)((sp / kStages) & 1), kWaitLimit, abort_flag)) {
-                issue_stage<DTYPE>(a, pc, pg, smem + slot * S::kStageBytes, &full[slot], &valid[slot]);
-                issued++;
-                cursor_advance(pc, a);
-                if (issued < nstages) load_pages(a, pc, pg);
-            } else if (!*abort_flag) {
-                *abort_flag = 1;
-                flag_error(a.err, kErrTimeout);
-            }
-        }
-        if (fresh) {
+    for (int i = 0; i < nstages; i++) {
+        const bool refill = i + kStages < nstages;  // pc = unit of stage i + kStages
+        if (refill && lane == 0) load_pages(a, pc, pg);  // consumed after this tile, if this warp refills
+        if (seg_left == 0) {  // a new (sequence, kv_head) segment starts at this unit
+            seg_left = min(cc.nch - cc.ch, nstages - i);
             load_q<NT>(a, cc.b, cc.kv, lane, qf, fac);
 #pragma unroll
             for (int nt = 0; nt < NT; nt++) {
                 m_run[nt][0] = m_run[nt][1] = kNegInf;
-                l_run[nt][0] = l_run[nt][1] = 0.f;
 #pragma unroll
-                for (int k = 0; k < 8; k++) o[nt][k][0] = o[nt][k][1] = o[nt][k][2] = o[nt][k][3] = 0.f;
+                for (int k = 0; k < 9; k++) o[nt][k][0] = o[nt][k][1] = o[nt][k][2] = o[nt][k][3] = 0.f;
             }
-            fresh = false;
         }
-        const int slot = (int)(i % kStages);
-        bool ok = mbar_wait_bounded(&full[slot], (uint32_t)((i / kStages) & 1), kWaitLimit, abort_flag);
+        const int slot = i % kStages;
+        const bool ok = mbar_wait_bounded(&full[slot], (uint32_t)((i / kStages) & 1), kWaitLimit, abort_flag);
         if (!ok && lane == 0 && !*abort_flag) {
             *abort_flag = 1;
             flag_error(a.err, kErrTimeout);
         }
         if (ok && valid[slot]) {
-            const int64_t left = (int64_t)cc.n - cc.chunk * kChunk - 16 * warp;
+            const int left = cc.n - cc.ch * kChunk - 16 * warp;
             if (left > 0) {
-                const int vt = left < 16 ? (int)left : 16;
+                const int vt = left < 16 ? left : 16;
                 const uint8_t *st = smem + slot * S::kStageBytes;
                 if (DTYPE == NVFP4KV_DTYPE_NVFP4)
-                    tile_nvfp4<NT>(st, 16 * warp, vt, log2Pc, lane, qf, fac, m_run, l_run, o);
+                    tile_nvfp4<NT>(st, 16 * warp, vt, log2Pc, lane, qf, fac, m_run, o);
                 else
-                    tile_fp8<NT>(st, 16 * warp, vt, lane, qf, fac, m_run, l_run, o);
+                    tile_fp8<NT>(st, 16 * warp, vt, lane, qf, fac, m_run, o);
             }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[slot]);
+        if (lane == 0 && slot_done_last(&done[slot])) {
+            done[slot] = 0;
+            if (refill && !*abort_flag) {
+                fence_proxy_async_smem();
+                issue_stage<DTYPE>(a, pc, pg, smem + slot * S::kStageBytes, &full[slot], &valid[slot]);
+                slot_issued[slot] += 1;
+            }
+        }
+        if (refill) cursor_next(pc, a);
 
-        // end of this pair's segment inside the CTA?
-        Cursor nx = cc;
-        cursor_advance(nx, a);
-        const bool seg_end = (i + 1 == nstages) || nx.b != cc.b || nx.kv != cc.kv;
-        if (seg_end) {
+        if (--seg_left > 0) {
+            cc.ch++;
+            continue;
+        }
+        // end of this pair's segment inside the CTA: this warp's partial (max, sum, acc)
+        {
             const int g = lane >> 2, cq = lane & 3;
+            const int64_t pidx = (c + (int64_t)cc.b * a.Hkv + cc.kv) * kWarps + warp;
 #pragma unroll
             for (int nt = 0; nt < NT; nt++) {
 #pragma unroll
                 for (int k = 0; k < 2; k++) {
-                    float l = l_run[nt][k];
-                    l += __shfl_xor_sync(0xffffffffu, l, 4);
-                    l += __shfl_xor_sync(0xffffffffu, l, 8);
-                    l += __shfl_xor_sync(0xffffffffu, l, 16);
-                    if (g == 0) merge_ml[warp * NT * 8 + nt * 8 + 2 * cq + k] = make_float2(m_run[nt][k], l);
-                }
+                    const int h = nt * 8 + 2 * cq + k;
+                    if (h >= a.G) continue;
+                    if (g == 0) a.part_ml[pidx * a.G + h] = make_float2(m_run[nt][k], o[nt][kLTile][k]);
+                    float *dst = a.part_acc + (pidx * a.G + h) * kHeadDim + 16 * g;
 #pragma unroll
-                for (int k = 0; k < 8; k++) {
-                    float *base = merge_o + (warp * NT * 8 + nt * 8 + 2 * cq) * kHeadDim + 16 * g + 2 * k;
-                    base[0] = o[nt][k][0];
-                    base[kHeadDim] = o[nt][k][1];
-                    base[1] = o[nt][k][2];
-                    base[kHeadDim + 1] = o[nt][k][3];
+                    for (int i2 = 0; i2 < 8; i2++)
+                        *reinterpret_cast<float2 *>(dst + 2 * i2) = make_float2(o[nt][i2][k], o[nt][i2][k + 2]);
                 }
             }
-            named_barrier_sync();
-            const int64_t off_p = (int64_t)a.Hkv * a.chunk_prefix[cc.b] + (int64_t)cc.kv * cc.nchunks;
-            const bool single = off_p >= u0 && off_p + cc.nchunks <= u1;
-            const int64_t slot_id = c + (int64_t)cc.b * a.Hkv + cc.kv;
-            for (int idx = tid; idx < a.G * kHeadDim; idx += kThreads) {
-                const int h = idx >> 7, d = idx & (kHeadDim - 1);
-                float mx = kNegInf;
-#pragma unroll
-                for (int w = 0; w < kWarps; w++) mx = fmaxf(mx, merge_ml[w * NT * 8 + h].x);
-                float L = 0.f, acc = 0.f;
-                if (mx != kNegInf) {
-#pragma unroll
-                    for (int w = 0; w < kWarps; w++) {
-                        const float2 ml = merge_ml[w * NT * 8 + h];
-                        const float f = ex2(ml.x - mx);
-                        L += f * ml.y;
-                        acc += f * merge_o[(w * NT * 8 + h) * kHeadDim + d];
-                    }
-                }
-                if (single) {
-                    const float y = L > 0.f ? acc / L * a.gv : 0.f;
-                    a.out[((int64_t)cc.b * a.Hq + (int64_t)cc.kv * a.G + h) * kHeadDim + d] = __float2bfloat16_rn(y);
-                } else {
-                    a.part_acc[(slot_id * a.G + h) * kHeadDim + d] = acc;
-                    if (d == 0) a.part_ml[slot_id * a.G + h] = make_float2(mx, L);
-                }
-            }
-            named_barrier_sync();
-            fresh = true;
         }
-        cc = nx;
+        if (i + 1 < nstages) {  // move to the first chunk of the next pair
+            cc.ch = cc.nch - 1;
+            cursor_next(cc, a);
+        }
     }
 
     // No copy may still be writing shared memory when the CTA exits.
+    __syncthreads();
     if (tid == 0 && *abort_flag) {
         for (int s = 0; s < kStages; s++) {
-            // stages s, s + kStages, ... were issued; wait for the last one issued into slot s
-            if (issued > s) {
-                const int64_t last = s + ((issued - 1 - s) / kStages) * kStages;
-                mbar_wait_bounded(&full[s], (uint32_t)((last / kStages) & 1), kWaitLimit, nullptr);
-            }
+            const int n = slot_issued[s];  // the slot's last copy completes phase n - 1
+            if (n > 0) mbar_wait_bounded(&full[s], (uint32_t)((n - 1) & 1), kWaitLimit, nullptr);
         }
     }
 }
@@ -713,7 +712,9 @@ struct ReduceArgs {
     __nv_bfloat16 *out;
 };
 
-// Log-sum-exp merge of the split partials: one warp per (sequence, query head).
+// Log-sum-exp merge of the per-warp partials of every CTA that covered the
+// pair, then normalisation and the V tensor scale: one warp per (sequence,
+// query head).
 __global__ void __launch_bounds__(256) reduce_kernel(ReduceArgs a) {
     const int lane = threadIdx.x & 31;
     const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
@@ -730,25 +731,31 @@ __global__ void __launch_bounds__(256) reduce_kernel(ReduceArgs a) {
     const int64_t off = (int64_t)a.Hkv * a.chunk_prefix[b] + (int64_t)kv * nch;
     const int64_t c0 = ((off + 1) * a.grid - 1) / U;
     const int64_t c1 = ((off + nch) * a.grid - 1) / U;
-    if (c0 == c1) return;  // written by the decode kernel
     const int64_t p = (int64_t)b * a.Hkv + kv;
     // CTAs with an empty range (possible when grid > U) wrote no partial
     auto empty_cta = [&](int64_t cc) { return cc * U / a.grid == (cc + 1) * U / a.grid; };
     float mx = kNegInf;
-    for (int64_t cc = c0; cc <= c1; cc++)
-        if (!empty_cta(cc)) mx = fmaxf(mx, a.part_ml[(cc + p) * a.G + hh].x);
+    for (int64_t cc = c0; cc <= c1; cc++) {
+        if (empty_cta(cc)) continue;
+#pragma unroll
+        for (int w = 0; w < kWarps; w++) mx = fmaxf(mx, a.part_ml[((cc + p) * kWarps + w) * a.G + hh].x);
+    }
     float L = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
     if (mx != kNegInf) {
         for (int64_t cc = c0; cc <= c1; cc++) {
             if (empty_cta(cc)) continue;
-            const float2 ml = a.part_ml[(cc + p) * a.G + hh];
-            const float f = ex2(ml.x - mx);
-            L += f * ml.y;
-            const float4 v = reinterpret_cast<const float4 *>(a.part_acc + ((cc + p) * a.G + hh) * kHeadDim)[lane];
-            acc[0] += f * v.x;
-            acc[1] += f * v.y;
-            acc[2] += f * v.z;
-            acc[3] += f * v.w;
+#pragma unroll
+            for (int w = 0; w < kWarps; w++) {
+                const int64_t idx = ((cc + p) * kWarps + w) * a.G + hh;
+                const float2 ml = a.part_ml[idx];
+                const float f = ex2(ml.x - mx);
+                L += f * ml.y;
+                const float4 v = reinterpret_cast<const float4 *>(a.part_acc + idx * kHeadDim)[lane];
+                acc[0] += f * v.x;
+                acc[1] += f * v.y;
+                acc[2] += f * v.z;
+                acc[3] += f * v.w;
+            }
         }
     }
     const float inv = L > 0.f ? a.gv / L : 0.f;
@@ -816,7 +823,7 @@ int decode_auto_grid(const nvfp4kv_cache &c, int group, cudaError_t *status) {
 
 size_t decode_workspace_bytes(const nvfp4kv_cache &c, int batch, int num_q_heads, int grid) {
     const int G = num_q_heads / c.num_kv_heads;
-    const size_t slots = (size_t)grid + (size_t)batch * c.num_kv_heads;
+    const size_t slots = ((size_t)grid + (size_t)batch * c.num_kv_heads) * kWarps;
     return align256(sizeof(int64_t) * ((size_t)batch + 1)) + align256(sizeof(float2) * slots * G) +
            sizeof(float) * slots * G * kHeadDim;
 }
@@ -830,7 +837,7 @@ cudaError_t launch_decode(const nvfp4kv_cache &c, const void *q, int batch, int 
     cudaError_t e = prepare_kernel(c.dtype, nt, nullptr);
     if (e != cudaSuccess) return e;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
-    const size_t slots = (size_t)grid + (size_t)batch * c.num_kv_heads;
+    const size_t slots = ((size_t)grid + (size_t)batch * c.num_kv_heads) * kWarps;
     int64_t *prefix = reinterpret_cast<int64_t *>(ws);
     float2 *part_ml = reinterpret_cast<float2 *>(ws + align256(sizeof(int64_t) * ((size_t)batch + 1)));
     float *part_acc = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(part_ml) + align256(sizeof(float2) * slots * G));
