@@ -39,13 +39,15 @@
  *
  * Pool layout, one slab per (page, kv_head), slabs ordered page-major:
  *   pool = uint8[num_pages][num_kv_heads][slab_bytes]
- *   NVFP4 slab (144 * P bytes):
- *     K codes  uint8[P][64]  byte i of row t = element 2i (low nibble) and
- *                            element 2i+1 (high nibble) of token row t
- *     K scales uint8[P][8]   E4M3 scale of block j (elements 16j..16j+15)
- *     V codes  uint8[P][64]  as K codes
- *     V scales uint8[8][P]   block-major: scale of block j of row t at [j][t]
- *   FP8 slab (256 * P bytes):  K uint8[P][128] | V uint8[P][128] (E4M3 codes)
+ *   A slab is P/16 groups of 16 consecutive token rows; group j (rows 16j ..
+ *   16j+15) starts at byte j * group_bytes and holds, for its rows r = 0..15:
+ *   NVFP4 group (2304 bytes, slab = 144 * P):
+ *     K codes  uint8[16][64]  byte i of row r = element 2i (low nibble) and
+ *                             element 2i+1 (high nibble) of that token's K row
+ *     K scales uint8[16][8]   E4M3 scale of block b (elements 16b..16b+15)
+ *     V codes  uint8[16][64]  as K codes
+ *     V scales uint8[8][16]   block-major: scale of block b of row r at [b][r]
+ *   FP8 group (4096 bytes, slab = 256 * P):  K uint8[16][128] | V uint8[16][128]
  *   Token position t of a sequence is row t % P of page block_table[t / P].
  *   A nibble is an E2M1 code: bit 3 sign, bits 2..0 magnitude index into
  *   {0, 0.5, 1, 1.5, 2, 3, 4, 6}.

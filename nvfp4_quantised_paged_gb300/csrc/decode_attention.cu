@@ -11,20 +11,25 @@
 //   * Work split.  The KV of every (sequence, kv_head) pair is cut into
 //     64-token chunks; all chunks of all pairs form one flat range that is cut
 //     into `grid` equal contiguous pieces, one per CTA (grid = SM count x
-//     resident CTAs for an auto split).  A CTA therefore streams an equal
-//     number of bytes whatever the mix of sequence lengths.  A pair covered by
-//     one CTA gets its output written directly; a pair spread over several CTAs
-//     leaves one (max, sum, acc) partial per CTA, merged by a separate
-//     log-sum-exp reduction kernel.
-//   * Staging.  One thread issues 1-D bulk (TMA) copies of each 64-token chunk
-//     (9,216 bytes for NVFP4) into a 4-stage shared-memory ring, completion
-//     tracked by mbarriers; every wait is bounded and reports a timeout in the
-//     device error word instead of spinning forever.
+//     resident CTAs for an auto split), so every CTA streams the same number
+//     of bytes whatever the mix of sequence lengths.  Each of the CTA's four
+//     warps takes one 16-token group of every chunk and leaves one
+//     (max, sum, acc) partial per pair it touched; a separate log-sum-exp
+//     reduction kernel merges the partials of a pair and normalises.
+//   * Staging.  Each warp runs its own 6-deep ring: lane 0 fetches its next
+//     16-token group (2,304 contiguous bytes for NVFP4) with one 1-D bulk (TMA)
+//     copy completed on an mbarrier, refilling a slot as soon as the warp has
+//     used it.  Warps never wait for one another.  With 4 CTAs per SM about
+//     180 KB are in flight per SM, what HBM latency under load needs.  Every
+//     wait is bounded and reports a timeout in the device error word instead
+//     of spinning forever.
 //   * Tensor cores on the real contraction only: per warp and 16 tokens,
 //     S^T (16 tokens x 8 query heads of the group) = K Q^T and
 //     O^T (128 dims x 8 heads) += V^T P^T with mma.sync m16n8k16, FP16 inputs
 //     and FP32 accumulation.  Tokens sit on the M dimension, so a GQA group of
 //     up to 8 heads fills N = 8 with no padding; groups of 9-16 use two N tiles.
+//     The softmax denominators come from the same unit: an all-ones A operand
+//     times P^T.
 //   * Unpack.  ptxas for sm_103a accepts cvt.rn.f16x2.e2m1x2 (not the BF16
 //     form), so values are unpacked to FP16.  Every e2m1 x e4m3 product is an
 //     FP16 normal with <= 6 significant bits, so the scaled values are exact.
@@ -49,31 +54,32 @@ namespace {
 
 constexpr int kWarps = 4;
 constexpr int kThreads = 32 * kWarps;
-constexpr int kStages = 6;                 // ring depth: ~5 chunks in flight per CTA
-constexpr int kChunk = 64;                 // tokens per pipeline stage
+constexpr int kDepth = 6;                  // per-warp ring depth (5 groups in flight)
+constexpr int kChunk = 64;                 // tokens per unit of the work split (one group per warp)
 constexpr uint32_t kWaitLimit = 1u << 24;  // polls before a wait gives up (>= ~1 s)
 constexpr float kRescaleLog2 = 8.0f;
 constexpr float kNegInf = -__builtin_huge_valf();
 
+// One 16-token group of a page, as stored (see include/nvfp4kv.h).
 template <int DTYPE>
-struct Layout;
+struct Group;
 template <>
-struct Layout<NVFP4KV_DTYPE_NVFP4> {  // canonical 64-token stage
-    static constexpr int kStageBytes = 9216;
-    static constexpr int kKq = 0, kKs = 4096, kVq = 4608, kVs = 8704;
+struct Group<NVFP4KV_DTYPE_NVFP4> {
+    static constexpr int kBytes = 2304;
+    static constexpr int kKq = 0, kKs = 1024, kVq = 1152, kVs = 2176;
 };
 template <>
-struct Layout<NVFP4KV_DTYPE_FP8_E4M3> {
-    static constexpr int kStageBytes = 16384;
-    static constexpr int kKq = 0, kVq = 8192;
+struct Group<NVFP4KV_DTYPE_FP8_E4M3> {
+    static constexpr int kBytes = 4096;
+    static constexpr int kKq = 0, kVq = 2048;
 };
 
-template <int DTYPE, int NT>
+template <int DTYPE>
 struct Smem {
-    static constexpr int kStageBytes = Layout<DTYPE>::kStageBytes;
-    static constexpr int kBars = kStages * kStageBytes;  // u64 full[kStages]
-    static constexpr int kFlags = kBars + kStages * 8;    // int valid[kStages], done[kStages], issued[kStages], abort
-    static constexpr int kTotal = kFlags + (3 * kStages + 4) * 4;
+    static constexpr int kRing = kDepth * Group<DTYPE>::kBytes;   // one ring per warp
+    static constexpr int kBars = kWarps * kRing;                   // u64 full[kWarps][kDepth]
+    static constexpr int kFlags = kBars + kWarps * kDepth * 8;     // int valid[kWarps][kDepth]
+    static constexpr int kTotal = kFlags + kWarps * kDepth * 4;
 };
 
 struct DecodeArgs {
@@ -122,93 +128,34 @@ __device__ __forceinline__ void cursor_next(Cursor &cu, const DecodeArgs &a) {
     if (cu.b < a.B) cursor_seq(cu, a);
 }
 
-// Block-table entries of the pages behind the stage at `cu` (-2 = not needed).
-__device__ __forceinline__ void load_pages(const DecodeArgs &a, const Cursor &cu, int32_t (&pg)[4]) {
-    const int32_t *row = a.block_table + (int64_t)cu.b * a.max_pages;
-    const int tok0 = cu.ch * kChunk;
-    if (a.P >= kChunk) {
-        pg[0] = __ldg(row + (tok0 >> a.log2P));
-        pg[1] = pg[2] = pg[3] = -2;
-    } else {
-        const int np = kChunk >> a.log2P;
-#pragma unroll
-        for (int j = 0; j < 4; j++) {
-            const int t = tok0 + (j << a.log2P);
-            pg[j] = (j < np && t < cu.n) ? __ldg(row + (t >> a.log2P)) : -2;
-        }
-    }
+// Page of this warp's group of the unit at `cu` (-2: the group lies past the
+// sequence end and is not fetched).
+__device__ __forceinline__ int32_t group_page(const DecodeArgs &a, const Cursor &cu, int warp) {
+    const int t = cu.ch * kChunk + 16 * warp;
+    if (t >= cu.n) return -2;
+    return __ldg(a.block_table + (int64_t)cu.b * a.max_pages + (t >> a.log2P));
 }
 
-// Producer: stage `cu` into `stage` (thread 0 only).
+// Lane 0: fetch this warp's group of unit `cu` into `dst`.
 template <int DTYPE>
-__device__ __forceinline__ void issue_stage(const DecodeArgs &a, const Cursor &cu, const int32_t (&pg)[4],
-                                            uint8_t *stage, uint64_t *full, int *valid) {
-    bool ok = true;
-#pragma unroll
-    for (int j = 0; j < 4; j++)
-        if (pg[j] != -2 && (pg[j] < 0 || (int64_t)pg[j] >= a.num_pages)) ok = false;
-    if (!ok) {
+__device__ __forceinline__ void issue_group(const DecodeArgs &a, const Cursor &cu, int warp, int32_t pg,
+                                            uint8_t *dst, uint64_t *full, int *valid) {
+    if (pg == -2) {  // nothing to fetch: the tile is skipped
+        *valid = 0;
+        mbar_arrive(full);
+        return;
+    }
+    if (pg < 0 || (int64_t)pg >= a.num_pages) {
         flag_error(a.err, kErrPage);
         *valid = 0;
         mbar_arrive(full);
         return;
     }
     *valid = 1;
-    const int P = a.P;
-    if (P == kChunk) {
-        const uint8_t *src = a.pool + ((int64_t)pg[0] * a.Hkv + cu.kv) * a.slab;
-        mbar_arrive_expect_tx(full, (uint32_t)a.slab);
-        bulk_g2s(stage, src, (uint32_t)a.slab, full);
-        return;
-    }
-    if (DTYPE == NVFP4KV_DTYPE_NVFP4) {
-        using L = Layout<NVFP4KV_DTYPE_NVFP4>;
-        if (P > kChunk) {  // P = 128: half a page
-            const int h = cu.ch & 1;
-            const uint8_t *s = a.pool + ((int64_t)pg[0] * a.Hkv + cu.kv) * a.slab;
-            mbar_arrive_expect_tx(full, L::kStageBytes);
-            bulk_g2s(stage + L::kKq, s + h * 4096, 4096, full);
-            bulk_g2s(stage + L::kKs, s + 64 * P + h * 512, 512, full);
-            bulk_g2s(stage + L::kVq, s + 72 * P + h * 4096, 4096, full);
-#pragma unroll
-            for (int j = 0; j < 8; j++) bulk_g2s(stage + L::kVs + j * 64, s + 136 * P + j * P + h * 64, 64, full);
-        } else {  // P = 16 or 32: 64 / P pages
-            const int np = kChunk / P;
-            uint32_t bytes = 0;
-            for (int j = 0; j < np; j++)
-                if (pg[j] >= 0) bytes += 144u * P;
-            mbar_arrive_expect_tx(full, bytes);
-            for (int j = 0; j < np; j++) {
-                if (pg[j] < 0) continue;
-                const uint8_t *s = a.pool + ((int64_t)pg[j] * a.Hkv + cu.kv) * a.slab;
-                bulk_g2s(stage + L::kKq + j * 64 * P, s, 64 * P, full);
-                bulk_g2s(stage + L::kKs + j * 8 * P, s + 64 * P, 8 * P, full);
-                bulk_g2s(stage + L::kVq + j * 64 * P, s + 72 * P, 64 * P, full);
-                bulk_g2s(stage + L::kVs + j * 8 * P, s + 136 * P, 8 * P, full);
-            }
-        }
-    } else {
-        using L = Layout<NVFP4KV_DTYPE_FP8_E4M3>;
-        if (P > kChunk) {
-            const int h = cu.ch & 1;
-            const uint8_t *s = a.pool + ((int64_t)pg[0] * a.Hkv + cu.kv) * a.slab;
-            mbar_arrive_expect_tx(full, L::kStageBytes);
-            bulk_g2s(stage + L::kKq, s + h * 8192, 8192, full);
-            bulk_g2s(stage + L::kVq, s + 128 * P + h * 8192, 8192, full);
-        } else {
-            const int np = kChunk / P;
-            uint32_t bytes = 0;
-            for (int j = 0; j < np; j++)
-                if (pg[j] >= 0) bytes += 256u * P;
-            mbar_arrive_expect_tx(full, bytes);
-            for (int j = 0; j < np; j++) {
-                if (pg[j] < 0) continue;
-                const uint8_t *s = a.pool + ((int64_t)pg[j] * a.Hkv + cu.kv) * a.slab;
-                bulk_g2s(stage + L::kKq + j * 128 * P, s, 128 * P, full);
-                bulk_g2s(stage + L::kVq + j * 128 * P, s + 128 * P, 128 * P, full);
-            }
-        }
-    }
+    const int row = (cu.ch * kChunk + 16 * warp) & (a.P - 1);
+    const uint8_t *src = a.pool + ((int64_t)pg * a.Hkv + cu.kv) * a.slab + (row >> 4) * Group<DTYPE>::kBytes;
+    mbar_arrive_expect_tx(full, Group<DTYPE>::kBytes);
+    bulk_g2s(dst, src, Group<DTYPE>::kBytes, full);
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -219,6 +166,12 @@ __device__ __forceinline__ uint32_t bitsel(uint32_t m, uint32_t a, uint32_t b) {
     uint32_t r;
     asm("lop3.b32 %0, %1, %2, %3, 0xE4;" : "=r"(r) : "r"(a), "r"(b), "r"(m));
     return r;
+}
+
+// Orders this thread's generic-proxy shared-memory accesses before its
+// following bulk (async-proxy) copies into the same buffer.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // Q fragments of one (sequence, kv_head): lane (g, c) holds head nt*8+g,
@@ -336,18 +289,17 @@ __device__ __forceinline__ void softmax_tile(const float (&s)[NT][4], int g, int
     }
 }
 
-// One warp, one 16-token tile of an NVFP4 stage.  vt = valid rows (1..16).
+// One warp, one 16-token NVFP4 group (rows 0..15).  vt = valid rows (1..16).
 template <int NT>
-__device__ __forceinline__ void tile_nvfp4(const uint8_t *st, int r0, int vt, int log2Pc, int lane,
-                                           const uint32_t (&qf)[NT][8][2], const float (&fac)[NT][2],
-                                           float (&m_run)[NT][2], float (&o)[NT][9][4]) {
-    using L = Layout<NVFP4KV_DTYPE_NVFP4>;
+__device__ __forceinline__ void tile_nvfp4(const uint8_t *st, int vt, int lane, const uint32_t (&qf)[NT][8][2],
+                                           const float (&fac)[NT][2], float (&m_run)[NT][2], float (&o)[NT][9][4]) {
+    using L = Group<NVFP4KV_DTYPE_NVFP4>;
     const int g = lane >> 2, c = lane & 3;
     // ---- S^T = K Q^T.  Lane loads channels 32c..32c+31 (16 bytes) of rows g, g+8.
-    const uint8_t *krow = st + L::kKq + (r0 + g) * 64 + 16 * c;
+    const uint8_t *krow = st + L::kKq + g * 64 + 16 * c;
     const uint4 kA = *reinterpret_cast<const uint4 *>(krow);
     const uint4 kB = *reinterpret_cast<const uint4 *>(krow + 8 * 64);
-    const uint8_t *ks = st + L::kKs + (r0 + g) * 8 + 2 * c;
+    const uint8_t *ks = st + L::kKs + g * 8 + 2 * c;
     const uint32_t sA = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t *>(ks));
     const uint32_t sB = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t *>(ks + 8 * 8));
     const uint32_t sA_lo = __byte_perm(sA, 0, 0x1010), sA_hi = __byte_perm(sA, 0, 0x3232);
@@ -386,18 +338,14 @@ __device__ __forceinline__ void tile_nvfp4(const uint8_t *st, int r0, int vt, in
     softmax_tile<NT>(s, g, vt, fac, m_run, o, pb);
 
     // ---- O^T += V^T P^T.  Lane owns channels 16g..16g+15 (block g) of tokens 2c, 2c+1, 2c+8, 2c+9.
-    const int t0 = r0 + 2 * c;
-    const uint8_t *vrow = st + L::kVq + t0 * 64 + 8 * g;
+    const uint8_t *vrow = st + L::kVq + (2 * c) * 64 + 8 * g;
     uint2 v0 = *reinterpret_cast<const uint2 *>(vrow);
     uint2 v1 = *reinterpret_cast<const uint2 *>(vrow + 64);
     uint2 v2 = *reinterpret_cast<const uint2 *>(vrow + 8 * 64);
     uint2 v3 = *reinterpret_cast<const uint2 *>(vrow + 9 * 64);
-    const int Pc = 1 << log2Pc;
-    const uint8_t *vs = st + L::kVs + ((t0 >> log2Pc) << (log2Pc + 3)) + g * Pc + (t0 & (Pc - 1));
+    const uint8_t *vs = st + L::kVs + g * 16 + 2 * c;  // V scales [8][16]: rows 2c, 2c+1 and 2c+8, 2c+9
     uint32_t vs01 = *reinterpret_cast<const uint16_t *>(vs);
-    // V scales of rows t0+8, t0+9 (block-major sub-pages of Pc rows)
-    const uint8_t *vs8 = st + L::kVs + (((t0 + 8) >> log2Pc) << (log2Pc + 3)) + g * Pc + ((t0 + 8) & (Pc - 1));
-    uint32_t vs23 = *reinterpret_cast<const uint16_t *>(vs8);
+    uint32_t vs23 = *reinterpret_cast<const uint16_t *>(vs + 8);
     if (vt < 16) {  // rows past the sequence end may hold stale bytes: zero codes and scales
         const int j = 2 * c;
         if (j >= vt) { v0 = make_uint2(0, 0); vs01 &= 0xff00u; }
@@ -433,16 +381,16 @@ __device__ __forceinline__ void tile_nvfp4(const uint8_t *st, int r0, int vt, in
         mma_f16_16816(o[nt][kLTile], kOnesF16x2, kOnesF16x2, kOnesF16x2, kOnesF16x2, pb[nt][0], pb[nt][1]);
 }
 
-// One warp, one 16-token tile of an FP8 stage.
+// One warp, one 16-token FP8 group.
 template <int NT>
-__device__ __forceinline__ void tile_fp8(const uint8_t *st, int r0, int vt, int lane, const uint32_t (&qf)[NT][8][2],
+__device__ __forceinline__ void tile_fp8(const uint8_t *st, int vt, int lane, const uint32_t (&qf)[NT][8][2],
                                          const float (&fac)[NT][2], float (&m_run)[NT][2], float (&o)[NT][9][4]) {
-    using L = Layout<NVFP4KV_DTYPE_FP8_E4M3>;
+    using L = Group<NVFP4KV_DTYPE_FP8_E4M3>;
     const int g = lane >> 2, c = lane & 3;
     uint32_t kA[8], kB[8];
     {
-        const uint4 *pa = reinterpret_cast<const uint4 *>(st + L::kKq + (r0 + g) * 128 + 32 * c);
-        const uint4 *pbk = reinterpret_cast<const uint4 *>(st + L::kKq + (r0 + g + 8) * 128 + 32 * c);
+        const uint4 *pa = reinterpret_cast<const uint4 *>(st + L::kKq + g * 128 + 32 * c);
+        const uint4 *pbk = reinterpret_cast<const uint4 *>(st + L::kKq + (g + 8) * 128 + 32 * c);
         const uint4 a0 = pa[0], a1 = pa[1], b0 = pbk[0], b1 = pbk[1];
         kA[0] = a0.x; kA[1] = a0.y; kA[2] = a0.z; kA[3] = a0.w; kA[4] = a1.x; kA[5] = a1.y; kA[6] = a1.z; kA[7] = a1.w;
         kB[0] = b0.x; kB[1] = b0.y; kB[2] = b0.z; kB[3] = b0.w; kB[4] = b1.x; kB[5] = b1.y; kB[6] = b1.z; kB[7] = b1.w;
@@ -470,12 +418,12 @@ __device__ __forceinline__ void tile_fp8(const uint8_t *st, int r0, int vt, int 
     softmax_tile<NT>(s, g, vt, fac, m_run, o, pb);
 
     // V: lane owns channels 16g..16g+15 (16 bytes) of tokens 2c, 2c+1, 2c+8, 2c+9.
-    const int t0 = r0 + 2 * c;
+    const uint8_t *vrow = st + L::kVq + (2 * c) * 128 + 16 * g;
     uint4 v[4];
-    v[0] = *reinterpret_cast<const uint4 *>(st + L::kVq + t0 * 128 + 16 * g);
-    v[1] = *reinterpret_cast<const uint4 *>(st + L::kVq + (t0 + 1) * 128 + 16 * g);
-    v[2] = *reinterpret_cast<const uint4 *>(st + L::kVq + (t0 + 8) * 128 + 16 * g);
-    v[3] = *reinterpret_cast<const uint4 *>(st + L::kVq + (t0 + 9) * 128 + 16 * g);
+    v[0] = *reinterpret_cast<const uint4 *>(vrow);
+    v[1] = *reinterpret_cast<const uint4 *>(vrow + 128);
+    v[2] = *reinterpret_cast<const uint4 *>(vrow + 8 * 128);
+    v[3] = *reinterpret_cast<const uint4 *>(vrow + 9 * 128);
     if (vt < 16) {
         const int rel[4] = {2 * c, 2 * c + 1, 2 * c + 8, 2 * c + 9};
 #pragma unroll
@@ -499,24 +447,10 @@ __device__ __forceinline__ void tile_fp8(const uint8_t *st, int r0, int vt, int 
         mma_f16_16816(o[nt][kLTile], kOnesF16x2, kOnesF16x2, kOnesF16x2, kOnesF16x2, pb[nt][0], pb[nt][1]);
 }
 
-// Counts one warp as done with a slot; true for the warp that completes the
-// count (release/acquire at CTA scope: the other warps' reads of the slot
-// happen before the last warp refills it).
-__device__ __forceinline__ bool slot_done_last(int *done) {
-    int old;
-    asm volatile("atom.acq_rel.cta.shared::cta.add.s32 %0, [%1], 1;" : "=r"(old) : "r"(smem_u32(done)) : "memory");
-    return old == kWarps - 1;
-}
-
-// Orders this thread's generic-proxy shared-memory accesses before its
-// following bulk (async-proxy) copies into the same buffer.
-__device__ __forceinline__ void fence_proxy_async_smem() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 template <int DTYPE, int NT>
 __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : 2) decode_kernel(DecodeArgs a) {
-    using S = Smem<DTYPE, NT>;
+    using S = Smem<DTYPE>;
+    constexpr int kGB = Group<DTYPE>::kBytes;
     extern __shared__ __align__(128) uint8_t smem[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
@@ -526,11 +460,10 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : 2) decode_kernel(Decod
     if (u0 >= u1) return;
     const int nstages = (int)(u1 - u0);
 
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + S::kBars);
-    int *valid = reinterpret_cast<int *>(smem + S::kFlags);
-    int *done = valid + kStages;
-    int *slot_issued = done + kStages;
-    volatile int *abort_flag = slot_issued + kStages;
+    // this warp's ring, barriers and flags
+    uint8_t *ring = smem + warp * S::kRing;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + S::kBars) + warp * kDepth;
+    int *valid = reinterpret_cast<int *>(smem + S::kFlags) + warp * kDepth;
 
     // Locate the first unit: the last sequence b whose first unit is <= u0.
     Cursor cc;
@@ -548,41 +481,38 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : 2) decode_kernel(Decod
         cc.ch = rem - cc.kv * cc.nch;
     }
 
-    // Every warp tracks the unit kStages ahead of the one it consumes: the warp
-    // that finishes a slot last refills it with that unit (lane 0 only).
-    Cursor pc = cc;
-    int32_t pg[4] = {-2, -2, -2, -2};
-    if (tid == 0) {
-        for (int s = 0; s < kStages; s++) {
+    if (lane == 0) {
+        for (int s = 0; s < kDepth; s++) {
             mbar_init(&full[s], 1);
             valid[s] = 0;
-            done[s] = 0;
-            slot_issued[s] = 0;
         }
-        *abort_flag = 0;
         fence_mbar_init();
     }
-    __syncthreads();
+    __syncwarp();
+
+    // Producer cursor (lane 0 issues): the unit kDepth stages ahead.
+    Cursor pc = cc;
+    int32_t pg = -2;
+    int issued = 0;  // copies issued by this warp (for the drain after a timeout)
     {
-        const int first = nstages < kStages ? nstages : kStages;
+        const int first = nstages < kDepth ? nstages : kDepth;
         for (int s = 0; s < first; s++) {
-            if (tid == 0) {
-                load_pages(a, pc, pg);
-                issue_stage<DTYPE>(a, pc, pg, smem + s * S::kStageBytes, &full[s], &valid[s]);
-                slot_issued[s] = 1;
+            if (lane == 0) {
+                issue_group<DTYPE>(a, pc, warp, group_page(a, pc, warp), ring + s * kGB, &full[s], &valid[s]);
+                issued++;
             }
             cursor_next(pc, a);
         }
     }
 
-    const int log2Pc = a.log2P < 6 ? a.log2P : 6;
     uint32_t qf[NT][8][2];
     float fac[NT][2], m_run[NT][2], o[NT][9][4];
     int seg_left = 0;
+    bool aborted = false;
 
     for (int i = 0; i < nstages; i++) {
-        const bool refill = i + kStages < nstages;  // pc = unit of stage i + kStages
-        if (refill && lane == 0) load_pages(a, pc, pg);  // consumed after this tile, if this warp refills
+        const bool refill = i + kDepth < nstages;         // pc = unit of stage i + kDepth
+        if (refill && lane == 0) pg = group_page(a, pc, warp);  // used after this tile
         if (seg_left == 0) {  // a new (sequence, kv_head) segment starts at this unit
             seg_left = min(cc.nch - cc.ch, nstages - i);
             load_q<NT>(a, cc.b, cc.kv, lane, qf, fac);
@@ -593,30 +523,30 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : 2) decode_kernel(Decod
                 for (int k = 0; k < 9; k++) o[nt][k][0] = o[nt][k][1] = o[nt][k][2] = o[nt][k][3] = 0.f;
             }
         }
-        const int slot = i % kStages;
-        const bool ok = mbar_wait_bounded(&full[slot], (uint32_t)((i / kStages) & 1), kWaitLimit, abort_flag);
-        if (!ok && lane == 0 && !*abort_flag) {
-            *abort_flag = 1;
-            flag_error(a.err, kErrTimeout);
+        const int slot = i % kDepth;
+        bool ok = false;
+        if (!aborted) {
+            ok = mbar_wait_bounded(&full[slot], (uint32_t)((i / kDepth) & 1), kWaitLimit, nullptr);
+            if (!ok) {
+                aborted = true;
+                if (lane == 0) flag_error(a.err, kErrTimeout);
+            }
         }
         if (ok && valid[slot]) {
             const int left = cc.n - cc.ch * kChunk - 16 * warp;
-            if (left > 0) {
-                const int vt = left < 16 ? left : 16;
-                const uint8_t *st = smem + slot * S::kStageBytes;
-                if (DTYPE == NVFP4KV_DTYPE_NVFP4)
-                    tile_nvfp4<NT>(st, 16 * warp, vt, log2Pc, lane, qf, fac, m_run, o);
-                else
-                    tile_fp8<NT>(st, 16 * warp, vt, lane, qf, fac, m_run, o);
-            }
+            const int vt = left < 16 ? left : 16;
+            const uint8_t *st = ring + slot * kGB;
+            if (DTYPE == NVFP4KV_DTYPE_NVFP4)
+                tile_nvfp4<NT>(st, vt, lane, qf, fac, m_run, o);
+            else
+                tile_fp8<NT>(st, vt, lane, qf, fac, m_run, o);
         }
         __syncwarp();
-        if (lane == 0 && slot_done_last(&done[slot])) {
-            done[slot] = 0;
-            if (refill && !*abort_flag) {
+        if (refill && !aborted) {
+            if (lane == 0) {
                 fence_proxy_async_smem();
-                issue_stage<DTYPE>(a, pc, pg, smem + slot * S::kStageBytes, &full[slot], &valid[slot]);
-                slot_issued[slot] += 1;
+                issue_group<DTYPE>(a, pc, warp, pg, ring + slot * kGB, &full[slot], &valid[slot]);
+                issued++;
             }
         }
         if (refill) cursor_next(pc, a);
@@ -649,12 +579,12 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : 2) decode_kernel(Decod
         }
     }
 
-    // No copy may still be writing shared memory when the CTA exits.
-    __syncthreads();
-    if (tid == 0 && *abort_flag) {
-        for (int s = 0; s < kStages; s++) {
-            const int n = slot_issued[s];  // the slot's last copy completes phase n - 1
-            if (n > 0) mbar_wait_bounded(&full[s], (uint32_t)((n - 1) & 1), kWaitLimit, nullptr);
+    // After a timeout, no copy of this warp may still be writing shared memory
+    // when the CTA exits: wait (bounded) for the last copy issued into each slot.
+    if (aborted && lane == 0) {
+        for (int s = 0; s < kDepth && s < issued; s++) {
+            const int n = (issued - 1 - s) / kDepth + 1;  // copies issued into slot s
+            mbar_wait_bounded(&full[s], (uint32_t)((n - 1) & 1), kWaitLimit, nullptr);
         }
     }
 }
@@ -771,12 +701,12 @@ const void *kernel_fn() {
 
 const void *select_kernel(int dtype, int nt, int *smem_bytes) {
     if (dtype == NVFP4KV_DTYPE_NVFP4) {
-        if (nt == 1) { *smem_bytes = Smem<0, 1>::kTotal; return kernel_fn<0, 1>(); }
-        *smem_bytes = Smem<0, 2>::kTotal;
+        *smem_bytes = Smem<0>::kTotal;
+        if (nt == 1) return kernel_fn<0, 1>();
         return kernel_fn<0, 2>();
     }
-    if (nt == 1) { *smem_bytes = Smem<1, 1>::kTotal; return kernel_fn<1, 1>(); }
-    *smem_bytes = Smem<1, 2>::kTotal;
+    *smem_bytes = Smem<1>::kTotal;
+    if (nt == 1) return kernel_fn<1, 1>();
     return kernel_fn<1, 2>();
 }
 

@@ -85,12 +85,14 @@ __global__ void __launch_bounds__(256) prefix_dequant_kernel(PrefixArgs a) {
         return;
     }
     const int rp = (int)(t & (a.P - 1));
+    const int rr = rp & 15;  // row inside its 16-token group
     const uint8_t *slab = a.pool + (page * a.Hkv + h) * a.slab;
     const float g = which ? a.gv : a.gk;
     uint32_t o[8];
     if (a.dtype == NVFP4KV_DTYPE_NVFP4) {
-        const uint2 codes = __ldg(reinterpret_cast<const uint2 *>(slab + (which ? 72 * a.P : 0) + rp * 64 + blk * 8));
-        const uint32_t sbyte = which ? __ldg(slab + 136 * a.P + blk * a.P + rp) : __ldg(slab + 64 * a.P + rp * 8 + blk);
+        const uint8_t *grp = slab + (rp >> 4) * 2304;
+        const uint2 codes = __ldg(reinterpret_cast<const uint2 *>(grp + (which ? 1152 : 0) + rr * 64 + blk * 8));
+        const uint32_t sbyte = __ldg(grp + (which ? 2176 + blk * 16 + rr : 1024 + rr * 8 + blk));
         const uint32_t s2 = e4m3x2_to_f16x2(sbyte | (sbyte << 8));  // {s, s}
         uint32_t f[8];
         e2m1x8_to_f16x2x4(codes.x, f[0], f[1], f[2], f[3]);
@@ -98,7 +100,8 @@ __global__ void __launch_bounds__(256) prefix_dequant_kernel(PrefixArgs a) {
 #pragma unroll
         for (int i = 0; i < 8; i++) o[i] = f16x2_to_bf16x2_scaled(hmul2(f[i], s2), g);
     } else {
-        const uint4 c = __ldg(reinterpret_cast<const uint4 *>(slab + (which ? 128 * a.P : 0) + rp * 128 + blk * 16));
+        const uint4 c = __ldg(
+            reinterpret_cast<const uint4 *>(slab + (rp >> 4) * 4096 + (which ? 2048 : 0) + rr * 128 + blk * 16));
         const uint32_t w[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
         for (int i = 0; i < 4; i++) {

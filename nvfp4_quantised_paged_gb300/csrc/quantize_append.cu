@@ -126,11 +126,11 @@ __global__ void __launch_bounds__(256) append_nvfp4_kernel(AppendArgs a) {
     quantize_block16<kUnitScale>(x0, x1, which ? a.gv : a.gk, codes, sbyte);
     const int64_t page = slot >> a.log2P;
     const int r = (int)(slot & (a.P - 1));
-    uint8_t *slab = a.pool + (page * a.Hkv + h) * a.slab;
-    uint8_t *code_row = slab + (which ? 72 * a.P : 0) + r * 64;
-    *reinterpret_cast<uint2 *>(code_row + blk * 8) = codes;
-    uint8_t *scale_dst = which ? slab + 136 * a.P + blk * a.P + r : slab + 64 * a.P + r * 8 + blk;
-    *scale_dst = (uint8_t)sbyte;
+    // 16-token groups of 2304 bytes: K codes | K scales | V codes | V scales [8][16]
+    uint8_t *grp = a.pool + (page * a.Hkv + h) * a.slab + (r >> 4) * 2304;
+    const int rr = r & 15;
+    *reinterpret_cast<uint2 *>(grp + (which ? 1152 : 0) + rr * 64 + blk * 8) = codes;
+    grp[which ? 2176 + blk * 16 + rr : 1024 + rr * 8 + blk] = (uint8_t)sbyte;
 }
 
 // FP8 pool: one thread converts one 16-value block to 16 E4M3 bytes.
@@ -169,8 +169,9 @@ __global__ void __launch_bounds__(256) append_fp8_kernel(AppendArgs a) {
     }
     const int64_t page = slot >> a.log2P;
     const int r = (int)(slot & (a.P - 1));
-    uint8_t *slab = a.pool + (page * a.Hkv + h) * a.slab;
-    uint8_t *dst = slab + (which ? 128 * a.P : 0) + r * 128 + blk * 16;
+    // 16-token groups of 4096 bytes: K codes [16][128] | V codes [16][128]
+    uint8_t *dst = a.pool + (page * a.Hkv + h) * a.slab + (r >> 4) * 4096 + (which ? 2048 : 0) + (r & 15) * 128 +
+                   blk * 16;
     *reinterpret_cast<uint4 *>(dst) = make_uint4(out[0], out[1], out[2], out[3]);
 }
 

@@ -31,10 +31,12 @@
  *   Nibble order: element 2i in the low nibble of byte i.  Query head h reads
  *   KV head h / G (G = query heads per KV head).
  *
- * Pool layout (one slab per (page, kv_head), slabs ordered page-major):
- *   NVFP4: K codes [P][64] | K scales [P][8] | V codes [P][64] | V scales [8][P]
- *          (K scales row-major, V scales block-major: block j of row t at [j][t])
- *   FP8  : K codes [P][128] | V codes [P][128]
+ * Pool layout (one slab per (page, kv_head), slabs ordered page-major).  A
+ * slab of P tokens is P/16 groups of 16 consecutive tokens, each group laid out
+ * as (row r = 0..15 of the group):
+ *   NVFP4 (2304 B): K codes [16][64] | K scales [16][8] | V codes [16][64] |
+ *                   V scales [8][16] (block-major: block j of row r at [j][r])
+ *   FP8   (4096 B): K codes [16][128] | V codes [16][128]
  * Token t of a sequence lives in page block_table[t / P] at row t % P.
  *
  * Build: gcc -O2 -std=c11 -ffp-contract=off -shared -fPIC -pthread -lm
@@ -194,6 +196,7 @@ static double nvfp4_dequant(uint8_t code, uint8_t scale, float g)
 
 int64_t oracle_slab_bytes(int dtype, int page_size)
 {
+    if (page_size < 16 || page_size % 16) return -1;
     if (dtype == ORACLE_DTYPE_NVFP4) return (int64_t)page_size * (64 + 8 + 64 + 8);
     if (dtype == ORACLE_DTYPE_FP8) return (int64_t)page_size * (128 + 128);
     return -1;
@@ -213,19 +216,21 @@ static uint8_t *slab_ptr(const pool_t *p, int64_t page, int kv)
     return p->pool + (page * p->num_kv_heads + kv) * oracle_slab_bytes(p->dtype, p->page_size);
 }
 
-/* Row `row` of K (which = 0) or V (which = 1) of one slab: codes and scales. */
+/* Row `row` of K (which = 0) or V (which = 1) of one slab: its codes, and the
+ * scale byte of block `blk` (16-token groups, see the header). */
 static uint8_t *codes_row(const pool_t *p, uint8_t *slab, int which, int row)
 {
-    int P = p->page_size;
-    if (p->dtype == ORACLE_DTYPE_NVFP4) return slab + (which ? 72 * P : 0) + row * 64;
-    return slab + (which ? 128 * P : 0) + row * 128;
+    int grp = row / 16, r = row % 16;
+    if (p->dtype == ORACLE_DTYPE_NVFP4) return slab + grp * 2304 + (which ? 1152 : 0) + r * 64;
+    return slab + grp * 4096 + (which ? 2048 : 0) + r * 128;
 }
-/* Scale byte of block `blk` of row `row`: K scales are [P][8], V scales [8][P]. */
+
 static uint8_t *scale_ptr(const pool_t *p, uint8_t *slab, int which, int row, int blk)
 {
-    int P = p->page_size;
-    if (which == 0) return slab + 64 * P + row * 8 + blk;
-    return slab + 136 * P + blk * P + row;
+    (void)p;
+    int grp = row / 16, r = row % 16;
+    if (which == 0) return slab + grp * 2304 + 1024 + r * 8 + blk;
+    return slab + grp * 2304 + 2176 + blk * 16 + r;
 }
 
 /* Dequantise one head_dim row of K or V into out[128] (double). */
@@ -453,7 +458,7 @@ int oracle_decode_attention(const uint8_t *pool, int64_t num_pages, int page_siz
 typedef struct {
     const uint16_t *k, *v;
     int64_t row_stride;
-    pool_t p; /* a one-row scratch pool */
+    pool_t p; /* a one-page scratch pool */
     int status;
 } bf16_rows_t;
 
@@ -476,9 +481,9 @@ static int bf16_row(void *ctx, int which, int64_t t, double *out)
 int oracle_sequence_attention(const uint16_t *q, int G, const uint16_t *k, const uint16_t *v, int64_t n,
                               int64_t row_stride, int dtype, float gk, float gv, double sm_scale, double *out)
 {
-    uint8_t slab[256];
-    if (G < 1 || G > 16 || oracle_slab_bytes(dtype, 1) < 0) return ORACLE_EINVAL;
-    bf16_rows_t ctx = {k, v, row_stride, {slab, 1, 1, 1, dtype, gk, gv}, 0};
+    uint8_t slab[4096]; /* one 16-token group; rows are quantised into row 0 */
+    if (G < 1 || G > 16 || oracle_slab_bytes(dtype, 16) < 0) return ORACLE_EINVAL;
+    bf16_rows_t ctx = {k, v, row_stride, {slab, 1, 16, 1, dtype, gk, gv}, 0};
     double qd[16 * HEAD_DIM];
     for (int i = 0; i < G * HEAD_DIM; i++) qd[i] = oracle_bf16_value(q[i]);
     double *scores = malloc(sizeof(double) * (size_t)G * (size_t)(n > 0 ? n : 1));

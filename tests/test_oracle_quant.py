@@ -124,20 +124,21 @@ def test_non_finite_input_rejected():
         oracle.quantize_block16(np.array([0x7F80] + [0] * 15, dtype=np.uint16))
 
 
-def _layout_offsets(P):
-    """The cache's documented layout: K codes [P][64], K scales [P][8],
-    V codes [P][64], V scales [8][P] (block-major) per (page, kv_head) slab."""
-    return {"kq": 0, "ks": 64 * P, "vq": 72 * P, "vs": 136 * P}
+def _code_off(name, row):
+    """The cache's documented layout: a slab is P/16 groups of 16 tokens, each
+    K codes [16][64] | K scales [16][8] | V codes [16][64] | V scales [8][16]."""
+    grp, r = divmod(row, 16)
+    return grp * 2304 + (0 if name == "k" else 1152) + r * 64
 
 
-def _scale_index(P, name, row, blk):
-    off = _layout_offsets(P)
+def _scale_index(name, row, blk):
+    grp, r = divmod(row, 16)
     if name == "k":
-        return off["ks"] + row * 8 + blk
-    return off["vs"] + blk * P + row
+        return grp * 2304 + 1024 + r * 8 + blk
+    return grp * 2304 + 2176 + blk * 16 + r
 
 
-@pytest.mark.parametrize("P", [16, 64])
+@pytest.mark.parametrize("P", [16, 64, 128])
 def test_append_places_rows_at_documented_offsets(P):
     rng = np.random.default_rng(4)
     Hkv, T, num_pages = 3, 37, 9
@@ -147,7 +148,6 @@ def test_append_places_rows_at_documented_offsets(P):
     slots = rng.permutation(num_pages * P)[:T].astype(np.int64)
     slots[5] = -1  # skipped
     oracle.quantize_append(pool, to_bf16_bits(k), to_bf16_bits(v), slots)
-    off = _layout_offsets(P)
     touched = np.zeros((num_pages, P), dtype=bool)
     for t in range(T):
         if slots[t] < 0:
@@ -157,8 +157,8 @@ def test_append_places_rows_at_documented_offsets(P):
         for h in range(Hkv):
             slab = pool.data[page, h]
             for name, src in (("k", k[t, h]), ("v", v[t, h])):
-                q = slab[off[name + "q"] + row * 64: off[name + "q"] + row * 64 + 64]
-                s = [slab[_scale_index(P, name, row, j)] for j in range(8)]
+                q = slab[_code_off(name, row): _code_off(name, row) + 64]
+                s = [slab[_scale_index(name, row, j)] for j in range(8)]
                 vals = np.empty(128)
                 for d in range(128):
                     code = (q[d // 2] >> (4 * (d % 2))) & 15
@@ -172,8 +172,8 @@ def test_append_places_rows_at_documented_offsets(P):
             for h in range(Hkv):
                 slab = pool.data[page, h]
                 for name in ("k", "v"):
-                    assert np.all(slab[off[name + "q"] + row * 64: off[name + "q"] + row * 64 + 64] == 0xAB)
-                    assert all(slab[_scale_index(P, name, row, j)] == 0xAB for j in range(8))
+                    assert np.all(slab[_code_off(name, row): _code_off(name, row) + 64] == 0xAB)
+                    assert all(slab[_scale_index(name, row, j)] == 0xAB for j in range(8))
 
 
 def test_append_rejects_out_of_range_slot():
@@ -197,6 +197,7 @@ def test_fp8_append_matches_torch_cast():
         for t in range(T):
             page, row = divmod(int(slots[t]), P)
             for h in range(Hkv):
-                base = 0 if name == "k" else 128 * P
-                got = pool.data[page, h, base + row * 128: base + row * 128 + 128]
+                grp, r = divmod(row, 16)
+                base = grp * 4096 + (0 if name == "k" else 2048) + r * 128
+                got = pool.data[page, h, base: base + 128]
                 assert np.array_equal(got, ref[t, h])
