@@ -128,34 +128,47 @@ __device__ __forceinline__ void cursor_next(Cursor &cu, const DecodeArgs &a) {
     if (cu.b < a.B) cursor_seq(cu, a);
 }
 
-// Page of this warp's group of the unit at `cu` (-2: the group lies past the
-// sequence end and is not fetched).
-__device__ __forceinline__ int32_t group_page(const DecodeArgs &a, const Cursor &cu, int warp) {
-    const int t = cu.ch * kChunk + 16 * warp;
-    if (t >= cu.n) return -2;
-    return __ldg(a.block_table + (int64_t)cu.b * a.max_pages + (t >> a.log2P));
+// Source of this warp's 16-token group of unit j of the CTA's range, as one
+// 64-bit code: the group's global address, 0 when the group lies past the
+// sequence end (nothing to fetch), 1 when its block-table entry is out of range.
+// Each lane of a warp computes one unit, so a warp resolves 32 upcoming units
+// (binary search over the chunk prefix, block-table read) long before their
+// copies are issued.
+template <int DTYPE>
+__device__ __forceinline__ uint64_t group_src(const DecodeArgs &a, int64_t u0, int nstages, int j, int warp) {
+    if (j >= nstages) return 0;
+    const int64_t u = u0 + j;
+    int lo = 0, hi = a.B - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if ((int64_t)a.Hkv * a.chunk_prefix[mid] <= u) lo = mid;
+        else hi = mid - 1;
+    }
+    const int nch = (int)(a.chunk_prefix[lo + 1] - a.chunk_prefix[lo]);
+    const int rem = (int)(u - (int64_t)a.Hkv * a.chunk_prefix[lo]);
+    const int kv = rem / nch, ch = rem - kv * nch;
+    const int n = clamp_len(a.seq_lens[lo], (int64_t)a.max_pages * a.P);
+    const int t = ch * kChunk + 16 * warp;
+    if (t >= n) return 0;
+    const int32_t pg = __ldg(a.block_table + (int64_t)lo * a.max_pages + (t >> a.log2P));
+    if (pg < 0 || (int64_t)pg >= a.num_pages) return 1;
+    return reinterpret_cast<uint64_t>(a.pool + ((int64_t)pg * a.Hkv + kv) * a.slab +
+                                      ((t & (a.P - 1)) >> 4) * Group<DTYPE>::kBytes);
 }
 
-// Lane 0: fetch this warp's group of unit `cu` into `dst`.
+// Lane 0: fetch one group (code from group_src) into `dst`.
 template <int DTYPE>
-__device__ __forceinline__ void issue_group(const DecodeArgs &a, const Cursor &cu, int warp, int32_t pg,
-                                            uint8_t *dst, uint64_t *full, int *valid) {
-    if (pg == -2) {  // nothing to fetch: the tile is skipped
-        *valid = 0;
-        mbar_arrive(full);
-        return;
-    }
-    if (pg < 0 || (int64_t)pg >= a.num_pages) {
-        flag_error(a.err, kErrPage);
+__device__ __forceinline__ void issue_group(const DecodeArgs &a, uint64_t src, uint8_t *dst, uint64_t *full,
+                                            int *valid) {
+    if (src <= 1) {  // nothing to fetch, or a bad page (flagged): the tile is skipped
+        if (src == 1) flag_error(a.err, kErrPage);
         *valid = 0;
         mbar_arrive(full);
         return;
     }
     *valid = 1;
-    const int row = (cu.ch * kChunk + 16 * warp) & (a.P - 1);
-    const uint8_t *src = a.pool + ((int64_t)pg * a.Hkv + cu.kv) * a.slab + (row >> 4) * Group<DTYPE>::kBytes;
     mbar_arrive_expect_tx(full, Group<DTYPE>::kBytes);
-    bulk_g2s(dst, src, Group<DTYPE>::kBytes, full);
+    bulk_g2s(dst, reinterpret_cast<const void *>(src), Group<DTYPE>::kBytes, full);
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -490,18 +503,19 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : 2) decode_kernel(Decod
     }
     __syncwarp();
 
-    // Producer cursor (lane 0 issues): the unit kDepth stages ahead.
-    Cursor pc = cc;
-    int32_t pg = -2;
+    // Sources of upcoming groups, one unit per lane: `cur` holds units
+    // 32k .. 32k+31 (the batch being issued), `nxt` the following 32.
+    uint64_t cur = group_src<DTYPE>(a, u0, nstages, lane, warp);
+    uint64_t nxt = group_src<DTYPE>(a, u0, nstages, 32 + lane, warp);
     int issued = 0;  // copies issued by this warp (for the drain after a timeout)
     {
         const int first = nstages < kDepth ? nstages : kDepth;
         for (int s = 0; s < first; s++) {
+            const uint64_t src = __shfl_sync(0xffffffffu, cur, s);
             if (lane == 0) {
-                issue_group<DTYPE>(a, pc, warp, group_page(a, pc, warp), ring + s * kGB, &full[s], &valid[s]);
+                issue_group<DTYPE>(a, src, ring + s * kGB, &full[s], &valid[s]);
                 issued++;
             }
-            cursor_next(pc, a);
         }
     }
 
@@ -511,8 +525,12 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : 2) decode_kernel(Decod
     bool aborted = false;
 
     for (int i = 0; i < nstages; i++) {
-        const bool refill = i + kDepth < nstages;         // pc = unit of stage i + kDepth
-        if (refill && lane == 0) pg = group_page(a, pc, warp);  // used after this tile
+        const int next_unit = i + kDepth;  // refilled into this slot after this tile
+        const bool refill = next_unit < nstages;
+        if (refill && (next_unit & 31) == 0) {  // entering the next batch of 32 units
+            cur = nxt;
+            nxt = group_src<DTYPE>(a, u0, nstages, next_unit + 32 + lane, warp);
+        }
         if (seg_left == 0) {  // a new (sequence, kv_head) segment starts at this unit
             seg_left = min(cc.nch - cc.ch, nstages - i);
             load_q<NT>(a, cc.b, cc.kv, lane, qf, fac);
@@ -543,13 +561,13 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : 2) decode_kernel(Decod
         }
         __syncwarp();
         if (refill && !aborted) {
+            const uint64_t src = __shfl_sync(0xffffffffu, cur, next_unit & 31);
             if (lane == 0) {
                 fence_proxy_async_smem();
-                issue_group<DTYPE>(a, pc, warp, pg, ring + slot * kGB, &full[slot], &valid[slot]);
+                issue_group<DTYPE>(a, src, ring + slot * kGB, &full[slot], &valid[slot]);
                 issued++;
             }
         }
-        if (refill) cursor_next(pc, a);
 
         if (--seg_left > 0) {
             cc.ch++;
