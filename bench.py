@@ -325,7 +325,7 @@ def time_append(m, device, steps, warmup):
     us = s.elapsed_time(e) / steps * 1e3
     nbytes = append_bytes(w.num_tokens, w.num_kv_heads, 144)
     return {"workload": w.name, "us_per_call": us, "gb_per_s": nbytes / us / 1e3, "algorithmic_bytes": nbytes,
-            "note": "inputs 268 MB > L2 is false (129 MB L2 holds part): back-to-back calls"}
+            "note": "back-to-back calls; 268 MB of BF16 input per call exceeds the 129 MB L2"}
 
 
 def run_ours(args):
