@@ -215,13 +215,17 @@ NVFP4KV_API int nvfp4_prefix_dequant(const nvfp4kv_cache *cache, const int32_t *
  * out-of-range index since the last check) or NVFP4KV_ECUDA. */
 NVFP4KV_API int nvfp4kv_check_device_errors(cudaStream_t stream);
 
-/* Benchmark hook: while enabled, the i-th nvfp4_paged_decode_attention call
- * records before[i % count] on its stream immediately before launching the
- * decode kernel and after[i % count] immediately after it, so the caller can
- * time that kernel alone with cudaEventElapsedTime.  The events are created
- * and owned by the caller; count = 0 (or NULL arrays) disables the hook and
- * resets i.  Process-wide and not thread-safe: for benchmarks only. */
-NVFP4KV_API int nvfp4kv_profile_decode(const cudaEvent_t *before, const cudaEvent_t *after, int count);
+/* Benchmark hook: while enabled, every `every`-th nvfp4_paged_decode_attention
+ * call (calls 0, every, 2*every, ...; the j-th of them uses pair j % count)
+ * records before[] on its stream immediately before launching the decode
+ * kernel and after[] immediately after it, so the caller can time that kernel
+ * alone with cudaEventElapsedTime while the calls in between run undisturbed
+ * (an event between the launches keeps the decode kernel from starting early
+ * under programmatic dependent launch).  The events are created and owned by
+ * the caller; count = 0 (or NULL arrays) disables the hook and resets the call
+ * counter; every < 1 is EINVAL.  Process-wide and not thread-safe: for
+ * benchmarks only. */
+NVFP4KV_API int nvfp4kv_profile_decode(const cudaEvent_t *before, const cudaEvent_t *after, int count, int every);
 
 /* Static description of a status code. */
 NVFP4KV_API const char *nvfp4kv_status_string(int status);

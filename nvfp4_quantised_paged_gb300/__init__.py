@@ -64,7 +64,7 @@ def _load_library():
         "nvfp4_paged_decode_attention": (i32, [D, P, i32, i32, P, i32, P, f32, P, P, sz, i32, P]),
         "nvfp4_prefix_dequant": (i32, [D, P, i32, P, P, i32, i64, P, P, P]),
         "nvfp4kv_check_device_errors": (i32, [P]),
-        "nvfp4kv_profile_decode": (i32, [P, P, i32]),
+        "nvfp4kv_profile_decode": (i32, [P, P, i32, i32]),
         "nvfp4_paged_decode_attention_noalloc": (i32, [D, P, i32, i32, P, i32, P, f32, P, i32, P]),
     }
     for name, (res, args) in sig.items():
@@ -257,11 +257,12 @@ def prefix_dequant(cache: PagedCache, block_table: torch.Tensor, prefix_lens: to
     return k_ws, v_ws
 
 
-def profile_decode(before, after):
-    """Benchmark hook: record torch.cuda.Event pairs around each following
-    decode-kernel launch (call i uses pair i % len).  Pass empty lists to stop."""
+def profile_decode(before, after, every: int = 1):
+    """Benchmark hook: record torch.cuda.Event pairs around the decode-kernel
+    launch of every `every`-th following call (the j-th such call uses pair
+    j % len).  Pass empty lists to stop."""
     if not before:
-        _check(_lib.nvfp4kv_profile_decode(None, None, 0), "nvfp4kv_profile_decode")
+        _check(_lib.nvfp4kv_profile_decode(None, None, 0, 1), "nvfp4kv_profile_decode")
         return
     n = len(before)
     assert len(after) == n
@@ -270,7 +271,7 @@ def profile_decode(before, after):
             e.record()
     arr_b = (ctypes.c_void_p * n)(*[e.cuda_event for e in before])
     arr_a = (ctypes.c_void_p * n)(*[e.cuda_event for e in after])
-    _check(_lib.nvfp4kv_profile_decode(arr_b, arr_a, n), "nvfp4kv_profile_decode")
+    _check(_lib.nvfp4kv_profile_decode(arr_b, arr_a, n, int(every)), "nvfp4kv_profile_decode")
 
 
 def check_device_errors(stream: Optional[torch.cuda.Stream] = None) -> int:

@@ -72,6 +72,7 @@ int from_cuda(cudaError_t e) { return e == cudaSuccess ? NVFP4KV_OK : NVFP4KV_EC
 // Benchmark hook state (nvfp4kv_profile_decode).
 std::vector<cudaEvent_t> g_prof_before, g_prof_after;
 size_t g_prof_next = 0;
+size_t g_prof_every = 1;
 
 }  // namespace
 
@@ -159,9 +160,12 @@ int nvfp4_paged_decode_attention(const nvfp4kv_cache *cache, const void *q, int 
     if (!err) return NVFP4KV_ECUDA;
     cudaEvent_t before = nullptr, after = nullptr;
     if (!g_prof_before.empty()) {
-        const size_t i = g_prof_next++ % g_prof_before.size();
-        before = g_prof_before[i];
-        after = g_prof_after[i];
+        const size_t call = g_prof_next++;
+        if (call % g_prof_every == 0) {
+            const size_t i = (call / g_prof_every) % g_prof_before.size();
+            before = g_prof_before[i];
+            after = g_prof_after[i];
+        }
     }
     return from_cuda(launch_decode(*cache, q, batch, num_q_heads, block_table, max_pages_per_seq, seq_lens, sm_scale,
                                    out, workspace, grid, err, stream, before, after));
@@ -185,11 +189,13 @@ int nvfp4_prefix_dequant(const nvfp4kv_cache *cache, const int32_t *block_table,
                                            num_reqs, total_prefix_tokens, k_ws, v_ws, err, stream));
 }
 
-int nvfp4kv_profile_decode(const cudaEvent_t *before, const cudaEvent_t *after, int count) {
+int nvfp4kv_profile_decode(const cudaEvent_t *before, const cudaEvent_t *after, int count, int every) {
     g_prof_before.clear();
     g_prof_after.clear();
     g_prof_next = 0;
-    if (count < 0) return NVFP4KV_EINVAL;
+    g_prof_every = 1;
+    if (count < 0 || every < 1) return NVFP4KV_EINVAL;
+    g_prof_every = (size_t)every;
     if (count == 0 || !before || !after) return NVFP4KV_OK;
     for (int i = 0; i < count; i++) {
         if (!before[i] || !after[i]) {

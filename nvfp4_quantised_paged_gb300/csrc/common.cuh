@@ -171,6 +171,32 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
         : "memory");
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+//
+// A kernel launched with launch_pdl() may start while the previous kernel of
+// the stream is still running, once every CTA of that kernel has executed
+// pdl_launch_dependents() (or exited).  pdl_wait() blocks until the previous
+// kernel has completed and its memory operations are visible, so it must
+// come before the first access to anything that kernel (or earlier work)
+// writes.  Without a programmatic dependency both are no-ops.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+inline cudaError_t launch_pdl(const void *fn, unsigned grid, unsigned block, size_t smem, cudaStream_t stream,
+                              void **args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
 // ---------------------------------------------------------------- misc
 
 __host__ __device__ __forceinline__ int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }

@@ -12,17 +12,21 @@
 //     64-token chunks; all chunks of all pairs form one flat range that is cut
 //     into `grid` equal contiguous pieces, one per CTA (grid = SM count x
 //     resident CTAs for an auto split), so every CTA streams the same number
-//     of bytes whatever the mix of sequence lengths.  Each of the CTA's four
-//     warps takes one 16-token group of every chunk and leaves one
-//     (max, sum, acc) partial per pair it touched; a separate log-sum-exp
-//     reduction kernel merges the partials of a pair and normalises.
-//   * Staging.  Each warp runs its own 6-deep ring: lane 0 fetches its next
-//     16-token group (2,304 contiguous bytes for NVFP4) with one 1-D bulk (TMA)
-//     copy completed on an mbarrier, refilling a slot as soon as the warp has
-//     used it.  Warps never wait for one another.  With 4 CTAs per SM about
-//     180 KB are in flight per SM, what HBM latency under load needs.  Every
-//     wait is bounded and reports a timeout in the device error word instead
-//     of spinning forever.
+//     of bytes whatever the mix of sequence lengths.  A CTA is a single warp
+//     that takes whole chunks and leaves one (max, sum, acc) partial per pair
+//     it touched; a separate log-sum-exp reduction kernel merges the partials
+//     of a pair and normalises.
+//   * Staging.  Each CTA runs a 2-deep ring of chunk stages: lane 0 fetches
+//     the next chunk (9,216 contiguous bytes for NVFP4 when pages hold >= 64
+//     tokens, else one copy per page) with 1-D bulk (TMA) copies completed on
+//     an mbarrier, refilling a stage as soon as the warp has used it.  The
+//     lanes resolve the sources of the next 8-32 chunks (one page each) well
+//     ahead of their copies.  With 11 CTAs per SM about 200 KB of ring per SM
+//     keep HBM busy.  Every wait is bounded and reports a timeout in the
+//     device error word instead of spinning forever.
+//   * The four 16-token groups of a chunk are processed together, step by
+//     step, so their conversions and products interleave and the per-stage
+//     bookkeeping is paid once per 64 tokens.
 //   * Tensor cores on the real contraction only: per warp and 16 tokens,
 //     S^T (16 tokens x 8 query heads of the group) = K Q^T and
 //     O^T (128 dims x 8 heads) += V^T P^T with mma.sync m16n8k16, FP16 inputs
@@ -52,10 +56,10 @@ namespace nvfp4kv {
 
 namespace {
 
-constexpr int kWarps = 4;
-constexpr int kThreads = 32 * kWarps;
-constexpr int kDepth = 6;                  // per-warp ring depth (5 groups in flight)
-constexpr int kChunk = 64;                 // tokens per unit of the work split (one group per warp)
+constexpr int kThreads = 32;               // one warp per CTA
+constexpr int kChunk = 64;                 // tokens per unit of the work split (one ring stage)
+constexpr int kGroups = kChunk / 16;       // 16-token groups per stage
+constexpr int kDepth = 2;                  // ring depth: one stage computed while the next lands
 constexpr uint32_t kWaitLimit = 1u << 24;  // polls before a wait gives up (>= ~1 s)
 constexpr float kRescaleLog2 = 8.0f;
 constexpr float kNegInf = -__builtin_huge_valf();
@@ -74,12 +78,14 @@ struct Group<NVFP4KV_DTYPE_FP8_E4M3> {
     static constexpr int kKq = 0, kVq = 2048;
 };
 
+// Shared memory of one CTA (one warp): a kDepth-deep ring of 64-token stages,
+// their mbarriers and the mask of groups each stage holds.
 template <int DTYPE>
 struct Smem {
-    static constexpr int kRing = kDepth * Group<DTYPE>::kBytes;   // one ring per warp
-    static constexpr int kBars = kWarps * kRing;                   // u64 full[kWarps][kDepth]
-    static constexpr int kFlags = kBars + kWarps * kDepth * 8;     // int valid[kWarps][kDepth]
-    static constexpr int kTotal = kFlags + kWarps * kDepth * 4;
+    static constexpr int kStage = kGroups * Group<DTYPE>::kBytes;
+    static constexpr int kBars = kDepth * kStage;           // u64 full[kDepth]
+    static constexpr int kFlags = kBars + kDepth * 8;       // int valid[kDepth]
+    static constexpr int kTotal = kFlags + kDepth * 4;
 };
 
 struct DecodeArgs {
@@ -95,8 +101,8 @@ struct DecodeArgs {
     float score_log2;             // sm_scale * g_K * log2(e)
     float gv;
     __nv_bfloat16 *out;
-    float *part_acc;  // [slots][kWarps][G][128]
-    float2 *part_ml;  // [slots][kWarps][G]
+    float *part_acc;  // [slots][G][128]
+    float2 *part_ml;  // [slots][G]
     int grid;
     unsigned *err;
 };
@@ -128,14 +134,19 @@ __device__ __forceinline__ void cursor_next(Cursor &cu, const DecodeArgs &a) {
     if (cu.b < a.B) cursor_seq(cu, a);
 }
 
-// Source of this warp's 16-token group of unit j of the CTA's range, as one
-// 64-bit code: the group's global address, 0 when the group lies past the
-// sequence end (nothing to fetch), 1 when its block-table entry is out of range.
-// Each lane of a warp computes one unit, so a warp resolves 32 upcoming units
-// (binary search over the chunk prefix, block-table read) long before their
-// copies are issued.
+// A 64-token chunk spans npp = max(1, 64 / P) pages, so it is fetched as npp
+// parts of min(P, 64) tokens, each contiguous in its page's slab.  A part's
+// source is one 64-bit code: 0 when the part starts past the sequence end,
+// kBadPage when its block-table entry is out of range, else the global address
+// of its first group (256-byte aligned: groups are 2,304 or 4,096 bytes and the
+// pool is 256-byte aligned) plus the number of its groups holding tokens in the
+// low bits.  The 32 lanes of the warp resolve the parts of 32 / npp upcoming
+// units (binary search over the chunk prefix, block-table read) long before
+// their copies are issued.
+constexpr uint64_t kBadPage = 0xff;
+
 template <int DTYPE>
-__device__ __forceinline__ uint64_t group_src(const DecodeArgs &a, int64_t u0, int nstages, int j, int warp) {
+__device__ __forceinline__ uint64_t part_src(const DecodeArgs &a, int64_t u0, int nstages, int j, int part) {
     if (j >= nstages) return 0;
     const int64_t u = u0 + j;
     int lo = 0, hi = a.B - 1;
@@ -148,27 +159,76 @@ __device__ __forceinline__ uint64_t group_src(const DecodeArgs &a, int64_t u0, i
     const int rem = (int)(u - (int64_t)a.Hkv * a.chunk_prefix[lo]);
     const int kv = rem / nch, ch = rem - kv * nch;
     const int n = clamp_len(a.seq_lens[lo], (int64_t)a.max_pages * a.P);
-    const int t = ch * kChunk + 16 * warp;
+    const int span = a.P < kChunk ? a.P : kChunk;
+    const int t = ch * kChunk + part * span;
     if (t >= n) return 0;
     const int32_t pg = __ldg(a.block_table + (int64_t)lo * a.max_pages + (t >> a.log2P));
-    if (pg < 0 || (int64_t)pg >= a.num_pages) return 1;
+    if (pg < 0 || (int64_t)pg >= a.num_pages) return kBadPage;
+    const int ng = (min(span, n - t) + 15) >> 4;
     return reinterpret_cast<uint64_t>(a.pool + ((int64_t)pg * a.Hkv + kv) * a.slab +
-                                      ((t & (a.P - 1)) >> 4) * Group<DTYPE>::kBytes);
+                                      ((t & (a.P - 1)) >> 4) * Group<DTYPE>::kBytes) |
+           (uint64_t)ng;
 }
 
-// Lane 0: fetch one group (code from group_src) into `dst`.
+// Fetch one 64-token stage.  Every lane passes the codes of the stage's parts
+// (lanes first .. first + npp - 1 of `codes`); lane 0 issues one bulk copy per
+// part into `dst` and records which groups arrive in *valid (bit i = group i).
+// Groups that are not fetched (past the end, or a bad page, which is flagged)
+// are masked out of the tile arithmetic.
 template <int DTYPE>
-__device__ __forceinline__ void issue_group(const DecodeArgs &a, uint64_t src, uint8_t *dst, uint64_t *full,
-                                            int *valid) {
-    if (src <= 1) {  // nothing to fetch, or a bad page (flagged): the tile is skipped
-        if (src == 1) flag_error(a.err, kErrPage);
-        *valid = 0;
+__device__ __forceinline__ void issue_stage(const DecodeArgs &a, uint64_t codes, int first, int npp, int lane,
+                                            uint8_t *dst, uint64_t *full, int *valid) {
+    constexpr int kGB = Group<DTYPE>::kBytes;
+    if (npp == 1) {  // pages of >= 64 tokens: one copy (the common case, kept short)
+        uint64_t s0 = __shfl_sync(0xffffffffu, codes, first);
+        if (lane != 0) return;
+        if (s0 == kBadPage) {
+            flag_error(a.err, kErrPage);
+            s0 = 0;
+        }
+        const int ng = (int)(s0 & 0xff);
+        *valid = (1 << ng) - 1;
+        if (ng == 0) {
+            mbar_arrive(full);
+            return;
+        }
+        mbar_arrive_expect_tx(full, (uint32_t)ng * kGB);
+        bulk_g2s(dst, reinterpret_cast<const void *>(s0 & ~(uint64_t)0xff), (uint32_t)ng * kGB, full);
+        return;
+    }
+    const int gpp = kGroups / npp;  // groups per part
+    uint64_t src[kGroups];
+#pragma unroll
+    for (int p = 0; p < kGroups; p++) {
+        src[p] = 0;
+        if (p < npp) src[p] = __shfl_sync(0xffffffffu, codes, first + p);
+    }
+    if (lane != 0) return;
+    uint32_t tx = 0;
+    int mask = 0;
+#pragma unroll
+    for (int p = 0; p < kGroups; p++) {
+        if (src[p] == kBadPage) {
+            flag_error(a.err, kErrPage);
+            src[p] = 0;
+        }
+        const int ng = (int)(src[p] & 0xff);
+        tx += (uint32_t)ng * kGB;
+        mask |= ((1 << ng) - 1) << (p * gpp);
+    }
+    *valid = mask;
+    if (tx == 0) {
         mbar_arrive(full);
         return;
     }
-    *valid = 1;
-    mbar_arrive_expect_tx(full, Group<DTYPE>::kBytes);
-    bulk_g2s(dst, reinterpret_cast<const void *>(src), Group<DTYPE>::kBytes, full);
+    mbar_arrive_expect_tx(full, tx);
+#pragma unroll
+    for (int p = 0; p < kGroups; p++) {
+        const int ng = (int)(src[p] & 0xff);
+        if (ng)
+            bulk_g2s(dst + p * gpp * kGB, reinterpret_cast<const void *>(src[p] & ~(uint64_t)0xff), (uint32_t)ng * kGB,
+                     full);
+    }
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -245,33 +305,43 @@ __device__ __forceinline__ void load_q(const DecodeArgs &a, int b, int kv, int l
 constexpr int kLTile = 8;
 constexpr uint32_t kOnesF16x2 = 0x3c003c00u;
 
-// Online softmax on one 16-token S^T tile (rows g, g+8 of the lane; columns =
-// heads nt*8+2c, +1), producing the P^T operand of the P.V product.  Scores
-// are in base 2; the running max moves only when a score exceeds it by more
-// than 2^kRescaleLog2, so probabilities stay <= 2^8 (exact enough in FP16).
-template <int NT>
-__device__ __forceinline__ void softmax_tile(const float (&s)[NT][4], int g, int vt, const float (&fac)[NT][2],
-                                             float (&m_run)[NT][2], float (&o)[NT][9][4], uint32_t (&pb)[NT][2]) {
-    float x[NT][4];
+// Online softmax over T 16-token S^T tiles at once (rows g, g+8 of each tile;
+// columns = heads nt*8+2c, +1), producing the P^T operands of the P.V
+// products.  Scores are in base 2; the running max moves only when a score
+// exceeds it by more than 2^kRescaleLog2, so probabilities stay <= 2^8 (exact
+// enough in FP16) and most calls skip the cross-lane max and the rescale.
+// vt[t] = valid rows of tile t (0..16); tile 0 holds at least one.
+template <int NT, int T>
+__device__ __forceinline__ void softmax_tiles(const float (&s)[T][NT][4], int g, const int (&vt)[T],
+                                              const float (&fac)[NT][2], float (&m_run)[NT][2], float (&o)[NT][9][4],
+                                              uint32_t (&pb)[T][NT][2]) {
+    float x[T][NT][4];
     bool need = false;
 #pragma unroll
-    for (int nt = 0; nt < NT; nt++) {
+    for (int t = 0; t < T; t++)
 #pragma unroll
-        for (int e = 0; e < 4; e++) x[nt][e] = fmaf(s[nt][e], fac[nt][e & 1], -m_run[nt][e & 1]);
-        if (vt < 16) {
-            if (g >= vt) x[nt][0] = x[nt][1] = kNegInf;
-            if (g + 8 >= vt) x[nt][2] = x[nt][3] = kNegInf;
+        for (int nt = 0; nt < NT; nt++) {
+#pragma unroll
+            for (int e = 0; e < 4; e++) x[t][nt][e] = fmaf(s[t][nt][e], fac[nt][e & 1], -m_run[nt][e & 1]);
+            if (vt[t] < 16) {
+                if (g >= vt[t]) x[t][nt][0] = x[t][nt][1] = kNegInf;
+                if (g + 8 >= vt[t]) x[t][nt][2] = x[t][nt][3] = kNegInf;
+            }
+#pragma unroll
+            for (int e = 0; e < 4; e++) need |= x[t][nt][e] > kRescaleLog2;  // +inf on a segment's first stage
         }
-#pragma unroll
-        for (int e = 0; e < 4; e++) need |= x[nt][e] > kRescaleLog2;  // +inf on the first tile
-    }
     if (__any_sync(0xffffffffu, need)) {
 #pragma unroll
         for (int nt = 0; nt < NT; nt++) {
-            float y[4];
+            float y[T][4];
+            float t0 = kNegInf, t1 = kNegInf;
 #pragma unroll
-            for (int e = 0; e < 4; e++) y[e] = x[nt][e] == kNegInf ? kNegInf : s[nt][e] * fac[nt][e & 1];
-            float t0 = fmaxf(y[0], y[2]), t1 = fmaxf(y[1], y[3]);
+            for (int t = 0; t < T; t++) {
+#pragma unroll
+                for (int e = 0; e < 4; e++) y[t][e] = x[t][nt][e] == kNegInf ? kNegInf : s[t][nt][e] * fac[nt][e & 1];
+                t0 = fmaxf(t0, fmaxf(y[t][0], y[t][2]));
+                t1 = fmaxf(t1, fmaxf(y[t][1], y[t][3]));
+            }
 #pragma unroll
             for (int sh = 4; sh < 32; sh <<= 1) {
                 t0 = fmaxf(t0, __shfl_xor_sync(0xffffffffu, t0, sh));
@@ -288,110 +358,126 @@ __device__ __forceinline__ void softmax_tile(const float (&s)[NT][4], int g, int
                 o[nt][i][2] *= a0;
                 o[nt][i][3] *= a1;
             }
-            x[nt][0] = y[0] - n0;
-            x[nt][1] = y[1] - n1;
-            x[nt][2] = y[2] - n0;
-            x[nt][3] = y[3] - n1;
+#pragma unroll
+            for (int t = 0; t < T; t++) {
+                x[t][nt][0] = y[t][0] - n0;
+                x[t][nt][1] = y[t][1] - n1;
+                x[t][nt][2] = y[t][2] - n0;
+                x[t][nt][3] = y[t][3] - n1;
+            }
         }
     }
 #pragma unroll
-    for (int nt = 0; nt < NT; nt++) {
-        const float p0 = ex2(x[nt][0]), p1 = ex2(x[nt][1]), p2 = ex2(x[nt][2]), p3 = ex2(x[nt][3]);
-        pb[nt][0] = movmatrix_trans(f32x2_to_f16x2(p1, p0));
-        pb[nt][1] = movmatrix_trans(f32x2_to_f16x2(p3, p2));
-    }
+    for (int t = 0; t < T; t++)
+#pragma unroll
+        for (int nt = 0; nt < NT; nt++) {
+            const float p0 = ex2(x[t][nt][0]), p1 = ex2(x[t][nt][1]), p2 = ex2(x[t][nt][2]), p3 = ex2(x[t][nt][3]);
+            pb[t][nt][0] = movmatrix_trans(f32x2_to_f16x2(p1, p0));
+            pb[t][nt][1] = movmatrix_trans(f32x2_to_f16x2(p3, p2));
+        }
 }
 
-// One warp, one 16-token NVFP4 group (rows 0..15).  vt = valid rows (1..16).
-template <int NT>
-__device__ __forceinline__ void tile_nvfp4(const uint8_t *st, int vt, int lane, const uint32_t (&qf)[NT][8][2],
-                                           const float (&fac)[NT][2], float (&m_run)[NT][2], float (&o)[NT][9][4]) {
+// One warp, T consecutive 16-token NVFP4 groups (st = the first), written
+// step by step for all T tiles together so that their conversions and
+// products interleave.  vt[t] = valid rows of group t (0..16).
+template <int NT, int T>
+__device__ __forceinline__ void tiles_nvfp4(const uint8_t *st, const int (&vt)[T], int lane,
+                                            const uint32_t (&qf)[NT][8][2], const float (&fac)[NT][2],
+                                            float (&m_run)[NT][2], float (&o)[NT][9][4]) {
     using L = Group<NVFP4KV_DTYPE_NVFP4>;
     const int g = lane >> 2, c = lane & 3;
     // ---- S^T = K Q^T.  Lane loads channels 32c..32c+31 (16 bytes) of rows g, g+8.
-    const uint8_t *krow = st + L::kKq + g * 64 + 16 * c;
-    const uint4 kA = *reinterpret_cast<const uint4 *>(krow);
-    const uint4 kB = *reinterpret_cast<const uint4 *>(krow + 8 * 64);
-    const uint8_t *ks = st + L::kKs + g * 8 + 2 * c;
-    const uint32_t sA = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t *>(ks));
-    const uint32_t sB = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t *>(ks + 8 * 8));
-    const uint32_t sA_lo = __byte_perm(sA, 0, 0x1010), sA_hi = __byte_perm(sA, 0, 0x3232);
-    const uint32_t sB_lo = __byte_perm(sB, 0, 0x1010), sB_hi = __byte_perm(sB, 0, 0x3232);
-    const uint32_t kAw[4] = {kA.x, kA.y, kA.z, kA.w}, kBw[4] = {kB.x, kB.y, kB.z, kB.w};
-    float sacc[2][NT][4];
+    float s[T][NT][4];
 #pragma unroll
-    for (int x = 0; x < 2; x++)
+    for (int t = 0; t < T; t++) {
+        const uint8_t *gt = st + t * L::kBytes;
+        const uint8_t *krow = gt + L::kKq + g * 64 + 16 * c;
+        const uint4 kA = *reinterpret_cast<const uint4 *>(krow);
+        const uint4 kB = *reinterpret_cast<const uint4 *>(krow + 8 * 64);
+        const uint8_t *ks = gt + L::kKs + g * 8 + 2 * c;
+        const uint32_t sA = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t *>(ks));
+        const uint32_t sB = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t *>(ks + 8 * 8));
+        const uint32_t sA_lo = __byte_perm(sA, 0, 0x1010), sA_hi = __byte_perm(sA, 0, 0x3232);
+        const uint32_t sB_lo = __byte_perm(sB, 0, 0x1010), sB_hi = __byte_perm(sB, 0, 0x3232);
+        const uint32_t kAw[4] = {kA.x, kA.y, kA.z, kA.w}, kBw[4] = {kB.x, kB.y, kB.z, kB.w};
+        float sacc[2][NT][4];
+#pragma unroll
+        for (int x = 0; x < 2; x++)
+#pragma unroll
+            for (int nt = 0; nt < NT; nt++)
+#pragma unroll
+                for (int e = 0; e < 4; e++) sacc[x][nt][e] = 0.f;
+#pragma unroll
+        for (int m = 0; m < 4; m++) {  // word m = bytes 4m..4m+3 = k-steps 2m, 2m+1; block 2c + (m >= 2)
+            uint32_t fa[4], fb[4];
+            e2m1x8_to_f16x2x4(kAw[m], fa[0], fa[1], fa[2], fa[3]);
+            e2m1x8_to_f16x2x4(kBw[m], fb[0], fb[1], fb[2], fb[3]);
+            const uint32_t sa = m < 2 ? sA_lo : sA_hi, sb = m < 2 ? sB_lo : sB_hi;
+#pragma unroll
+            for (int e = 0; e < 4; e++) {
+                fa[e] = hmul2(fa[e], sa);
+                fb[e] = hmul2(fb[e], sb);
+            }
+#pragma unroll
+            for (int nt = 0; nt < NT; nt++) {
+                mma_f16_16816(sacc[0][nt], fa[0], fb[0], fa[1], fb[1], qf[nt][2 * m][0], qf[nt][2 * m][1]);
+                mma_f16_16816(sacc[1][nt], fa[2], fb[2], fa[3], fb[3], qf[nt][2 * m + 1][0], qf[nt][2 * m + 1][1]);
+            }
+        }
 #pragma unroll
         for (int nt = 0; nt < NT; nt++)
 #pragma unroll
-            for (int e = 0; e < 4; e++) sacc[x][nt][e] = 0.f;
-#pragma unroll
-    for (int m = 0; m < 4; m++) {  // word m = bytes 4m..4m+3 = k-steps 2m, 2m+1; block 2c + (m >= 2)
-        uint32_t fa[4], fb[4];
-        e2m1x8_to_f16x2x4(kAw[m], fa[0], fa[1], fa[2], fa[3]);
-        e2m1x8_to_f16x2x4(kBw[m], fb[0], fb[1], fb[2], fb[3]);
-        const uint32_t sa = m < 2 ? sA_lo : sA_hi, sb = m < 2 ? sB_lo : sB_hi;
-#pragma unroll
-        for (int e = 0; e < 4; e++) {
-            fa[e] = hmul2(fa[e], sa);
-            fb[e] = hmul2(fb[e], sb);
-        }
-#pragma unroll
-        for (int nt = 0; nt < NT; nt++) {
-            mma_f16_16816(sacc[0][nt], fa[0], fb[0], fa[1], fb[1], qf[nt][2 * m][0], qf[nt][2 * m][1]);
-            mma_f16_16816(sacc[1][nt], fa[2], fb[2], fa[3], fb[3], qf[nt][2 * m + 1][0], qf[nt][2 * m + 1][1]);
-        }
+            for (int e = 0; e < 4; e++) s[t][nt][e] = sacc[0][nt][e] + sacc[1][nt][e];
     }
-    float s[NT][4];
-#pragma unroll
-    for (int nt = 0; nt < NT; nt++)
-#pragma unroll
-        for (int e = 0; e < 4; e++) s[nt][e] = sacc[0][nt][e] + sacc[1][nt][e];
-    uint32_t pb[NT][2];
-    softmax_tile<NT>(s, g, vt, fac, m_run, o, pb);
+    uint32_t pb[T][NT][2];
+    softmax_tiles<NT, T>(s, g, vt, fac, m_run, o, pb);
 
     // ---- O^T += V^T P^T.  Lane owns channels 16g..16g+15 (block g) of tokens 2c, 2c+1, 2c+8, 2c+9.
-    const uint8_t *vrow = st + L::kVq + (2 * c) * 64 + 8 * g;
-    uint2 v0 = *reinterpret_cast<const uint2 *>(vrow);
-    uint2 v1 = *reinterpret_cast<const uint2 *>(vrow + 64);
-    uint2 v2 = *reinterpret_cast<const uint2 *>(vrow + 8 * 64);
-    uint2 v3 = *reinterpret_cast<const uint2 *>(vrow + 9 * 64);
-    const uint8_t *vs = st + L::kVs + g * 16 + 2 * c;  // V scales [8][16]: rows 2c, 2c+1 and 2c+8, 2c+9
-    uint32_t vs01 = *reinterpret_cast<const uint16_t *>(vs);
-    uint32_t vs23 = *reinterpret_cast<const uint16_t *>(vs + 8);
-    if (vt < 16) {  // rows past the sequence end may hold stale bytes: zero codes and scales
-        const int j = 2 * c;
-        if (j >= vt) { v0 = make_uint2(0, 0); vs01 &= 0xff00u; }
-        if (j + 1 >= vt) { v1 = make_uint2(0, 0); vs01 &= 0x00ffu; }
-        if (j + 8 >= vt) { v2 = make_uint2(0, 0); vs23 &= 0xff00u; }
-        if (j + 9 >= vt) { v3 = make_uint2(0, 0); vs23 &= 0x00ffu; }
-    }
-    const uint32_t sv01 = e4m3x2_to_f16x2(vs01), sv23 = e4m3x2_to_f16x2(vs23);
-    // swap nibbles so each byte holds (token a, token b) of one channel
-    const uint32_t M = 0x0f0f0f0fu;
-    const uint32_t E[4] = {bitsel(M, v0.x, v1.x << 4), bitsel(M, v0.y, v1.y << 4), bitsel(M, v2.x, v3.x << 4),
-                           bitsel(M, v2.y, v3.y << 4)};
-    const uint32_t O[4] = {bitsel(M, v0.x >> 4, v1.x), bitsel(M, v0.y >> 4, v1.y), bitsel(M, v2.x >> 4, v3.x),
-                           bitsel(M, v2.y >> 4, v3.y)};
 #pragma unroll
-    for (int half = 0; half < 2; half++) {  // m-tiles 4*half .. 4*half+3
-        uint32_t e01[4], o01[4], e23[4], o23[4];
-        e2m1x8_to_f16x2x4(E[half], e01[0], e01[1], e01[2], e01[3]);
-        e2m1x8_to_f16x2x4(O[half], o01[0], o01[1], o01[2], o01[3]);
-        e2m1x8_to_f16x2x4(E[2 + half], e23[0], e23[1], e23[2], e23[3]);
-        e2m1x8_to_f16x2x4(O[2 + half], o23[0], o23[1], o23[2], o23[3]);
-#pragma unroll
-        for (int q = 0; q < 4; q++) {
-            const int i = 4 * half + q;  // m-tile i: rows g -> channel 16g+2i, g+8 -> 16g+2i+1
-            const uint32_t A0 = hmul2(e01[q], sv01), A1 = hmul2(o01[q], sv01);
-            const uint32_t A2 = hmul2(e23[q], sv23), A3 = hmul2(o23[q], sv23);
-#pragma unroll
-            for (int nt = 0; nt < NT; nt++) mma_f16_16816(o[nt][i], A0, A1, A2, A3, pb[nt][0], pb[nt][1]);
+    for (int t = 0; t < T; t++) {
+        const uint8_t *gt = st + t * L::kBytes;
+        const uint8_t *vrow = gt + L::kVq + (2 * c) * 64 + 8 * g;
+        uint2 v0 = *reinterpret_cast<const uint2 *>(vrow);
+        uint2 v1 = *reinterpret_cast<const uint2 *>(vrow + 64);
+        uint2 v2 = *reinterpret_cast<const uint2 *>(vrow + 8 * 64);
+        uint2 v3 = *reinterpret_cast<const uint2 *>(vrow + 9 * 64);
+        const uint8_t *vs = gt + L::kVs + g * 16 + 2 * c;  // V scales [8][16]: rows 2c, 2c+1 and 2c+8, 2c+9
+        uint32_t vs01 = *reinterpret_cast<const uint16_t *>(vs);
+        uint32_t vs23 = *reinterpret_cast<const uint16_t *>(vs + 8);
+        if (vt[t] < 16) {  // rows past the end or not fetched may hold stale bytes: zero codes and scales
+            const int j = 2 * c;
+            if (j >= vt[t]) { v0 = make_uint2(0, 0); vs01 &= 0xff00u; }
+            if (j + 1 >= vt[t]) { v1 = make_uint2(0, 0); vs01 &= 0x00ffu; }
+            if (j + 8 >= vt[t]) { v2 = make_uint2(0, 0); vs23 &= 0xff00u; }
+            if (j + 9 >= vt[t]) { v3 = make_uint2(0, 0); vs23 &= 0x00ffu; }
         }
-    }
+        const uint32_t sv01 = e4m3x2_to_f16x2(vs01), sv23 = e4m3x2_to_f16x2(vs23);
+        // swap nibbles so each byte holds (token a, token b) of one channel
+        const uint32_t M = 0x0f0f0f0fu;
+        const uint32_t E[4] = {bitsel(M, v0.x, v1.x << 4), bitsel(M, v0.y, v1.y << 4), bitsel(M, v2.x, v3.x << 4),
+                               bitsel(M, v2.y, v3.y << 4)};
+        const uint32_t O[4] = {bitsel(M, v0.x >> 4, v1.x), bitsel(M, v0.y >> 4, v1.y), bitsel(M, v2.x >> 4, v3.x),
+                               bitsel(M, v2.y >> 4, v3.y)};
 #pragma unroll
-    for (int nt = 0; nt < NT; nt++)
-        mma_f16_16816(o[nt][kLTile], kOnesF16x2, kOnesF16x2, kOnesF16x2, kOnesF16x2, pb[nt][0], pb[nt][1]);
+        for (int half = 0; half < 2; half++) {  // m-tiles 4*half .. 4*half+3
+            uint32_t e01[4], o01[4], e23[4], o23[4];
+            e2m1x8_to_f16x2x4(E[half], e01[0], e01[1], e01[2], e01[3]);
+            e2m1x8_to_f16x2x4(O[half], o01[0], o01[1], o01[2], o01[3]);
+            e2m1x8_to_f16x2x4(E[2 + half], e23[0], e23[1], e23[2], e23[3]);
+            e2m1x8_to_f16x2x4(O[2 + half], o23[0], o23[1], o23[2], o23[3]);
+#pragma unroll
+            for (int q = 0; q < 4; q++) {
+                const int i = 4 * half + q;  // m-tile i: rows g -> channel 16g+2i, g+8 -> 16g+2i+1
+                const uint32_t A0 = hmul2(e01[q], sv01), A1 = hmul2(o01[q], sv01);
+                const uint32_t A2 = hmul2(e23[q], sv23), A3 = hmul2(o23[q], sv23);
+#pragma unroll
+                for (int nt = 0; nt < NT; nt++) mma_f16_16816(o[nt][i], A0, A1, A2, A3, pb[t][nt][0], pb[t][nt][1]);
+            }
+        }
+#pragma unroll
+        for (int nt = 0; nt < NT; nt++)
+            mma_f16_16816(o[nt][kLTile], kOnesF16x2, kOnesF16x2, kOnesF16x2, kOnesF16x2, pb[t][nt][0], pb[t][nt][1]);
+    }
 }
 
 // One warp, one 16-token FP8 group.
@@ -422,13 +508,15 @@ __device__ __forceinline__ void tile_fp8(const uint8_t *st, int vt, int lane, co
 #pragma unroll
         for (int nt = 0; nt < NT; nt++) mma_f16_16816(sacc[j & 1][nt], A0, A1, A2, A3, qf[nt][j][0], qf[nt][j][1]);
     }
-    float s[NT][4];
+    float s[1][NT][4];
 #pragma unroll
     for (int nt = 0; nt < NT; nt++)
 #pragma unroll
-        for (int e = 0; e < 4; e++) s[nt][e] = sacc[0][nt][e] + sacc[1][nt][e];
-    uint32_t pb[NT][2];
-    softmax_tile<NT>(s, g, vt, fac, m_run, o, pb);
+        for (int e = 0; e < 4; e++) s[0][nt][e] = sacc[0][nt][e] + sacc[1][nt][e];
+    uint32_t pb1[1][NT][2];
+    const int vt1[1] = {vt};
+    softmax_tiles<NT, 1>(s, g, vt1, fac, m_run, o, pb1);
+    const uint32_t(&pb)[NT][2] = pb1[0];
 
     // V: lane owns channels 16g..16g+15 (16 bytes) of tokens 2c, 2c+1, 2c+8, 2c+9.
     const uint8_t *vrow = st + L::kVq + (2 * c) * 128 + 16 * g;
@@ -460,12 +548,15 @@ __device__ __forceinline__ void tile_fp8(const uint8_t *st, int vt, int lane, co
         mma_f16_16816(o[nt][kLTile], kOnesF16x2, kOnesF16x2, kOnesF16x2, kOnesF16x2, pb[nt][0], pb[nt][1]);
 }
 
+// One CTA = one warp: streams its contiguous range of 64-token units through
+// a kDepth-deep ring of stages, one unit per stage.
 template <int DTYPE, int NT>
-__global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : 2) decode_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(kThreads, NT == 1 ? 12 : 6) decode_kernel(DecodeArgs a) {
     using S = Smem<DTYPE>;
-    constexpr int kGB = Group<DTYPE>::kBytes;
     extern __shared__ __align__(128) uint8_t smem[];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int lane = threadIdx.x;
+    pdl_launch_dependents();  // the reduction may be scheduled once every CTA runs
+    pdl_wait();               // chunk_prefix comes from the plan kernel
 
     const int64_t U = (int64_t)a.Hkv * a.chunk_prefix[a.B];
     const int64_t c = blockIdx.x;
@@ -473,10 +564,9 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : 2) decode_kernel(Decod
     if (u0 >= u1) return;
     const int nstages = (int)(u1 - u0);
 
-    // this warp's ring, barriers and flags
-    uint8_t *ring = smem + warp * S::kRing;
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + S::kBars) + warp * kDepth;
-    int *valid = reinterpret_cast<int *>(smem + S::kFlags) + warp * kDepth;
+    uint8_t *ring = smem;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + S::kBars);
+    int *valid = reinterpret_cast<int *>(smem + S::kFlags);
 
     // Locate the first unit: the last sequence b whose first unit is <= u0.
     Cursor cc;
@@ -503,19 +593,20 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : 2) decode_kernel(Decod
     }
     __syncwarp();
 
-    // Sources of upcoming groups, one unit per lane: `cur` holds units
-    // 32k .. 32k+31 (the batch being issued), `nxt` the following 32.
-    uint64_t cur = group_src<DTYPE>(a, u0, nstages, lane, warp);
-    uint64_t nxt = group_src<DTYPE>(a, u0, nstages, 32 + lane, warp);
-    int issued = 0;  // copies issued by this warp (for the drain after a timeout)
+    // Part sources of upcoming units: lane l resolves part l % npp of unit
+    // l / npp of a batch of upb = 32 / npp units; `cur` holds the batch being
+    // issued, `nxt` the following one.
+    const int lnpp = a.P >= kChunk ? 0 : (a.P == 32 ? 1 : 2);
+    const int npp = 1 << lnpp, upb = 32 >> lnpp;
+    const int my_unit = lane >> lnpp, my_part = lane & (npp - 1);
+    uint64_t cur = part_src<DTYPE>(a, u0, nstages, my_unit, my_part);
+    uint64_t nxt = part_src<DTYPE>(a, u0, nstages, upb + my_unit, my_part);
+    int issued = 0;  // stages issued (for the drain after a timeout)
     {
         const int first = nstages < kDepth ? nstages : kDepth;
         for (int s = 0; s < first; s++) {
-            const uint64_t src = __shfl_sync(0xffffffffu, cur, s);
-            if (lane == 0) {
-                issue_group<DTYPE>(a, src, ring + s * kGB, &full[s], &valid[s]);
-                issued++;
-            }
+            issue_stage<DTYPE>(a, cur, s << lnpp, npp, lane, ring + s * S::kStage, &full[s], &valid[s]);
+            issued++;
         }
     }
 
@@ -523,13 +614,16 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : 2) decode_kernel(Decod
     float fac[NT][2], m_run[NT][2], o[NT][9][4];
     int seg_left = 0;
     bool aborted = false;
+    int slot = 0;
+    uint32_t phase = 0;
 
     for (int i = 0; i < nstages; i++) {
-        const int next_unit = i + kDepth;  // refilled into this slot after this tile
+        const int next_unit = i + kDepth;  // refilled into this slot after this stage
         const bool refill = next_unit < nstages;
-        if (refill && (next_unit & 31) == 0) {  // entering the next batch of 32 units
+        const int in_batch = next_unit & (upb - 1);
+        if (refill && in_batch == 0) {  // entering the next batch
             cur = nxt;
-            nxt = group_src<DTYPE>(a, u0, nstages, next_unit + 32 + lane, warp);
+            nxt = part_src<DTYPE>(a, u0, nstages, next_unit + upb + my_unit, my_part);
         }
         if (seg_left == 0) {  // a new (sequence, kv_head) segment starts at this unit
             seg_left = min(cc.nch - cc.ch, nstages - i);
@@ -541,42 +635,54 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : 2) decode_kernel(Decod
                 for (int k = 0; k < 9; k++) o[nt][k][0] = o[nt][k][1] = o[nt][k][2] = o[nt][k][3] = 0.f;
             }
         }
-        const int slot = i % kDepth;
         bool ok = false;
         if (!aborted) {
-            ok = mbar_wait_bounded(&full[slot], (uint32_t)((i / kDepth) & 1), kWaitLimit, nullptr);
+            ok = mbar_wait_bounded(&full[slot], phase, kWaitLimit, nullptr);
             if (!ok) {
                 aborted = true;
                 if (lane == 0) flag_error(a.err, kErrTimeout);
             }
         }
-        if (ok && valid[slot]) {
-            const int left = cc.n - cc.ch * kChunk - 16 * warp;
-            const int vt = left < 16 ? left : 16;
-            const uint8_t *st = ring + slot * kGB;
-            if (DTYPE == NVFP4KV_DTYPE_NVFP4)
-                tile_nvfp4<NT>(st, vt, lane, qf, fac, m_run, o);
-            else
-                tile_fp8<NT>(st, vt, lane, qf, fac, m_run, o);
+        const int mask = ok ? valid[slot] : 0;
+        if (mask) {
+            const int left = cc.n - cc.ch * kChunk;
+            int vt[kGroups];
+#pragma unroll
+            for (int t = 0; t < kGroups; t++) vt[t] = max(0, min(16, left - 16 * t));
+            if (mask != (1 << min(kGroups, (left + 15) >> 4)) - 1) {  // a part was not fetched (bad page)
+#pragma unroll
+                for (int t = 0; t < kGroups; t++)
+                    if (!((mask >> t) & 1)) vt[t] = 0;
+            }
+            const uint8_t *st = ring + slot * S::kStage;
+            if (DTYPE == NVFP4KV_DTYPE_NVFP4) {
+                tiles_nvfp4<NT, kGroups>(st, vt, lane, qf, fac, m_run, o);
+            } else {
+#pragma unroll
+                for (int t = 0; t < kGroups; t++)
+                    if (vt[t] > 0) tile_fp8<NT>(st + t * Group<DTYPE>::kBytes, vt[t], lane, qf, fac, m_run, o);
+            }
         }
         __syncwarp();
         if (refill && !aborted) {
-            const uint64_t src = __shfl_sync(0xffffffffu, cur, next_unit & 31);
-            if (lane == 0) {
-                fence_proxy_async_smem();
-                issue_group<DTYPE>(a, src, ring + slot * kGB, &full[slot], &valid[slot]);
-                issued++;
-            }
+            if (lane == 0) fence_proxy_async_smem();
+            issue_stage<DTYPE>(a, cur, in_batch << lnpp, npp, lane, ring + slot * S::kStage, &full[slot],
+                               &valid[slot]);
+            issued++;
+        }
+        if (++slot == kDepth) {
+            slot = 0;
+            phase ^= 1u;
         }
 
         if (--seg_left > 0) {
             cc.ch++;
             continue;
         }
-        // end of this pair's segment inside the CTA: this warp's partial (max, sum, acc)
+        // end of this pair's segment inside the CTA: its partial (max, sum, acc)
         {
             const int g = lane >> 2, cq = lane & 3;
-            const int64_t pidx = (c + (int64_t)cc.b * a.Hkv + cc.kv) * kWarps + warp;
+            const int64_t pidx = c + (int64_t)cc.b * a.Hkv + cc.kv;
 #pragma unroll
             for (int nt = 0; nt < NT; nt++) {
 #pragma unroll
@@ -597,11 +703,11 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : 2) decode_kernel(Decod
         }
     }
 
-    // After a timeout, no copy of this warp may still be writing shared memory
-    // when the CTA exits: wait (bounded) for the last copy issued into each slot.
+    // After a timeout, no copy may still be writing shared memory when the
+    // CTA exits: wait (bounded) for the last stage issued into each slot.
     if (aborted && lane == 0) {
         for (int s = 0; s < kDepth && s < issued; s++) {
-            const int n = (issued - 1 - s) / kDepth + 1;  // copies issued into slot s
+            const int n = (issued - 1 - s) / kDepth + 1;  // stages issued into slot s
             mbar_wait_bounded(&full[s], (uint32_t)((n - 1) & 1), kWaitLimit, nullptr);
         }
     }
@@ -611,6 +717,8 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : 2) decode_kernel(Decod
 __global__ void __launch_bounds__(1024) plan_kernel(const int32_t *seq_lens, int B, int64_t max_tokens,
                                                     int64_t *prefix, unsigned *err) {
     __shared__ int64_t warp_sums[32];
+    pdl_launch_dependents();  // let the decode kernel launch; it waits for this one to finish
+    pdl_wait();               // seq_lens may come from earlier work on the stream
     const int tid = threadIdx.x;
     const int per = (B + 1023) / 1024;
     const int lo = min(B, tid * per), hi = min(B, lo + per);
@@ -660,56 +768,106 @@ struct ReduceArgs {
     __nv_bfloat16 *out;
 };
 
-// Log-sum-exp merge of the per-warp partials of every CTA that covered the
-// pair, then normalisation and the V tensor scale: one warp per (sequence,
-// query head).
-__global__ void __launch_bounds__(256) reduce_kernel(ReduceArgs a) {
-    const int lane = threadIdx.x & 31;
-    const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
-    if (row >= (int64_t)a.B * a.Hq) return;
-    const int b = (int)(row / a.Hq), h = (int)(row % a.Hq);
-    const int kv = h / a.G, hh = h % a.G;
-    const int64_t nch = a.chunk_prefix[b + 1] - a.chunk_prefix[b];
-    uint2 *dst = reinterpret_cast<uint2 *>(a.out + row * kHeadDim) + lane;
-    if (nch == 0) {
-        *dst = make_uint2(0u, 0u);
-        return;
-    }
-    const int64_t U = (int64_t)a.Hkv * a.chunk_prefix[a.B];
-    const int64_t off = (int64_t)a.Hkv * a.chunk_prefix[b] + (int64_t)kv * nch;
-    const int64_t c0 = ((off + 1) * a.grid - 1) / U;
-    const int64_t c1 = ((off + nch) * a.grid - 1) / U;
-    const int64_t p = (int64_t)b * a.Hkv + kv;
-    // CTAs with an empty range (possible when grid > U) wrote no partial
-    auto empty_cta = [&](int64_t cc) { return cc * U / a.grid == (cc + 1) * U / a.grid; };
-    float mx = kNegInf;
-    for (int64_t cc = c0; cc <= c1; cc++) {
-        if (empty_cta(cc)) continue;
+// Log-sum-exp merge of the partials of every CTA that covered a pair, then
+// normalisation and the V tensor scale.  A CTA of kReduceWarps warps serves
+// kReduceWarps / wpr output rows (sequence, query head) with wpr warps each:
+// the warps of a row split its partials (every wpr-th one, four loads in
+// flight), each keeping a running (max, sum, acc) with lane l owning dims
+// 4l..4l+3, and merge through shared memory.  The host picks wpr from the
+// average number of partials per pair: one warp per row when pairs are
+// covered by a handful of CTAs, all eight when a few long sequences are
+// spread over hundreds.
+constexpr int kReduceWarps = 8;
+
+__device__ __forceinline__ float lse_factor(float m, float mx) { return m == kNegInf ? 0.f : ex2(m - mx); }
+
+__global__ void __launch_bounds__(32 * kReduceWarps) reduce_kernel(ReduceArgs a, int wpr) {
+    __shared__ float4 s_acc[kReduceWarps][32];
+    __shared__ float s_m[kReduceWarps], s_l[kReduceWarps];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    pdl_wait();  // partials come from the decode kernel
+    const int64_t row = (int64_t)blockIdx.x * (kReduceWarps / wpr) + warp / wpr;
+    const int sub = warp % wpr;  // this warp's share of the row's partials
+    const bool live = row < (int64_t)a.B * a.Hq;
+    float m_w = kNegInf, l_w = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    int64_t nch = 0;
+    if (live) {
+        const int b = (int)(row / a.Hq), h = (int)(row % a.Hq);
+        const int kv = h / a.G, hh = h % a.G;
+        nch = a.chunk_prefix[b + 1] - a.chunk_prefix[b];
+        if (nch > 0) {
+            const int64_t U = (int64_t)a.Hkv * a.chunk_prefix[a.B];
+            const int64_t off = (int64_t)a.Hkv * a.chunk_prefix[b] + (int64_t)kv * nch;
+            const int64_t c0 = ((off + 1) * a.grid - 1) / U;
+            const int64_t c1 = ((off + nch) * a.grid - 1) / U;
+            const int64_t p = (int64_t)b * a.Hkv + kv;
+            // CTAs with an empty range (possible when grid > U) wrote no partial
+            auto empty_cta = [&](int64_t cc) { return cc * U / a.grid == (cc + 1) * U / a.grid; };
+            for (int64_t base = c0 + sub; base <= c1; base += 4 * wpr) {
+                float2 ml[4];
+                float4 v[4];
 #pragma unroll
-        for (int w = 0; w < kWarps; w++) mx = fmaxf(mx, a.part_ml[((cc + p) * kWarps + w) * a.G + hh].x);
-    }
-    float L = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
-    if (mx != kNegInf) {
-        for (int64_t cc = c0; cc <= c1; cc++) {
-            if (empty_cta(cc)) continue;
+                for (int k = 0; k < 4; k++) {
+                    const int64_t cc = base + (int64_t)k * wpr;
+                    ml[k] = make_float2(kNegInf, 0.f);
+                    v[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (cc <= c1 && !empty_cta(cc)) {
+                        const int64_t idx = (cc + p) * a.G + hh;
+                        ml[k] = a.part_ml[idx];
+                        v[k] = reinterpret_cast<const float4 *>(a.part_acc + idx * kHeadDim)[lane];
+                    }
+                }
+                float mx = m_w;
 #pragma unroll
-            for (int w = 0; w < kWarps; w++) {
-                const int64_t idx = ((cc + p) * kWarps + w) * a.G + hh;
-                const float2 ml = a.part_ml[idx];
-                const float f = ex2(ml.x - mx);
-                L += f * ml.y;
-                const float4 v = reinterpret_cast<const float4 *>(a.part_acc + idx * kHeadDim)[lane];
-                acc[0] += f * v.x;
-                acc[1] += f * v.y;
-                acc[2] += f * v.z;
-                acc[3] += f * v.w;
+                for (int k = 0; k < 4; k++) mx = fmaxf(mx, ml[k].x);
+                const float f0 = lse_factor(m_w, mx);
+                l_w *= f0;
+                acc.x *= f0;
+                acc.y *= f0;
+                acc.z *= f0;
+                acc.w *= f0;
+#pragma unroll
+                for (int k = 0; k < 4; k++) {
+                    const float f = lse_factor(ml[k].x, mx);
+                    l_w += f * ml[k].y;
+                    acc.x += f * v[k].x;
+                    acc.y += f * v[k].y;
+                    acc.z += f * v[k].z;
+                    acc.w += f * v[k].w;
+                }
+                m_w = mx;
             }
         }
     }
-    const float inv = L > 0.f ? a.gv / L : 0.f;
-    const __nv_bfloat162 lo2 = __floats2bfloat162_rn(acc[0] * inv, acc[1] * inv);
-    const __nv_bfloat162 hi2 = __floats2bfloat162_rn(acc[2] * inv, acc[3] * inv);
-    *dst = make_uint2(*reinterpret_cast<const uint32_t *>(&lo2), *reinterpret_cast<const uint32_t *>(&hi2));
+    if (wpr > 1) {
+        s_acc[warp][lane] = acc;
+        if (lane == 0) {
+            s_m[warp] = m_w;
+            s_l[warp] = l_w;
+        }
+        __syncthreads();
+        if (sub != 0) return;
+        float mx = kNegInf;
+        for (int w = 0; w < wpr; w++) mx = fmaxf(mx, s_m[warp + w]);
+        l_w = 0.f;
+        acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int w = 0; w < wpr; w++) {
+            const float f = lse_factor(s_m[warp + w], mx);
+            const float4 v = s_acc[warp + w][lane];
+            l_w += f * s_l[warp + w];
+            acc.x += f * v.x;
+            acc.y += f * v.y;
+            acc.z += f * v.z;
+            acc.w += f * v.w;
+        }
+    }
+    if (!live) return;
+    const float inv = l_w > 0.f ? a.gv / l_w : 0.f;  // a sequence of length 0 gets zeros
+    const __nv_bfloat162 lo2 = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+    const __nv_bfloat162 hi2 = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+    reinterpret_cast<uint2 *>(a.out + row * kHeadDim)[lane] =
+        make_uint2(*reinterpret_cast<const uint32_t *>(&lo2), *reinterpret_cast<const uint32_t *>(&hi2));
 }
 
 template <int DTYPE, int NT>
@@ -771,7 +929,7 @@ int decode_auto_grid(const nvfp4kv_cache &c, int group, cudaError_t *status) {
 
 size_t decode_workspace_bytes(const nvfp4kv_cache &c, int batch, int num_q_heads, int grid) {
     const int G = num_q_heads / c.num_kv_heads;
-    const size_t slots = ((size_t)grid + (size_t)batch * c.num_kv_heads) * kWarps;
+    const size_t slots = (size_t)grid + (size_t)batch * c.num_kv_heads;
     return align256(sizeof(int64_t) * ((size_t)batch + 1)) + align256(sizeof(float2) * slots * G) +
            sizeof(float) * slots * G * kHeadDim;
 }
@@ -785,14 +943,17 @@ cudaError_t launch_decode(const nvfp4kv_cache &c, const void *q, int batch, int 
     cudaError_t e = prepare_kernel(c.dtype, nt, nullptr);
     if (e != cudaSuccess) return e;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
-    const size_t slots = ((size_t)grid + (size_t)batch * c.num_kv_heads) * kWarps;
+    const size_t slots = (size_t)grid + (size_t)batch * c.num_kv_heads;
     int64_t *prefix = reinterpret_cast<int64_t *>(ws);
     float2 *part_ml = reinterpret_cast<float2 *>(ws + align256(sizeof(int64_t) * ((size_t)batch + 1)));
     float *part_acc = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(part_ml) + align256(sizeof(float2) * slots * G));
 
-    plan_kernel<<<1, 1024, 0, stream>>>(seq_lens, batch, (int64_t)max_pages * c.page_size, prefix, err);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    {
+        int64_t max_tokens = (int64_t)max_pages * c.page_size;
+        void *pargs[] = {&seq_lens, &batch, &max_tokens, &prefix, &err};
+        e = launch_pdl(reinterpret_cast<const void *>(&plan_kernel), 1, 1024, 0, stream, pargs);
+        if (e != cudaSuccess) return e;
+    }
 
     DecodeArgs a;
     a.pool = static_cast<const uint8_t *>(c.pool);
@@ -820,7 +981,7 @@ cudaError_t launch_decode(const nvfp4kv_cache &c, const void *q, int batch, int 
     const void *fn = select_kernel(c.dtype, nt, &smem);
     void *args[] = {&a};
     if (before && (e = cudaEventRecord(before, stream)) != cudaSuccess) return e;
-    e = cudaLaunchKernel(fn, dim3((unsigned)grid), dim3(kThreads), args, (size_t)smem, stream);
+    e = launch_pdl(fn, (unsigned)grid, kThreads, (size_t)smem, stream, args);
     if (e != cudaSuccess) return e;
     if (after && (e = cudaEventRecord(after, stream)) != cudaSuccess) return e;
 
@@ -836,8 +997,14 @@ cudaError_t launch_decode(const nvfp4kv_cache &c, const void *q, int batch, int 
     r.gv = c.v_global_scale;
     r.out = static_cast<__nv_bfloat16 *>(out);
     const int64_t rows = (int64_t)batch * num_q_heads;
-    reduce_kernel<<<(unsigned)ceil_div64(rows, 8), 256, 0, stream>>>(r);
-    return cudaGetLastError();
+    // warps per output row from the average number of partials per pair
+    const int64_t pairs = (int64_t)batch * c.num_kv_heads;
+    const int64_t avg_parts = (grid + 2 * pairs - 1) / pairs;
+    int wpr = avg_parts <= 4 ? 1 : avg_parts <= 8 ? 2 : avg_parts <= 16 ? 4 : 8;
+    const int64_t rows_per_cta = kReduceWarps / wpr;
+    void *rargs[] = {&r, &wpr};
+    return launch_pdl(reinterpret_cast<const void *>(&reduce_kernel), (unsigned)ceil_div64(rows, rows_per_cta),
+                      32 * kReduceWarps, 0, stream, rargs);
 }
 
 }  // namespace nvfp4kv

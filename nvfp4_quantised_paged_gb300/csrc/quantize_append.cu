@@ -104,6 +104,7 @@ __device__ __forceinline__ void quantize_block16(const uint4 &a, const uint4 &b,
 // Thread id -> (token, kv_head, which, block), block fastest.
 template <bool kUnitScale>
 __global__ void __launch_bounds__(256) append_nvfp4_kernel(AppendArgs a) {
+    pdl_launch_dependents();  // a dependent decode plan may launch early; it waits for this kernel
     // the host guarantees num_tokens * Hkv * 16 < 2^31
     const uint32_t id = blockIdx.x * blockDim.x + threadIdx.x;
     if (id >= (uint32_t)(a.num_tokens * a.Hkv * 16)) return;
@@ -136,6 +137,7 @@ __global__ void __launch_bounds__(256) append_nvfp4_kernel(AppendArgs a) {
 // FP8 pool: one thread converts one 16-value block to 16 E4M3 bytes.
 template <bool kUnitScale>
 __global__ void __launch_bounds__(256) append_fp8_kernel(AppendArgs a) {
+    pdl_launch_dependents();  // a dependent decode plan may launch early; it waits for this kernel
     // the host guarantees num_tokens * Hkv * 16 < 2^31
     const uint32_t id = blockIdx.x * blockDim.x + threadIdx.x;
     if (id >= (uint32_t)(a.num_tokens * a.Hkv * 16)) return;
