@@ -12,18 +12,22 @@
 //     64-token chunks; all chunks of all pairs form one flat range that is cut
 //     into `grid` equal contiguous pieces, one per CTA (grid = SM count x
 //     resident CTAs for an auto split), so every CTA streams the same number
-//     of bytes whatever the mix of sequence lengths.  A CTA is a single warp
-//     that takes whole chunks and leaves one (max, sum, acc) partial per pair
-//     it touched; a separate log-sum-exp reduction kernel merges the partials
-//     of a pair and normalises.
-//   * Staging.  Each CTA runs a 2-deep ring of chunk stages: lane 0 fetches
-//     the next chunk (9,216 contiguous bytes for NVFP4 when pages hold >= 64
-//     tokens, else one copy per page) with 1-D bulk (TMA) copies completed on
-//     an mbarrier, refilling a stage as soon as the warp has used it.  The
-//     lanes resolve the sources of the next 8-32 chunks (one page each) well
-//     ahead of their copies.  With 11 CTAs per SM about 200 KB of ring per SM
-//     keep HBM busy.  Every wait is bounded and reports a timeout in the
-//     device error word instead of spinning forever.
+//     of bytes whatever the mix of sequence lengths.  The two warps of a CTA
+//     take alternate chunks of its range and each leaves one (max, sum, acc)
+//     partial per pair it touched; a separate log-sum-exp reduction kernel
+//     merges the partials of a pair and normalises.
+//   * Staging.  The CTA's warps share a ring of three chunk stages: the warp
+//     that used a stage refills it (lane 0, one 1-D bulk (TMA) copy of 9,216
+//     contiguous bytes for NVFP4 when pages hold >= 64 tokens, else one copy
+//     per page, completed on the stage's mbarrier) with the chunk three
+//     places ahead, which belongs to the other warp, and publishes the chunk
+//     index so that a warp never waits on a barrier phase that belongs to an
+//     earlier use of the stage.  The lanes resolve the sources of the next
+//     8-32 refills (one page each) well ahead of their copies.  Eight CTAs
+//     (16 warps, 128 registers each) per SM hold ~220 KB of ring; the data of
+//     a chunk has always landed when its warp gets to it.  Every wait is
+//     bounded and reports a timeout in the device error word instead of
+//     spinning forever.
 //   * The four 16-token groups of a chunk are processed together, step by
 //     step, so their conversions and products interleave and the per-stage
 //     bookkeeping is paid once per 64 tokens.
@@ -56,10 +60,11 @@ namespace nvfp4kv {
 
 namespace {
 
-constexpr int kThreads = 32;               // one warp per CTA
+constexpr int kWarps = 2;                  // warps per CTA, sharing one ring
+constexpr int kThreads = 32 * kWarps;
 constexpr int kChunk = 64;                 // tokens per unit of the work split (one ring stage)
 constexpr int kGroups = kChunk / 16;       // 16-token groups per stage
-constexpr int kDepth = 2;                  // ring depth: one stage computed while the next lands
+constexpr int kSlots = 3;                  // ring stages per CTA: two computed, one landing
 constexpr uint32_t kWaitLimit = 1u << 24;  // polls before a wait gives up (>= ~1 s)
 constexpr float kRescaleLog2 = 8.0f;
 constexpr float kNegInf = -__builtin_huge_valf();
@@ -78,14 +83,17 @@ struct Group<NVFP4KV_DTYPE_FP8_E4M3> {
     static constexpr int kKq = 0, kVq = 2048;
 };
 
-// Shared memory of one CTA (one warp): a kDepth-deep ring of 64-token stages,
-// their mbarriers and the mask of groups each stage holds.
+// Shared memory of one CTA: a ring of kSlots 64-token stages, their
+// mbarriers, the mask of groups each stage holds, the index of the chunk last
+// issued into each stage, and an abort flag.
 template <int DTYPE>
 struct Smem {
     static constexpr int kStage = kGroups * Group<DTYPE>::kBytes;
-    static constexpr int kBars = kDepth * kStage;           // u64 full[kDepth]
-    static constexpr int kFlags = kBars + kDepth * 8;       // int valid[kDepth]
-    static constexpr int kTotal = kFlags + kDepth * 4;
+    static constexpr int kBars = kSlots * kStage;           // u64 full[kSlots]
+    static constexpr int kFlags = kBars + kSlots * 8;       // int valid[kSlots]
+    static constexpr int kSeq = kFlags + kSlots * 4;        // int seq[kSlots]
+    static constexpr int kAbort = kSeq + kSlots * 4;        // int abort
+    static constexpr int kTotal = kAbort + 4;
 };
 
 struct DecodeArgs {
@@ -101,8 +109,8 @@ struct DecodeArgs {
     float score_log2;             // sm_scale * g_K * log2(e)
     float gv;
     __nv_bfloat16 *out;
-    float *part_acc;  // [slots][G][128]
-    float2 *part_ml;  // [slots][G]
+    float *part_acc;  // [slots][kWarps][G][128]
+    float2 *part_ml;  // [slots][kWarps][G]
     int grid;
     unsigned *err;
 };
@@ -123,15 +131,19 @@ __device__ __forceinline__ void cursor_seq(Cursor &cu, const DecodeArgs &a) {
     cu.n = clamp_len(a.seq_lens[cu.b], (int64_t)a.max_pages * a.P);
 }
 
-__device__ __forceinline__ void cursor_next(Cursor &cu, const DecodeArgs &a) {
-    if (++cu.ch < cu.nch) return;
-    cu.ch = 0;
-    if (++cu.kv < a.Hkv) return;
-    cu.kv = 0;
-    do {
-        ++cu.b;
-    } while (cu.b < a.B && a.chunk_prefix[cu.b + 1] == a.chunk_prefix[cu.b]);
-    if (cu.b < a.B) cursor_seq(cu, a);
+// Move the cursor `steps` units forward (the caller keeps it inside the range).
+__device__ __forceinline__ void cursor_advance(Cursor &cu, const DecodeArgs &a, int steps) {
+    cu.ch += steps;
+    while (cu.ch >= cu.nch) {
+        cu.ch -= cu.nch;
+        if (++cu.kv < a.Hkv) continue;
+        cu.kv = 0;
+        do {
+            ++cu.b;
+        } while (cu.b < a.B && a.chunk_prefix[cu.b + 1] == a.chunk_prefix[cu.b]);
+        if (cu.b >= a.B) return;
+        cursor_seq(cu, a);
+    }
 }
 
 // A 64-token chunk spans npp = max(1, 64 / P) pages, so it is fetched as npp
@@ -548,13 +560,36 @@ __device__ __forceinline__ void tile_fp8(const uint8_t *st, int vt, int lane, co
         mma_f16_16816(o[nt][kLTile], kOnesF16x2, kOnesF16x2, kOnesF16x2, kOnesF16x2, pb[nt][0], pb[nt][1]);
 }
 
-// One CTA = one warp: streams its contiguous range of 64-token units through
-// a kDepth-deep ring of stages, one unit per stage.
+__device__ __forceinline__ void st_release_shared(int *p, int v) {
+    asm volatile("st.release.cta.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ int ld_acquire_shared(const int *p) {
+    int v;
+    asm volatile("ld.acquire.cta.shared::cta.b32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
+    return v;
+}
+
+// Bounded wait until chunk `want` has been issued into its stage (seq == want).
+__device__ __forceinline__ bool wait_issued(const int *seq, int want, const volatile int *abort) {
+    for (uint32_t it = 0; it < kWaitLimit; it++) {
+        if (ld_acquire_shared(seq) == want) return true;
+        if (*abort) return false;
+        if (it > 64) __nanosleep(64);
+    }
+    return false;
+}
+
+// A CTA streams its contiguous range of 64-token units through a ring of
+// kSlots stages shared by its kWarps warps: unit i of the range is computed
+// by warp i % kWarps from stage i % kSlots, and the warp that used a stage
+// refills it with unit i + kSlots.  Each warp keeps its own (max, sum, acc)
+// per pair and leaves its own partial.
 template <int DTYPE, int NT>
-__global__ void __launch_bounds__(kThreads, NT == 1 ? 12 : 6) decode_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(kThreads, DTYPE == NVFP4KV_DTYPE_NVFP4 && NT == 1 ? 8 : 4) decode_kernel(DecodeArgs a) {
     using S = Smem<DTYPE>;
     extern __shared__ __align__(128) uint8_t smem[];
-    const int lane = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     pdl_launch_dependents();  // the reduction may be scheduled once every CTA runs
     pdl_wait();               // chunk_prefix comes from the plan kernel
 
@@ -567,80 +602,112 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 12 : 6) decode_kernel(Deco
     uint8_t *ring = smem;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + S::kBars);
     int *valid = reinterpret_cast<int *>(smem + S::kFlags);
+    int *seq = reinterpret_cast<int *>(smem + S::kSeq);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + S::kAbort);
 
-    // Locate the first unit: the last sequence b whose first unit is <= u0.
+    if (tid == 0) {
+        for (int s = 0; s < kSlots; s++) {
+            mbar_init(&full[s], 1);
+            valid[s] = 0;
+            seq[s] = -1;
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    const int lnpp = a.P >= kChunk ? 0 : (a.P == 32 ? 1 : 2);
+    const int npp = 1 << lnpp, upb = 32 >> lnpp;
+    const int my_unit = lane >> lnpp, my_part = lane & (npp - 1);
+    if (warp == 0) {  // the first kSlots units
+        const uint64_t pro = my_unit < kSlots ? part_src<DTYPE>(a, u0, nstages, my_unit, my_part) : 0;
+        const int first = nstages < kSlots ? nstages : kSlots;
+        for (int s = 0; s < first; s++) {
+            issue_stage<DTYPE>(a, pro, s << lnpp, npp, lane, ring + s * S::kStage, &full[s], &valid[s]);
+            if (lane == 0) st_release_shared(&seq[s], s);
+        }
+    }
+
+    // This warp computes units warp + k * kWarps (k = 0, 1, ...) and after
+    // each refills its stage with unit warp + kSlots + k * kWarps.  Sources
+    // of the refills: lane l resolves part l % npp of refill k0 + l / npp;
+    // `cur` holds the batch of upb refills being issued, `nxt` the next one.
+    auto refill_unit = [&](int k) { return warp + kSlots + k * kWarps; };
+    uint64_t cur = part_src<DTYPE>(a, u0, nstages, refill_unit(my_unit), my_part);
+    uint64_t nxt = part_src<DTYPE>(a, u0, nstages, refill_unit(upb + my_unit), my_part);
+
     Cursor cc;
-    {
+    if (warp < nstages) {  // locate unit u0 + warp
+        const int64_t uw = u0 + warp;
         int lo = 0, hi = a.B - 1;
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
-            if ((int64_t)a.Hkv * a.chunk_prefix[mid] <= u0) lo = mid;
+            if ((int64_t)a.Hkv * a.chunk_prefix[mid] <= uw) lo = mid;
             else hi = mid - 1;
         }
         cc.b = lo;
         cursor_seq(cc, a);
-        const int rem = (int)(u0 - (int64_t)a.Hkv * a.chunk_prefix[lo]);
+        const int rem = (int)(uw - (int64_t)a.Hkv * a.chunk_prefix[lo]);
         cc.kv = rem / cc.nch;
         cc.ch = rem - cc.kv * cc.nch;
     }
 
-    if (lane == 0) {
-        for (int s = 0; s < kDepth; s++) {
-            mbar_init(&full[s], 1);
-            valid[s] = 0;
-        }
-        fence_mbar_init();
-    }
-    __syncwarp();
-
-    // Part sources of upcoming units: lane l resolves part l % npp of unit
-    // l / npp of a batch of upb = 32 / npp units; `cur` holds the batch being
-    // issued, `nxt` the following one.
-    const int lnpp = a.P >= kChunk ? 0 : (a.P == 32 ? 1 : 2);
-    const int npp = 1 << lnpp, upb = 32 >> lnpp;
-    const int my_unit = lane >> lnpp, my_part = lane & (npp - 1);
-    uint64_t cur = part_src<DTYPE>(a, u0, nstages, my_unit, my_part);
-    uint64_t nxt = part_src<DTYPE>(a, u0, nstages, upb + my_unit, my_part);
-    int issued = 0;  // stages issued (for the drain after a timeout)
-    {
-        const int first = nstages < kDepth ? nstages : kDepth;
-        for (int s = 0; s < first; s++) {
-            issue_stage<DTYPE>(a, cur, s << lnpp, npp, lane, ring + s * S::kStage, &full[s], &valid[s]);
-            issued++;
-        }
-    }
-
     uint32_t qf[NT][8][2];
     float fac[NT][2], m_run[NT][2], o[NT][9][4];
-    int seg_left = 0;
+    int64_t acc_pair = -1;  // pair whose partial this warp is accumulating
     bool aborted = false;
-    int slot = 0;
-    uint32_t phase = 0;
 
-    for (int i = 0; i < nstages; i++) {
-        const int next_unit = i + kDepth;  // refilled into this slot after this stage
-        const bool refill = next_unit < nstages;
-        const int in_batch = next_unit & (upb - 1);
-        if (refill && in_batch == 0) {  // entering the next batch
-            cur = nxt;
-            nxt = part_src<DTYPE>(a, u0, nstages, next_unit + upb + my_unit, my_part);
+    // this warp's partial of pair `pair`: (max, sum, acc)
+    auto write_partial = [&](int64_t pair) {
+        const int g = lane >> 2, cq = lane & 3;
+        const int64_t pidx = (c + pair) * kWarps + warp;
+#pragma unroll
+        for (int nt = 0; nt < NT; nt++) {
+#pragma unroll
+            for (int k = 0; k < 2; k++) {
+                const int h = nt * 8 + 2 * cq + k;
+                if (h >= a.G) continue;
+                if (g == 0) a.part_ml[pidx * a.G + h] = make_float2(m_run[nt][k], o[nt][kLTile][k]);
+                float *dst = a.part_acc + (pidx * a.G + h) * kHeadDim + 16 * g;
+#pragma unroll
+                for (int i2 = 0; i2 < 8; i2++)
+                    *reinterpret_cast<float2 *>(dst + 2 * i2) = make_float2(o[nt][i2][k], o[nt][i2][k + 2]);
+            }
         }
-        if (seg_left == 0) {  // a new (sequence, kv_head) segment starts at this unit
-            seg_left = min(cc.nch - cc.ch, nstages - i);
+    };
+
+    int k = 0;
+    for (int i = warp; i < nstages; i += kWarps, k++) {
+        const int j = i + kSlots;  // refilled into this stage after this unit
+        const bool refill = j < nstages;
+        const int in_batch = k & (upb - 1);
+        if (in_batch == 0 && k > 0) {  // entering the next batch of refills
+            cur = nxt;
+            nxt = part_src<DTYPE>(a, u0, nstages, refill_unit(k + upb + my_unit), my_part);
+        }
+        const int64_t pair = (int64_t)cc.b * a.Hkv + cc.kv;
+        if (pair != acc_pair) {  // this warp starts on a new (sequence, kv_head)
+            if (acc_pair >= 0) write_partial(acc_pair);
+            acc_pair = pair;
             load_q<NT>(a, cc.b, cc.kv, lane, qf, fac);
 #pragma unroll
             for (int nt = 0; nt < NT; nt++) {
                 m_run[nt][0] = m_run[nt][1] = kNegInf;
 #pragma unroll
-                for (int k = 0; k < 9; k++) o[nt][k][0] = o[nt][k][1] = o[nt][k][2] = o[nt][k][3] = 0.f;
+                for (int q = 0; q < 9; q++) o[nt][q][0] = o[nt][q][1] = o[nt][q][2] = o[nt][q][3] = 0.f;
             }
         }
+        const int slot = i % kSlots;
         bool ok = false;
         if (!aborted) {
-            ok = mbar_wait_bounded(&full[slot], phase, kWaitLimit, nullptr);
+            ok = wait_issued(&seq[slot], i, abort_flag) &&
+                 mbar_wait_bounded(&full[slot], (uint32_t)((i / kSlots) & 1), kWaitLimit, abort_flag);
             if (!ok) {
                 aborted = true;
-                if (lane == 0) flag_error(a.err, kErrTimeout);
+                if (lane == 0) {
+                    *abort_flag = 1;
+                    flag_error(a.err, kErrTimeout);
+                }
             }
         }
         const int mask = ok ? valid[slot] : 0;
@@ -668,47 +735,19 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 12 : 6) decode_kernel(Deco
             if (lane == 0) fence_proxy_async_smem();
             issue_stage<DTYPE>(a, cur, in_batch << lnpp, npp, lane, ring + slot * S::kStage, &full[slot],
                                &valid[slot]);
-            issued++;
+            if (lane == 0) st_release_shared(&seq[slot], j);
         }
-        if (++slot == kDepth) {
-            slot = 0;
-            phase ^= 1u;
-        }
-
-        if (--seg_left > 0) {
-            cc.ch++;
-            continue;
-        }
-        // end of this pair's segment inside the CTA: its partial (max, sum, acc)
-        {
-            const int g = lane >> 2, cq = lane & 3;
-            const int64_t pidx = c + (int64_t)cc.b * a.Hkv + cc.kv;
-#pragma unroll
-            for (int nt = 0; nt < NT; nt++) {
-#pragma unroll
-                for (int k = 0; k < 2; k++) {
-                    const int h = nt * 8 + 2 * cq + k;
-                    if (h >= a.G) continue;
-                    if (g == 0) a.part_ml[pidx * a.G + h] = make_float2(m_run[nt][k], o[nt][kLTile][k]);
-                    float *dst = a.part_acc + (pidx * a.G + h) * kHeadDim + 16 * g;
-#pragma unroll
-                    for (int i2 = 0; i2 < 8; i2++)
-                        *reinterpret_cast<float2 *>(dst + 2 * i2) = make_float2(o[nt][i2][k], o[nt][i2][k + 2]);
-                }
-            }
-        }
-        if (i + 1 < nstages) {  // move to the first chunk of the next pair
-            cc.ch = cc.nch - 1;
-            cursor_next(cc, a);
-        }
+        if (i + kWarps < nstages) cursor_advance(cc, a, kWarps);
     }
+    if (acc_pair >= 0) write_partial(acc_pair);
 
     // After a timeout, no copy may still be writing shared memory when the
-    // CTA exits: wait (bounded) for the last stage issued into each slot.
-    if (aborted && lane == 0) {
-        for (int s = 0; s < kDepth && s < issued; s++) {
-            const int n = (issued - 1 - s) / kDepth + 1;  // stages issued into slot s
-            mbar_wait_bounded(&full[s], (uint32_t)((n - 1) & 1), kWaitLimit, nullptr);
+    // CTA exits: wait (bounded) for the last chunk issued into each stage.
+    __syncthreads();
+    if (*abort_flag && tid == 0) {
+        for (int s = 0; s < kSlots; s++) {
+            const int last = seq[s];
+            if (last >= 0) mbar_wait_bounded(&full[s], (uint32_t)((last / kSlots) & 1), kWaitLimit, nullptr);
         }
     }
 }
@@ -802,18 +841,30 @@ __global__ void __launch_bounds__(32 * kReduceWarps) reduce_kernel(ReduceArgs a,
             const int64_t c0 = ((off + 1) * a.grid - 1) / U;
             const int64_t c1 = ((off + nch) * a.grid - 1) / U;
             const int64_t p = (int64_t)b * a.Hkv + kv;
-            // CTAs with an empty range (possible when grid > U) wrote no partial
-            auto empty_cta = [&](int64_t cc) { return cc * U / a.grid == (cc + 1) * U / a.grid; };
-            for (int64_t base = c0 + sub; base <= c1; base += 4 * wpr) {
+            // Candidate partials: (CTA cc, warp w) for cc in [c0, c1].  Warp w of
+            // CTA cc left one iff the CTA's units of this pair include one with
+            // index (within the CTA's range) = w mod kWarps; an empty CTA (possible
+            // when grid > U) left none.
+            auto has_partial = [&](int64_t cc, int w) {
+                const int64_t cu0 = cc * U / a.grid, cu1 = (cc + 1) * U / a.grid;
+                const int64_t lo = (off > cu0 ? off : cu0) - cu0;
+                const int64_t hi = (off + nch < cu1 ? off + nch : cu1) - cu0;
+                if (hi <= lo) return false;
+                return hi - lo > (int64_t)((w - lo % kWarps + kWarps) % kWarps);
+            };
+            const int64_t ncand = (c1 - c0 + 1) * kWarps;
+            for (int64_t base = sub; base < ncand; base += 4 * wpr) {
                 float2 ml[4];
                 float4 v[4];
 #pragma unroll
                 for (int k = 0; k < 4; k++) {
-                    const int64_t cc = base + (int64_t)k * wpr;
+                    const int64_t q = base + (int64_t)k * wpr;
                     ml[k] = make_float2(kNegInf, 0.f);
                     v[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (cc <= c1 && !empty_cta(cc)) {
-                        const int64_t idx = (cc + p) * a.G + hh;
+                    const int64_t cc = c0 + q / kWarps;
+                    const int w = (int)(q % kWarps);
+                    if (q < ncand && has_partial(cc, w)) {
+                        const int64_t idx = ((cc + p) * kWarps + w) * a.G + hh;
                         ml[k] = a.part_ml[idx];
                         v[k] = reinterpret_cast<const float4 *>(a.part_acc + idx * kHeadDim)[lane];
                     }
@@ -929,7 +980,7 @@ int decode_auto_grid(const nvfp4kv_cache &c, int group, cudaError_t *status) {
 
 size_t decode_workspace_bytes(const nvfp4kv_cache &c, int batch, int num_q_heads, int grid) {
     const int G = num_q_heads / c.num_kv_heads;
-    const size_t slots = (size_t)grid + (size_t)batch * c.num_kv_heads;
+    const size_t slots = ((size_t)grid + (size_t)batch * c.num_kv_heads) * kWarps;
     return align256(sizeof(int64_t) * ((size_t)batch + 1)) + align256(sizeof(float2) * slots * G) +
            sizeof(float) * slots * G * kHeadDim;
 }
@@ -943,7 +994,7 @@ cudaError_t launch_decode(const nvfp4kv_cache &c, const void *q, int batch, int 
     cudaError_t e = prepare_kernel(c.dtype, nt, nullptr);
     if (e != cudaSuccess) return e;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
-    const size_t slots = (size_t)grid + (size_t)batch * c.num_kv_heads;
+    const size_t slots = ((size_t)grid + (size_t)batch * c.num_kv_heads) * kWarps;
     int64_t *prefix = reinterpret_cast<int64_t *>(ws);
     float2 *part_ml = reinterpret_cast<float2 *>(ws + align256(sizeof(int64_t) * ((size_t)batch + 1)));
     float *part_acc = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(part_ml) + align256(sizeof(float2) * slots * G));
@@ -999,7 +1050,7 @@ cudaError_t launch_decode(const nvfp4kv_cache &c, const void *q, int batch, int 
     const int64_t rows = (int64_t)batch * num_q_heads;
     // warps per output row from the average number of partials per pair
     const int64_t pairs = (int64_t)batch * c.num_kv_heads;
-    const int64_t avg_parts = (grid + 2 * pairs - 1) / pairs;
+    const int64_t avg_parts = (grid + 2 * pairs - 1) / pairs * kWarps;
     int wpr = avg_parts <= 4 ? 1 : avg_parts <= 8 ? 2 : avg_parts <= 16 ? 4 : 8;
     const int64_t rows_per_cta = kReduceWarps / wpr;
     void *rargs[] = {&r, &wpr};
