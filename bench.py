@@ -337,6 +337,28 @@ def time_append(m, device, steps, warmup):
             "note": "back-to-back calls; 268 MB of BF16 input per call exceeds the 129 MB L2"}
 
 
+def time_calibrate(m, device, steps, warmup):
+    """Tensor-scale calibration (amax of K and V) over the 65,536-token append input."""
+    import torch
+
+    import workloads
+    w = workloads.append_65k()
+    k, v = w.kv(device)
+    for _ in range(warmup):
+        m.calibrate_global_scales(k, v, w.num_kv_heads)
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    s.record()
+    for _ in range(steps):
+        m.calibrate_global_scales(k, v, w.num_kv_heads)
+    e.record()
+    torch.cuda.synchronize()
+    us = s.elapsed_time(e) / steps * 1e3
+    nbytes = 2 * w.num_tokens * w.num_kv_heads * 128 * 2
+    return {"workload": w.name, "us_per_call": us, "gb_per_s": nbytes / us / 1e3, "algorithmic_bytes": nbytes,
+            "note": "reads K and V once (BF16); back-to-back calls over 268 MB, beyond the 129 MB L2"}
+
+
 def run_ours(args):
     import torch
 
@@ -483,6 +505,7 @@ def run_ours(args):
                              "call_us": call4, "call_gb_per_s": b4 / call4 / 1e3,
                              "kv_tokens_per_s": 2 * 1048576 / (call4 * 1e-6)}
         comp["append_65k"] = time_append(m, device, 50, 5)
+        comp["calibrate_65k"] = time_calibrate(m, device, 50, 5)
         line["comparisons"] = comp
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -127,6 +127,27 @@ NVFP4KV_API size_t nvfp4kv_pool_bytes(const nvfp4kv_cache *cache);
 NVFP4KV_API int nvfp4_kv_quantize_append(const nvfp4kv_cache *cache, const void *k, const void *v, int64_t num_tokens,
                              int64_t token_stride, const int64_t *slot_mapping, cudaStream_t stream);
 
+/*
+ * Calibrate the per-tensor FP32 global scales of K and V.
+ * Source: section A4 (outlook): the page's benchmarks fix the FP32 tensor
+ * scale at 1.0 and name its calibration as the way to avoid overflow and
+ * underflow of the block scales.  The rule used is the two-level NVFP4 one:
+ *   g = amax / (6 * 448)   (FP32 IEEE division; g = 1 when amax = 0),
+ * amax = the largest finite |x| over all num_tokens x num_kv_heads x 128 BF16
+ * values of the tensor (Inf and NaN are ignored), so the block holding amax
+ * gets the largest E4M3 scale and no block scale saturates.
+ *
+ *   k, v          device BF16 [num_tokens][token_stride], layout as for
+ *                 nvfp4_kv_quantize_append (16-byte aligned; unused if
+ *                 num_tokens == 0).
+ *   scales        device float[2], 8-byte aligned, written with {g_K, g_V}
+ *                 (also used as scratch while the call runs on `stream`).
+ * Pass the results as k_global_scale / v_global_scale of the cache
+ * descriptor before appending.  Returns NVFP4KV_EINVAL for a bad argument.
+ */
+NVFP4KV_API int nvfp4kv_calibrate_global_scales(const void *k, const void *v, int64_t num_tokens, int num_kv_heads,
+                                                int64_t token_stride, float *scales, cudaStream_t stream);
+
 /* Workspace bytes nvfp4_paged_decode_attention needs for this shape and
  * num_splits on the current device (0 if the arguments are invalid). */
 NVFP4KV_API size_t nvfp4kv_decode_workspace_bytes(const nvfp4kv_cache *cache, int batch, int num_q_heads, int num_splits);
@@ -214,6 +235,17 @@ NVFP4KV_API int nvfp4_prefix_dequant(const nvfp4kv_cache *cache, const int32_t *
  * word.  Returns NVFP4KV_OK, NVFP4KV_EDEVICE_CHECK (some kernel skipped an
  * out-of-range index since the last check) or NVFP4KV_ECUDA. */
 NVFP4KV_API int nvfp4kv_check_device_errors(cudaStream_t stream);
+
+/* Failure-path self-test (no counterpart on the pages; for tests of failure
+ * detection).  Launches one warp on `stream` that waits on an mbarrier phase
+ * with the same bounded wait the decode kernel uses on its bulk copies:
+ * the phase completes only if `arrive` != 0.  After `poll_limit` unsuccessful
+ * polls (1 .. 2^24) the wait gives up, the kernel writes 1 to *result (device
+ * int, 4-byte aligned) and sets the timeout bit of the device error word, as a
+ * decode kernel whose copy never landed would; otherwise it writes 0.  The
+ * kernel then returns normally, so the context stays usable.  Returns
+ * NVFP4KV_EINVAL for a bad argument, NVFP4KV_ECUDA if the launch fails. */
+NVFP4KV_API int nvfp4kv_selftest_bounded_wait(int arrive, unsigned poll_limit, int *result, cudaStream_t stream);
 
 /* Benchmark hook: while enabled, every `every`-th nvfp4_paged_decode_attention
  * call (calls 0, every, 2*every, ...; the j-th of them uses pair j % count)

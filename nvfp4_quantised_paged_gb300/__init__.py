@@ -64,6 +64,8 @@ def _load_library():
         "nvfp4_paged_decode_attention": (i32, [D, P, i32, i32, P, i32, P, f32, P, P, sz, i32, P]),
         "nvfp4_prefix_dequant": (i32, [D, P, i32, P, P, i32, i64, P, P, P]),
         "nvfp4kv_check_device_errors": (i32, [P]),
+        "nvfp4kv_selftest_bounded_wait": (i32, [i32, ctypes.c_uint, P, P]),
+        "nvfp4kv_calibrate_global_scales": (i32, [P, P, i64, i32, i64, P, P]),
         "nvfp4kv_profile_decode": (i32, [P, P, i32, i32]),
         "nvfp4_paged_decode_attention_noalloc": (i32, [D, P, i32, i32, P, i32, P, f32, P, i32, P]),
     }
@@ -79,7 +81,8 @@ _lib = _load_library()
 EXPORTED_SYMBOLS = ("nvfp4kv_version", "nvfp4kv_status_string", "nvfp4kv_slab_bytes", "nvfp4kv_pool_bytes",
                     "nvfp4_kv_quantize_append", "nvfp4kv_decode_workspace_bytes", "nvfp4kv_decode_auto_splits",
                     "nvfp4_paged_decode_attention", "nvfp4_prefix_dequant", "nvfp4kv_check_device_errors",
-                    "nvfp4kv_profile_decode", "nvfp4_paged_decode_attention_noalloc")
+                    "nvfp4kv_profile_decode", "nvfp4_paged_decode_attention_noalloc",
+                    "nvfp4kv_selftest_bounded_wait", "nvfp4kv_calibrate_global_scales")
 
 NOALLOC_SCRATCH_BYTES = 64 << 20  # NVFP4KV_NOALLOC_SCRATCH_BYTES of the header
 
@@ -168,6 +171,30 @@ def quantize_append(cache: PagedCache, k: torch.Tensor, v: torch.Tensor, slot_ma
         raise ValueError("k and v must share a token stride")
     rc = _lib.nvfp4_kv_quantize_append(cache.desc, _ptr(k), _ptr(v), T, stride, _ptr(slot_mapping), _stream(stream))
     _check(rc, "nvfp4_kv_quantize_append")
+
+
+def calibrate_global_scales(k: torch.Tensor, v: torch.Tensor, num_kv_heads: int,
+                            stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """Per-tensor FP32 global scales {g_K, g_V} = amax / (6 * 448) of BF16 K and V
+    ([T][Hkv][128] or token-strided, as for quantize_append), as a device float32
+    tensor [2] (1.0 for an all-zero tensor)."""
+    T = int(k.shape[0])
+    row = int(num_kv_heads) * HEAD_DIM
+    for name, x in (("k", k), ("v", v)):
+        if not x.is_cuda or x.dtype != torch.bfloat16:
+            raise ValueError("%s must be a CUDA bfloat16 tensor" % name)
+        if x.shape[0] != T:
+            raise ValueError("k and v must have the same number of tokens")
+        if T > 0 and (not x[0].is_contiguous() or x[0].numel() != row):
+            raise ValueError("%s: each token must hold %d contiguous values" % (name, row))
+    stride = int(k.stride(0)) if T > 0 else row
+    if T > 0 and int(v.stride(0)) != stride:
+        raise ValueError("k and v must share a token stride")
+    scales = torch.empty(2, dtype=torch.float32, device=k.device)
+    rc = _lib.nvfp4kv_calibrate_global_scales(_ptr(k), _ptr(v), T, int(num_kv_heads), stride, _ptr(scales),
+                                              _stream(stream))
+    _check(rc, "nvfp4kv_calibrate_global_scales")
+    return scales
 
 
 def decode_workspace_bytes(cache: PagedCache, batch: int, num_q_heads: int, num_splits: int = 0) -> int:
@@ -272,6 +299,17 @@ def profile_decode(before, after, every: int = 1):
     arr_b = (ctypes.c_void_p * n)(*[e.cuda_event for e in before])
     arr_a = (ctypes.c_void_p * n)(*[e.cuda_event for e in after])
     _check(_lib.nvfp4kv_profile_decode(arr_b, arr_a, n, int(every)), "nvfp4kv_profile_decode")
+
+
+def selftest_bounded_wait(arrive: bool, poll_limit: int, stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """Failure-path self-test: one warp waits (at most poll_limit polls) on an
+    mbarrier phase that completes only if `arrive`.  Returns a device int32
+    tensor [1]: 1 if the wait gave up (the device error word then holds the
+    timeout bit), else 0."""
+    result = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    _check(_lib.nvfp4kv_selftest_bounded_wait(1 if arrive else 0, int(poll_limit), _ptr(result), _stream(stream)),
+           "nvfp4kv_selftest_bounded_wait")
+    return result
 
 
 def check_device_errors(stream: Optional[torch.cuda.Stream] = None) -> int:

@@ -119,6 +119,16 @@ int nvfp4_kv_quantize_append(const nvfp4kv_cache *cache, const void *k, const vo
     return from_cuda(launch_quantize_append(*cache, k, v, num_tokens, token_stride, slot_mapping, err, stream));
 }
 
+int nvfp4kv_calibrate_global_scales(const void *k, const void *v, int64_t num_tokens, int num_kv_heads,
+                                    int64_t token_stride, float *scales, cudaStream_t stream) {
+    if (num_tokens < 0 || num_kv_heads < 1 || !scales || !aligned(scales, 8)) return NVFP4KV_EINVAL;
+    if (num_tokens > 0) {
+        if (!k || !v || !aligned(k, 16) || !aligned(v, 16)) return NVFP4KV_EINVAL;
+        if (token_stride < (int64_t)num_kv_heads * kHeadDim || token_stride % 8) return NVFP4KV_EINVAL;
+    }
+    return from_cuda(launch_calibrate(k, v, num_tokens, num_kv_heads, token_stride, scales, stream));
+}
+
 int nvfp4kv_decode_auto_splits(const nvfp4kv_cache *cache, int num_q_heads) {
     if (check_cache(cache) || num_q_heads < 1 || num_q_heads % cache->num_kv_heads) return 0;
     const int G = num_q_heads / cache->num_kv_heads;
@@ -207,6 +217,14 @@ int nvfp4kv_profile_decode(const cudaEvent_t *before, const cudaEvent_t *after, 
         g_prof_after.push_back(after[i]);
     }
     return NVFP4KV_OK;
+}
+
+int nvfp4kv_selftest_bounded_wait(int arrive, unsigned poll_limit, int *result, cudaStream_t stream) {
+    if (!result || !aligned(result, 4) || poll_limit == 0 || poll_limit > (1u << 24)) return NVFP4KV_EINVAL;
+    cudaError_t e;
+    unsigned *err = error_word(&e);
+    if (!err) return NVFP4KV_ECUDA;
+    return from_cuda(launch_bounded_wait_selftest(arrive, poll_limit, result, err, stream));
 }
 
 int nvfp4kv_check_device_errors(cudaStream_t stream) {

@@ -29,4 +29,13 @@ cudaError_t launch_decode(const nvfp4kv_cache &c, const void *q, int batch, int 
                           void *out, void *workspace, int grid, unsigned *err, cudaStream_t stream,
                           cudaEvent_t before, cudaEvent_t after);
 
+// g_K, g_V = amax / (6 * 448) of K and V (1.0 for an all-zero tensor) into scales[0..1].
+cudaError_t launch_calibrate(const void *k, const void *v, int64_t num_tokens, int num_kv_heads, int64_t token_stride,
+                             float *scales, cudaStream_t stream);
+
+// One warp waits, at most poll_limit polls, on an mbarrier phase that completes
+// only if `arrive`; writes 1 to *result (and kErrTimeout to *err) if it gave up.
+cudaError_t launch_bounded_wait_selftest(int arrive, uint32_t poll_limit, int *result, unsigned *err,
+                                         cudaStream_t stream);
+
 }  // namespace nvfp4kv

@@ -57,6 +57,7 @@ def _load():
         P = ctypes.c_void_p
         i32, i64, f32, f64 = ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_double
         sig = {
+            "oracle_calibrate_global_scale": (f32, [P, i64]),
             "oracle_bf16_value": (f64, [ctypes.c_uint16]),
             "oracle_bf16_from_float": (ctypes.c_uint16, [f32]),
             "oracle_e4m3_value": (f64, [ctypes.c_uint8]),
@@ -149,6 +150,13 @@ def quantize_block16(x_bf16: np.ndarray, g: float = 1.0):
     scale = np.zeros(1, dtype=np.uint8)
     _check(_load().oracle_quantize_block16(_ptr(x), float(g), _ptr(codes), _ptr(scale)), "quantize_block16")
     return codes, int(scale[0])
+
+
+def calibrate_global_scale(x_bf16: np.ndarray) -> np.float32:
+    """FP32 tensor scale g = amax / (6 * 448) over the finite BF16 values (bits)
+    of x; 1.0 for an all-zero tensor."""
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16).reshape(-1)
+    return np.float32(_load().oracle_calibrate_global_scale(_ptr(x), x.size))
 
 
 def slab_bytes(dtype: int, page_size: int) -> int:

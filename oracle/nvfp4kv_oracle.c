@@ -16,7 +16,9 @@
  *   - decode attention reads them back, dequantises, and runs softmax
  *     attention (section A2, path 3), here in fp64;
  *   - chunked prefill / extend dequantises a cached prefix into a contiguous
- *     workspace (section A2, path 2), here BF16.
+ *     workspace (section A2, path 2), here BF16;
+ *   - the FP32 tensor scale, fixed at 1.0 by the page, can be calibrated
+ *     (section A4, outlook): g = amax / (6 * 448), the two-level NVFP4 rule.
  * The FP8 E4M3 cache the page compares against (section A4, the fp8_e4m3
  * baseline) is provided too.
  *
@@ -185,6 +187,24 @@ int oracle_quantize_block16(const uint16_t *x_bf16, float g, uint8_t *codes16, u
 }
 
 /* Dequantised value as stored by the cache: e2m1 * e4m3 * g (exact in double). */
+/*
+ * Per-tensor FP32 global scale (section A4, outlook: calibrating the tensor
+ * scale that the page fixes at 1.0).  amax = the largest finite |x| over the
+ * n BF16 values; g = amax / (6 * 448) in FP32, so that the block holding amax
+ * gets E4M3's largest scale; 1.0 when amax is 0 (nothing to calibrate).
+ */
+float oracle_calibrate_global_scale(const uint16_t *x_bf16, int64_t n)
+{
+    double amax = 0.0;
+    for (int64_t i = 0; i < n; i++) {
+        const double a = fabs(oracle_bf16_value(x_bf16[i]));
+        if (isfinite(a) && a > amax) amax = a;
+    }
+    if (amax == 0.0) return 1.0f;
+    const float largest_e2m1 = 6.0f, largest_e4m3 = 448.0f;
+    return (float)amax / (largest_e2m1 * largest_e4m3);
+}
+
 static double nvfp4_dequant(uint8_t code, uint8_t scale, float g)
 {
     return oracle_e2m1_value(code) * oracle_e4m3_value(scale) * (double)g;
