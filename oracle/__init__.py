@@ -58,6 +58,7 @@ def _load():
         i32, i64, f32, f64 = ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_double
         sig = {
             "oracle_calibrate_global_scale": (f32, [P, i64]),
+            "oracle_extend_attention": (i32, [P, P, P, P, P, P, P, i32, i32, i32, f64, P, i32]),
             "oracle_bf16_value": (f64, [ctypes.c_uint16]),
             "oracle_bf16_from_float": (ctypes.c_uint16, [f32]),
             "oracle_e4m3_value": (f64, [ctypes.c_uint8]),
@@ -230,3 +231,27 @@ def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
     b = np.ascontiguousarray(bits, dtype=np.uint16)
     with np.errstate(invalid="ignore"):
         return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def extend_attention(q: np.ndarray, k_prefix: np.ndarray, v_prefix: np.ndarray, cu_prefix: np.ndarray,
+                     k_chunk: np.ndarray, v_chunk: np.ndarray, cu_q: np.ndarray, sm_scale: float,
+                     nthreads: int = 0) -> np.ndarray:
+    """fp64 extend attention: chunk token i of request r attends to its prefix
+    rows (BF16 bits [total_prefix][Hkv][128], rows cu_prefix[r]..cu_prefix[r+1])
+    and to chunk tokens 0..i (BF16 bits [total_q][Hkv][128]); q: BF16 bits
+    [total_q][Hq][128].  Returns float64 [total_q][Hq][128]."""
+    q = np.ascontiguousarray(q, dtype=np.uint16)
+    kp, vp = np.ascontiguousarray(k_prefix, dtype=np.uint16), np.ascontiguousarray(v_prefix, dtype=np.uint16)
+    kn, vn = np.ascontiguousarray(k_chunk, dtype=np.uint16), np.ascontiguousarray(v_chunk, dtype=np.uint16)
+    cp = np.ascontiguousarray(cu_prefix, dtype=np.int32)
+    cq = np.ascontiguousarray(cu_q, dtype=np.int32)
+    total_q, hq = q.shape[0], q.shape[1]
+    hkv = kn.shape[1] if kn.ndim == 3 else kp.shape[1]
+    out = np.zeros((total_q, hq, HEAD_DIM), dtype=np.float64)
+    # a valid (never dereferenced) pointer for empty arrays
+    kp = kp if kp.size else np.zeros(1, np.uint16)
+    vp = vp if vp.size else np.zeros(1, np.uint16)
+    rc = _load().oracle_extend_attention(_ptr(q), _ptr(kp), _ptr(vp), _ptr(cp), _ptr(kn), _ptr(vn), _ptr(cq),
+                                         len(cq) - 1, hq, hkv, float(sm_scale), _ptr(out), int(nthreads))
+    _check(rc, "extend_attention")
+    return out

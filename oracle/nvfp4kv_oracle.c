@@ -16,7 +16,8 @@
  *   - decode attention reads them back, dequantises, and runs softmax
  *     attention (section A2, path 3), here in fp64;
  *   - chunked prefill / extend dequantises a cached prefix into a contiguous
- *     workspace (section A2, path 2), here BF16;
+ *     workspace (section A2, path 2), here BF16, and the new chunk attends to
+ *     [that prefix || its own K/V], causally within the chunk;
  *   - the FP32 tensor scale, fixed at 1.0 by the page, can be calibrated
  *     (section A4, outlook): g = amax / (6 * 448), the two-level NVFP4 rule.
  * The FP8 E4M3 cache the page compares against (section A4, the fp8_e4m3
@@ -544,4 +545,102 @@ int oracle_prefix_dequant(const uint8_t *pool, int64_t num_pages, int page_size,
         }
     }
     return ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------ */
+/* Extend attention (section A2, path 2)                                */
+/* ------------------------------------------------------------------ */
+
+/* Path 2's attention consumes two KV sources: the cached prefix as the
+ * workspace holds it (BF16 rows, written by prefix dequant) and the current
+ * chunk's own K/V.  Chunk token i of request r attends to all n_r prefix
+ * tokens and to chunk tokens 0..i (causal), i.e. to the first n_r + i + 1
+ * keys of [prefix || chunk]. */
+typedef struct {
+    const uint16_t *k_pre, *v_pre, *k_new, *v_new;
+    int64_t pre0, new0, n_prefix; /* first workspace row, first chunk row, prefix length */
+    int num_kv_heads, kv;
+} extend_rows_t;
+
+static int extend_row(void *ctx, int which, int64_t t, double *out)
+{
+    extend_rows_t *c = (extend_rows_t *)ctx;
+    const uint16_t *src;
+    if (t < c->n_prefix)
+        src = (which ? c->v_pre : c->k_pre) + ((c->pre0 + t) * c->num_kv_heads + c->kv) * HEAD_DIM;
+    else
+        src = (which ? c->v_new : c->k_new) + ((c->new0 + t - c->n_prefix) * c->num_kv_heads + c->kv) * HEAD_DIM;
+    for (int d = 0; d < HEAD_DIM; d++) out[d] = oracle_bf16_value(src[d]);
+    return 0;
+}
+
+typedef struct {
+    const uint16_t *q, *k_pre, *v_pre, *k_new, *v_new;
+    const int32_t *cu_prefix, *cu_q;
+    int num_reqs, num_q_heads, num_kv_heads;
+    double sm_scale;
+    double *out;
+    int64_t total_units, next_unit;
+    pthread_mutex_t lock;
+    int status;
+} extend_job_t;
+
+/* One unit = one (chunk token, kv head) of the flattened chunk tokens. */
+static void *extend_worker(void *arg)
+{
+    extend_job_t *j = (extend_job_t *)arg;
+    const int Hkv = j->num_kv_heads, G = j->num_q_heads / Hkv;
+    double qd[16 * HEAD_DIM];
+    for (;;) {
+        pthread_mutex_lock(&j->lock);
+        int64_t u = j->next_unit++;
+        pthread_mutex_unlock(&j->lock);
+        if (u >= j->total_units) break;
+        int64_t row = u / Hkv;
+        int kv = (int)(u % Hkv);
+        int r = 0;
+        while (r + 1 < j->num_reqs && j->cu_q[r + 1] <= row) r++;
+        int64_t i = row - j->cu_q[r];
+        int64_t n_prefix = (int64_t)j->cu_prefix[r + 1] - j->cu_prefix[r];
+        for (int h = 0; h < G; h++)
+            for (int d = 0; d < HEAD_DIM; d++)
+                qd[h * HEAD_DIM + d] = oracle_bf16_value(j->q[(row * j->num_q_heads + kv * G + h) * HEAD_DIM + d]);
+        extend_rows_t ctx = {j->k_pre, j->v_pre, j->k_new, j->v_new, j->cu_prefix[r], j->cu_q[r], n_prefix, Hkv, kv};
+        int64_t n = n_prefix + i + 1;
+        double *scores = malloc(sizeof(double) * (size_t)G * (size_t)n);
+        int rc = attend_group(qd, G, extend_row, &ctx, n, j->sm_scale,
+                              j->out + (row * j->num_q_heads + (int64_t)kv * G) * HEAD_DIM, scores);
+        free(scores);
+        if (rc) {
+            pthread_mutex_lock(&j->lock);
+            if (!j->status) j->status = rc;
+            pthread_mutex_unlock(&j->lock);
+        }
+    }
+    return NULL;
+}
+
+/* q: BF16 [total_q][num_q_heads][128]; k_new, v_new: BF16 [total_q][num_kv_heads][128]
+ * (request r's chunk = rows cu_q[r] .. cu_q[r+1]-1); k_pre, v_pre: BF16
+ * [total_prefix][num_kv_heads][128] (request r's prefix = rows cu_prefix[r] ..
+ * cu_prefix[r+1]-1, e.g. the output of oracle_prefix_dequant); out: double
+ * [total_q][num_q_heads][128]. */
+int oracle_extend_attention(const uint16_t *q, const uint16_t *k_pre, const uint16_t *v_pre, const int32_t *cu_prefix,
+                            const uint16_t *k_new, const uint16_t *v_new, const int32_t *cu_q, int num_reqs,
+                            int num_q_heads, int num_kv_heads, double sm_scale, double *out, int nthreads)
+{
+    if (num_reqs < 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads || num_q_heads / num_kv_heads > 16)
+        return ORACLE_EINVAL;
+    for (int r = 0; r < num_reqs; r++)
+        if (cu_q[r + 1] < cu_q[r] || cu_prefix[r + 1] < cu_prefix[r]) return ORACLE_EINVAL;
+    int64_t total_q = num_reqs ? cu_q[num_reqs] - cu_q[0] : 0;
+    if (num_reqs && cu_q[0] != 0) return ORACLE_EINVAL;
+    extend_job_t j = {q, k_pre, v_pre, k_new, v_new, cu_prefix, cu_q, num_reqs, num_q_heads, num_kv_heads, sm_scale,
+                      out, total_q * num_kv_heads, 0, PTHREAD_MUTEX_INITIALIZER, 0};
+    int nt = resolve_threads(nthreads);
+    pthread_t *th = malloc(sizeof(pthread_t) * (size_t)nt);
+    for (int i = 0; i < nt; i++) pthread_create(&th[i], NULL, extend_worker, &j);
+    for (int i = 0; i < nt; i++) pthread_join(th[i], NULL);
+    free(th);
+    return j.status;
 }
