@@ -70,6 +70,15 @@ def peak_hbm():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def load_bf16_peak():
+    """Measured dense BF16 TFLOP/s (burst, for a kernel timed alone), else the fallback."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"])
+    except Exception:
+        return 1900.0
+
+
 def decode_bytes(batch, seq_len, hq, hkv, max_pages, dtype_bytes_per_token_head):
     """Algorithmic bytes of one decode call: KV (+ scales) + block table + Q + out."""
     kv = batch * seq_len * hkv * dtype_bytes_per_token_head
@@ -359,6 +368,68 @@ def time_calibrate(m, device, steps, warmup):
             "note": "reads K and V once (BF16); back-to-back calls over 268 MB, beyond the 129 MB L2"}
 
 
+def extend_flops(prefix_lens, chunk, G, Hkv):
+    """Algorithmic FLOPs of extend attention: 2 * 2 * 128 per (query row, visible key)."""
+    return sum(Hkv * G * (chunk * p + chunk * (chunk + 1) // 2) for p in prefix_lens) * 4 * 128
+
+
+def time_extend(m, device, steps, warmup, peak_tflops):
+    """Path 2 on the agent mix's 8 extend requests: prefix dequant of their cached
+    prefixes (NVFP4 pages -> BF16 workspace), then extend attention of each
+    512-token chunk over [prefix || chunk]."""
+    import torch
+
+    import workloads
+    mix = workloads.agent_mix()
+    w = mix.decode
+    rows = mix.extend_rows()
+    cache = m.PagedCache(w.num_pages, w.page_size, w.num_kv_heads, device=device)
+    for row in rows:
+        k, v = w.seq_kv(row, device)
+        m.quantize_append(cache, k, v, w.slots(row).to(device))
+        del k, v
+    pl = w.seq_lens[rows].contiguous()
+    cu_p = torch.zeros(len(rows) + 1, dtype=torch.int32)
+    cu_p[1:] = torch.cumsum(pl, 0)
+    bt, pl_d, cu_p_d = w.block_table[rows].contiguous().to(device), pl.to(device), cu_p.to(device)
+    total = int(cu_p[-1])
+    L = mix.chunk_tokens
+    q = torch.cat([mix.chunk_q(r, device) for r in range(len(rows))])
+    kn = torch.cat([mix.chunk_kv(r, device)[0] for r in range(len(rows))])
+    vn = torch.cat([mix.chunk_kv(r, device)[1] for r in range(len(rows))])
+    cu_q = torch.arange(0, L * (len(rows) + 1), L, dtype=torch.int32, device=device)
+    kw, vw = m.prefix_dequant(cache, bt, pl_d, cu_p_d, total)
+    out = torch.empty_like(q)
+
+    def run(with_dequant):
+        if with_dequant:
+            m.prefix_dequant(cache, bt, pl_d, cu_p_d, total, k_ws=kw, v_ws=vw)
+        m.extend_attention(q, kw, vw, cu_p_d, kn, vn, cu_q, L, w.sm_scale, out=out)
+
+    res = {"workload": "agent-mix extends: 8 x 512-token chunks over prefixes of %s tokens, q32kv8"
+           % "/".join(str(int(x)) for x in pl)}
+    for key, wd in (("extend_us", False), ("path2_us", True)):
+        for _ in range(warmup):
+            run(wd)
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        s.record()
+        for _ in range(steps):
+            run(wd)
+        e.record()
+        torch.cuda.synchronize()
+        res[key] = s.elapsed_time(e) / steps * 1e3
+    assert m.check_device_errors() == 0
+    flops = extend_flops([int(x) for x in pl], L, w.num_q_heads // w.num_kv_heads, w.num_kv_heads)
+    res.update({"algorithmic_flops": flops, "extend_tflops": flops / res["extend_us"] / 1e6,
+                "extend_frac_of_bf16_peak": flops / res["extend_us"] / 1e6 / peak_tflops,
+                "bf16_peak_tflops": peak_tflops,
+                "note": "mma.sync BF16 tensor-core kernel; peak = measured cuBLAS BF16 burst"})
+    del cache
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_ours(args):
     import torch
 
@@ -506,6 +577,7 @@ def run_ours(args):
                              "kv_tokens_per_s": 2 * 1048576 / (call4 * 1e-6)}
         comp["append_65k"] = time_append(m, device, 50, 5)
         comp["calibrate_65k"] = time_calibrate(m, device, 50, 5)
+        comp["extend_agent_mix"] = time_extend(m, device, 10, 2, load_bf16_peak())
         line["comparisons"] = comp
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

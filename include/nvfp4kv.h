@@ -231,6 +231,34 @@ NVFP4KV_API int nvfp4_prefix_dequant(const nvfp4kv_cache *cache, const int32_t *
                          const int32_t *prefix_lens, const int32_t *cu_prefix_lens, int num_reqs,
                          int64_t total_prefix_tokens, void *k_ws, void *v_ws, cudaStream_t stream);
 
+/*
+ * Extend attention: each request's new chunk attends to [its cached prefix ||
+ * the chunk itself], causally within the chunk.
+ * Source: section A2, path 2 (chunked prefill / extend): the attention
+ * consumes the cached prefix as the layer-shared workspace holds it (written
+ * by nvfp4_prefix_dequant) and the current chunk's K/V.  Chunk token i of
+ * request r sees all prefix tokens of r and chunk tokens 0..i:
+ *   out[t][h] = sum_j softmax_j(sm_scale * q[t][h] . k_j) v_j
+ * over those keys, with query head h reading KV head h / G.
+ *
+ *   q               device BF16 [total_q][num_q_heads][128]; request r's
+ *                   chunk is rows cu_q_lens[r] .. cu_q_lens[r+1]-1.
+ *   k_prefix, v_prefix  device BF16 [total_prefix][num_kv_heads][128]; request
+ *                   r's prefix is rows cu_prefix_lens[r] .. cu_prefix_lens[r+1]-1
+ *                   (the nvfp4_prefix_dequant workspace layout).
+ *   k_chunk, v_chunk    device BF16 [total_q][num_kv_heads][128], rows as q.
+ *   cu_prefix_lens, cu_q_lens  device int32 [num_reqs + 1], non-decreasing.
+ *   max_q_len       host bound on every chunk length (grid size); a longer
+ *                   chunk is cut to it and flagged in the device error word.
+ *   out             device BF16 [total_q][num_q_heads][128].
+ * All data pointers 16-byte aligned.  Computes in BF16 x BF16 -> FP32 on the
+ * tensor cores (probabilities rounded to BF16).  num_reqs == 0 is a no-op.
+ */
+NVFP4KV_API int nvfp4_extend_attention(const void *q, const void *k_prefix, const void *v_prefix,
+                                       const int32_t *cu_prefix_lens, const void *k_chunk, const void *v_chunk,
+                                       const int32_t *cu_q_lens, int num_reqs, int max_q_len, int num_q_heads,
+                                       int num_kv_heads, float sm_scale, void *out, cudaStream_t stream);
+
 /* Synchronises `stream`, then reads and clears the current device's error
  * word.  Returns NVFP4KV_OK, NVFP4KV_EDEVICE_CHECK (some kernel skipped an
  * out-of-range index since the last check) or NVFP4KV_ECUDA. */

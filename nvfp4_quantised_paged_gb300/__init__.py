@@ -66,6 +66,7 @@ def _load_library():
         "nvfp4kv_check_device_errors": (i32, [P]),
         "nvfp4kv_selftest_bounded_wait": (i32, [i32, ctypes.c_uint, P, P]),
         "nvfp4kv_calibrate_global_scales": (i32, [P, P, i64, i32, i64, P, P]),
+        "nvfp4_extend_attention": (i32, [P, P, P, P, P, P, P, i32, i32, i32, i32, f32, P, P]),
         "nvfp4kv_profile_decode": (i32, [P, P, i32, i32]),
         "nvfp4_paged_decode_attention_noalloc": (i32, [D, P, i32, i32, P, i32, P, f32, P, i32, P]),
     }
@@ -82,7 +83,7 @@ EXPORTED_SYMBOLS = ("nvfp4kv_version", "nvfp4kv_status_string", "nvfp4kv_slab_by
                     "nvfp4_kv_quantize_append", "nvfp4kv_decode_workspace_bytes", "nvfp4kv_decode_auto_splits",
                     "nvfp4_paged_decode_attention", "nvfp4_prefix_dequant", "nvfp4kv_check_device_errors",
                     "nvfp4kv_profile_decode", "nvfp4_paged_decode_attention_noalloc",
-                    "nvfp4kv_selftest_bounded_wait", "nvfp4kv_calibrate_global_scales")
+                    "nvfp4kv_selftest_bounded_wait", "nvfp4kv_calibrate_global_scales", "nvfp4_extend_attention")
 
 NOALLOC_SCRATCH_BYTES = 64 << 20  # NVFP4KV_NOALLOC_SCRATCH_BYTES of the header
 
@@ -310,6 +311,42 @@ def selftest_bounded_wait(arrive: bool, poll_limit: int, stream: Optional[torch.
     _check(_lib.nvfp4kv_selftest_bounded_wait(1 if arrive else 0, int(poll_limit), _ptr(result), _stream(stream)),
            "nvfp4kv_selftest_bounded_wait")
     return result
+
+
+def extend_attention(q: torch.Tensor, k_prefix: torch.Tensor, v_prefix: torch.Tensor, cu_prefix_lens: torch.Tensor,
+                     k_chunk: torch.Tensor, v_chunk: torch.Tensor, cu_q_lens: torch.Tensor, max_q_len: int,
+                     sm_scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
+                     stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """Each request's chunk attends to [its prefix rows || the chunk], causally in
+    the chunk.  q: BF16 [total_q][Hq][128]; k_prefix, v_prefix: BF16
+    [total_prefix][Hkv][128] (e.g. from prefix_dequant); k_chunk, v_chunk: BF16
+    [total_q][Hkv][128]; cu_*: int32 [R+1]; max_q_len: bound on chunk lengths."""
+    for name, x in (("q", q), ("k_prefix", k_prefix), ("v_prefix", v_prefix), ("k_chunk", k_chunk),
+                    ("v_chunk", v_chunk)):
+        if not x.is_cuda or x.dtype != torch.bfloat16 or not x.is_contiguous() or x.dim() != 3 or x.shape[2] != HEAD_DIM:
+            raise ValueError("%s must be a contiguous CUDA bfloat16 tensor [rows][heads][128]" % name)
+    _require(cu_prefix_lens, "cu_prefix_lens", torch.int32)
+    _require(cu_q_lens, "cu_q_lens", torch.int32)
+    R = int(cu_q_lens.shape[0]) - 1
+    if int(cu_prefix_lens.shape[0]) != R + 1:
+        raise ValueError("cu_prefix_lens and cu_q_lens must have the same length")
+    hq, hkv = int(q.shape[1]), int(k_chunk.shape[1])
+    if k_prefix.shape[1] != hkv or v_prefix.shape[1] != hkv or v_chunk.shape[1] != hkv:
+        raise ValueError("K/V head counts differ")
+    if k_chunk.shape[0] != q.shape[0] or v_chunk.shape[0] != q.shape[0]:
+        raise ValueError("chunk K/V must have one row per query token")
+    if out is None:
+        out = torch.empty_like(q)
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(HEAD_DIM)
+    # an empty prefix still needs a valid aligned pointer
+    kp = k_prefix if k_prefix.numel() else torch.zeros((1, hkv, HEAD_DIM), dtype=torch.bfloat16, device=q.device)
+    vp = v_prefix if v_prefix.numel() else kp
+    rc = _lib.nvfp4_extend_attention(_ptr(q), _ptr(kp), _ptr(vp), _ptr(cu_prefix_lens), _ptr(k_chunk), _ptr(v_chunk),
+                                     _ptr(cu_q_lens), R, int(max_q_len), hq, hkv, float(sm_scale), _ptr(out),
+                                     _stream(stream))
+    _check(rc, "nvfp4_extend_attention")
+    return out
 
 
 def check_device_errors(stream: Optional[torch.cuda.Stream] = None) -> int:

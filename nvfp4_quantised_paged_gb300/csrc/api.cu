@@ -119,6 +119,29 @@ int nvfp4_kv_quantize_append(const nvfp4kv_cache *cache, const void *k, const vo
     return from_cuda(launch_quantize_append(*cache, k, v, num_tokens, token_stride, slot_mapping, err, stream));
 }
 
+int nvfp4_extend_attention(const void *q, const void *k_prefix, const void *v_prefix, const int32_t *cu_prefix_lens,
+                           const void *k_chunk, const void *v_chunk, const int32_t *cu_q_lens, int num_reqs,
+                           int max_q_len, int num_q_heads, int num_kv_heads, float sm_scale, void *out,
+                           cudaStream_t stream) {
+    if (num_reqs < 0 || max_q_len < 0 || num_kv_heads < 1 || num_q_heads < 1 || num_q_heads % num_kv_heads)
+        return NVFP4KV_EINVAL;
+    if (!isfinite(sm_scale)) return NVFP4KV_EINVAL;
+    if (num_reqs == 0 || max_q_len == 0) return NVFP4KV_OK;
+    if (!q || !k_chunk || !v_chunk || !out || !cu_prefix_lens || !cu_q_lens || !k_prefix || !v_prefix)
+        return NVFP4KV_EINVAL;
+    if (!aligned(q, 16) || !aligned(k_chunk, 16) || !aligned(v_chunk, 16) || !aligned(out, 16) ||
+        !aligned(k_prefix, 16) || !aligned(v_prefix, 16) || !aligned(cu_prefix_lens, 4) || !aligned(cu_q_lens, 4))
+        return NVFP4KV_EINVAL;
+    const int64_t G = num_q_heads / num_kv_heads;
+    if ((int64_t)max_q_len * G >= ((int64_t)1 << 31) || num_kv_heads > 65535 || num_reqs > 65535)
+        return NVFP4KV_EUNSUPPORTED;
+    cudaError_t e;
+    unsigned *err = error_word(&e);
+    if (!err) return NVFP4KV_ECUDA;
+    return from_cuda(launch_extend(q, k_prefix, v_prefix, cu_prefix_lens, k_chunk, v_chunk, cu_q_lens, num_reqs,
+                                   max_q_len, num_q_heads, num_kv_heads, sm_scale, out, err, stream));
+}
+
 int nvfp4kv_calibrate_global_scales(const void *k, const void *v, int64_t num_tokens, int num_kv_heads,
                                     int64_t token_stride, float *scales, cudaStream_t stream) {
     if (num_tokens < 0 || num_kv_heads < 1 || !scales || !aligned(scales, 8)) return NVFP4KV_EINVAL;

@@ -118,6 +118,27 @@ def test_agent_mix_full_size(m):
                                        np.array([n], dtype=np.int32), np.array([0, n], dtype=np.int32))
         assert np.array_equal(bits(kw[int(cu[r]):int(cu[r + 1])]), rk)
         assert np.array_equal(bits(vw[int(cu[r]):int(cu[r + 1])]), rv)
+    # extend attention of every request's 512-token chunk over [its prefix || chunk],
+    # sampled tokens against the oracle (a one-token chunk whose "prefix" is the
+    # workspace rows followed by the chunk rows before it: the same keys)
+    qs = [mix.chunk_q(r, "cuda") for r in range(len(rows))]
+    kvs = [mix.chunk_kv(r, "cuda") for r in range(len(rows))]
+    L = mix.chunk_tokens
+    cu_q = torch.arange(0, L * (len(rows) + 1), L, dtype=torch.int32)
+    out = m.extend_attention(torch.cat(qs), kw, vw, cu.cuda(), torch.cat([k for k, _ in kvs]),
+                             torch.cat([v for _, v in kvs]), cu_q.cuda(), L, w.sm_scale)
+    torch.cuda.synchronize()
+    assert m.check_device_errors() == 0
+    for r, i in ((0, 0), (4, 511), (6, 300)):   # request 4 has the longest prefix
+        a, b = int(cu[r]), int(cu[r + 1])
+        kpre = torch.cat([kw[a:b], kvs[r][0][:i]])
+        vpre = torch.cat([vw[a:b], kvs[r][1][:i]])
+        n = kpre.shape[0]
+        ref = oracle.extend_attention(bits(qs[r][i:i + 1]), bits(kpre), bits(vpre), np.array([0, n], np.int32),
+                                      bits(kvs[r][0][i:i + 1]), bits(kvs[r][1][i:i + 1]), np.array([0, 1], np.int32),
+                                      w.sm_scale)
+        check_attention(out[r * L + i:r * L + i + 1], ref, "agent extend r=%d token=%d" % (r, i))
+
     for r in range(len(rows)):
         k, v = mix.chunk_kv(r, "cuda")
         slots = mix.chunk_slots(r)

@@ -270,6 +270,11 @@ class AgentMixWorkload:
         return (draw_kv(self.chunk_tokens, w.num_kv_heads, w.seed, 300_000 + r, device, w.recipe, 0),
                 draw_kv(self.chunk_tokens, w.num_kv_heads, w.seed, 300_000 + r, device, w.recipe, 1))
 
+    def chunk_q(self, r: int, device) -> torch.Tensor:
+        """Queries of extend request r's chunk, BF16 [chunk_tokens][num_q_heads][128]."""
+        w = self.decode
+        return _normal((self.chunk_tokens, w.num_q_heads, HEAD_DIM), w.seed, 400_000 + r, device)
+
     def chunk_slots(self, r: int) -> torch.Tensor:
         """Slots of extend request r's chunk (positions prefix .. prefix+chunk)."""
         row = self.num_decode + r
