@@ -322,8 +322,9 @@ constexpr uint32_t kOnesF16x2 = 0x3c003c00u;
 // products.  Scores are in base 2; the running max moves only when a score
 // exceeds it by more than 2^kRescaleLog2, so probabilities stay <= 2^8 (exact
 // enough in FP16) and most calls skip the cross-lane max and the rescale.
-// vt[t] = valid rows of tile t (0..16); tile 0 holds at least one.
-template <int NT, int T>
+// vt[t] = valid rows of tile t (0..16); tile 0 holds at least one.  FULL:
+// every row of every tile is valid (vt is not read).
+template <int NT, int T, bool FULL = false>
 __device__ __forceinline__ void softmax_tiles(const float (&s)[T][NT][4], int g, const int (&vt)[T],
                                               const float (&fac)[NT][2], float (&m_run)[NT][2], float (&o)[NT][9][4],
                                               uint32_t (&pb)[T][NT][2]) {
@@ -335,7 +336,7 @@ __device__ __forceinline__ void softmax_tiles(const float (&s)[T][NT][4], int g,
         for (int nt = 0; nt < NT; nt++) {
 #pragma unroll
             for (int e = 0; e < 4; e++) x[t][nt][e] = fmaf(s[t][nt][e], fac[nt][e & 1], -m_run[nt][e & 1]);
-            if (vt[t] < 16) {
+            if (!FULL && vt[t] < 16) {
                 if (g >= vt[t]) x[t][nt][0] = x[t][nt][1] = kNegInf;
                 if (g + 8 >= vt[t]) x[t][nt][2] = x[t][nt][3] = kNegInf;
             }
@@ -391,8 +392,9 @@ __device__ __forceinline__ void softmax_tiles(const float (&s)[T][NT][4], int g,
 
 // One warp, T consecutive 16-token NVFP4 groups (st = the first), written
 // step by step for all T tiles together so that their conversions and
-// products interleave.  vt[t] = valid rows of group t (0..16).
-template <int NT, int T>
+// products interleave.  vt[t] = valid rows of group t (0..16); FULL: all 16
+// rows of every group are valid (the masking code is left out).
+template <int NT, int T, bool FULL = false>
 __device__ __forceinline__ void tiles_nvfp4(const uint8_t *st, const int (&vt)[T], int lane,
                                             const uint32_t (&qf)[NT][8][2], const float (&fac)[NT][2],
                                             float (&m_run)[NT][2], float (&o)[NT][9][4]) {
@@ -442,7 +444,7 @@ __device__ __forceinline__ void tiles_nvfp4(const uint8_t *st, const int (&vt)[T
             for (int e = 0; e < 4; e++) s[t][nt][e] = sacc[0][nt][e] + sacc[1][nt][e];
     }
     uint32_t pb[T][NT][2];
-    softmax_tiles<NT, T>(s, g, vt, fac, m_run, o, pb);
+    softmax_tiles<NT, T, FULL>(s, g, vt, fac, m_run, o, pb);
 
     // ---- O^T += V^T P^T.  Lane owns channels 16g..16g+15 (block g) of tokens 2c, 2c+1, 2c+8, 2c+9.
 #pragma unroll
@@ -456,7 +458,7 @@ __device__ __forceinline__ void tiles_nvfp4(const uint8_t *st, const int (&vt)[T
         const uint8_t *vs = gt + L::kVs + g * 16 + 2 * c;  // V scales [8][16]: rows 2c, 2c+1 and 2c+8, 2c+9
         uint32_t vs01 = *reinterpret_cast<const uint16_t *>(vs);
         uint32_t vs23 = *reinterpret_cast<const uint16_t *>(vs + 8);
-        if (vt[t] < 16) {  // rows past the end or not fetched may hold stale bytes: zero codes and scales
+        if (!FULL && vt[t] < 16) {  // rows past the end or not fetched may hold stale bytes: zero codes and scales
             const int j = 2 * c;
             if (j >= vt[t]) { v0 = make_uint2(0, 0); vs01 &= 0xff00u; }
             if (j + 1 >= vt[t]) { v1 = make_uint2(0, 0); vs01 &= 0x00ffu; }
@@ -677,6 +679,8 @@ __global__ void __launch_bounds__(kThreads, DTYPE == NVFP4KV_DTYPE_NVFP4 && NT =
     };
 
     int k = 0;
+    int slot = warp % kSlots;                     // i % kSlots
+    uint32_t phase = (uint32_t)(warp / kSlots) & 1u;  // (i / kSlots) & 1
     for (int i = warp; i < nstages; i += kWarps, k++) {
         const int j = i + kSlots;  // refilled into this stage after this unit
         const bool refill = j < nstages;
@@ -697,11 +701,10 @@ __global__ void __launch_bounds__(kThreads, DTYPE == NVFP4KV_DTYPE_NVFP4 && NT =
                 for (int q = 0; q < 9; q++) o[nt][q][0] = o[nt][q][1] = o[nt][q][2] = o[nt][q][3] = 0.f;
             }
         }
-        const int slot = i % kSlots;
         bool ok = false;
         if (!aborted) {
             ok = wait_issued(&seq[slot], i, abort_flag) &&
-                 mbar_wait_bounded(&full[slot], (uint32_t)((i / kSlots) & 1), kWaitLimit, abort_flag);
+                 mbar_wait_bounded(&full[slot], phase, kWaitLimit, abort_flag);
             if (!ok) {
                 aborted = true;
                 if (lane == 0) {
@@ -713,21 +716,26 @@ __global__ void __launch_bounds__(kThreads, DTYPE == NVFP4KV_DTYPE_NVFP4 && NT =
         const int mask = ok ? valid[slot] : 0;
         if (mask) {
             const int left = cc.n - cc.ch * kChunk;
-            int vt[kGroups];
-#pragma unroll
-            for (int t = 0; t < kGroups; t++) vt[t] = max(0, min(16, left - 16 * t));
-            if (mask != (1 << min(kGroups, (left + 15) >> 4)) - 1) {  // a part was not fetched (bad page)
-#pragma unroll
-                for (int t = 0; t < kGroups; t++)
-                    if (!((mask >> t) & 1)) vt[t] = 0;
-            }
             const uint8_t *st = ring + slot * S::kStage;
-            if (DTYPE == NVFP4KV_DTYPE_NVFP4) {
-                tiles_nvfp4<NT, kGroups>(st, vt, lane, qf, fac, m_run, o);
+            if (DTYPE == NVFP4KV_DTYPE_NVFP4 && left >= kChunk && mask == (1 << kGroups) - 1) {
+                const int vt[kGroups] = {16, 16, 16, 16};  // a whole chunk: no masking
+                tiles_nvfp4<NT, kGroups, true>(st, vt, lane, qf, fac, m_run, o);
             } else {
+                int vt[kGroups];
 #pragma unroll
-                for (int t = 0; t < kGroups; t++)
-                    if (vt[t] > 0) tile_fp8<NT>(st + t * Group<DTYPE>::kBytes, vt[t], lane, qf, fac, m_run, o);
+                for (int t = 0; t < kGroups; t++) vt[t] = max(0, min(16, left - 16 * t));
+                if (mask != (1 << min(kGroups, (left + 15) >> 4)) - 1) {  // a part was not fetched (bad page)
+#pragma unroll
+                    for (int t = 0; t < kGroups; t++)
+                        if (!((mask >> t) & 1)) vt[t] = 0;
+                }
+                if (DTYPE == NVFP4KV_DTYPE_NVFP4) {
+                    tiles_nvfp4<NT, kGroups, false>(st, vt, lane, qf, fac, m_run, o);
+                } else {
+#pragma unroll
+                    for (int t = 0; t < kGroups; t++)
+                        if (vt[t] > 0) tile_fp8<NT>(st + t * Group<DTYPE>::kBytes, vt[t], lane, qf, fac, m_run, o);
+                }
             }
         }
         __syncwarp();
@@ -738,6 +746,11 @@ __global__ void __launch_bounds__(kThreads, DTYPE == NVFP4KV_DTYPE_NVFP4 && NT =
             if (lane == 0) st_release_shared(&seq[slot], j);
         }
         if (i + kWarps < nstages) cursor_advance(cc, a, kWarps);
+        slot += kWarps;
+        if (slot >= kSlots) {
+            slot -= kSlots;
+            phase ^= 1u;
+        }
     }
     if (acc_pair >= 0) write_partial(acc_pair);
 
