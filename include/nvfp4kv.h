@@ -183,6 +183,32 @@ NVFP4KV_API int nvfp4_paged_decode_attention(const nvfp4kv_cache *cache, const v
                                  float sm_scale, void *out, void *workspace, size_t workspace_bytes, int num_splits,
                                  cudaStream_t stream);
 
+/*
+ * Decode step with the new token appended in the same launch.
+ * Source: section A2, path 3 (decode reads the NVFP4 cache in-kernel) with
+ * path 1's quantise-and-write of the new token's K/V fused in front of it.
+ * For every sequence b with seq_lens[b] >= 1, row b of k_new / v_new (the
+ * token at position seq_lens[b] - 1, already counted in seq_lens) is
+ * quantised exactly as nvfp4_kv_quantize_append would, and written through
+ * the block table to position seq_lens[b] - 1; then attention runs as in
+ * nvfp4_paged_decode_attention.  The result, pool and output alike, equals
+ * nvfp4_kv_quantize_append with slot_mapping[b] = slot(seq_lens[b] - 1)
+ * followed by nvfp4_paged_decode_attention.
+ *
+ *   k_new, v_new  device BF16 [batch][new_stride], kv head h at elements
+ *                 h*128 .. h*128+127 of a row; 16-byte aligned.
+ *   new_stride    elements between rows; >= num_kv_heads*128, a multiple of 8.
+ * Other arguments, workspace and errors as nvfp4_paged_decode_attention; a
+ * block-table entry out of range for the new token skips its write and is
+ * flagged in the device error word.
+ */
+NVFP4KV_API int nvfp4_paged_decode_attention_append(const nvfp4kv_cache *cache, const void *k_new, const void *v_new,
+                                                    int64_t new_stride, const void *q, int batch, int num_q_heads,
+                                                    const int32_t *block_table, int max_pages_per_seq,
+                                                    const int32_t *seq_lens, float sm_scale, void *out,
+                                                    void *workspace, size_t workspace_bytes, int num_splits,
+                                                    cudaStream_t stream);
+
 /* Size of the library's static scratch array used by
  * nvfp4_paged_decode_attention_noalloc (64 MiB on every GPU that loads the
  * library, held until the process exits). */
@@ -275,8 +301,9 @@ NVFP4KV_API int nvfp4kv_check_device_errors(cudaStream_t stream);
  * NVFP4KV_EINVAL for a bad argument, NVFP4KV_ECUDA if the launch fails. */
 NVFP4KV_API int nvfp4kv_selftest_bounded_wait(int arrive, unsigned poll_limit, int *result, cudaStream_t stream);
 
-/* Benchmark hook: while enabled, every `every`-th nvfp4_paged_decode_attention
- * call (calls 0, every, 2*every, ...; the j-th of them uses pair j % count)
+/* Benchmark hook: while enabled, every `every`-th decode call (of
+ * nvfp4_paged_decode_attention or nvfp4_paged_decode_attention_append: calls
+ * 0, every, 2*every, ...; the j-th of them uses pair j % count)
  * records before[] on its stream immediately before launching the decode
  * kernel and after[] immediately after it, so the caller can time that kernel
  * alone with cudaEventElapsedTime while the calls in between run undisturbed

@@ -67,6 +67,7 @@ def _load_library():
         "nvfp4kv_selftest_bounded_wait": (i32, [i32, ctypes.c_uint, P, P]),
         "nvfp4kv_calibrate_global_scales": (i32, [P, P, i64, i32, i64, P, P]),
         "nvfp4_extend_attention": (i32, [P, P, P, P, P, P, P, i32, i32, i32, i32, f32, P, P]),
+        "nvfp4_paged_decode_attention_append": (i32, [D, P, P, i64, P, i32, i32, P, i32, P, f32, P, P, sz, i32, P]),
         "nvfp4kv_profile_decode": (i32, [P, P, i32, i32]),
         "nvfp4_paged_decode_attention_noalloc": (i32, [D, P, i32, i32, P, i32, P, f32, P, i32, P]),
     }
@@ -83,7 +84,8 @@ EXPORTED_SYMBOLS = ("nvfp4kv_version", "nvfp4kv_status_string", "nvfp4kv_slab_by
                     "nvfp4_kv_quantize_append", "nvfp4kv_decode_workspace_bytes", "nvfp4kv_decode_auto_splits",
                     "nvfp4_paged_decode_attention", "nvfp4_prefix_dequant", "nvfp4kv_check_device_errors",
                     "nvfp4kv_profile_decode", "nvfp4_paged_decode_attention_noalloc",
-                    "nvfp4kv_selftest_bounded_wait", "nvfp4kv_calibrate_global_scales", "nvfp4_extend_attention")
+                    "nvfp4kv_selftest_bounded_wait", "nvfp4kv_calibrate_global_scales", "nvfp4_extend_attention",
+                    "nvfp4_paged_decode_attention_append")
 
 NOALLOC_SCRATCH_BYTES = 64 << 20  # NVFP4KV_NOALLOC_SCRATCH_BYTES of the header
 
@@ -237,6 +239,44 @@ def paged_decode_attention(cache: PagedCache, q: torch.Tensor, block_table: torc
                                            _ptr(seq_lens), float(sm_scale), _ptr(out), _ptr(workspace),
                                            workspace.numel(), int(num_splits), _stream(stream))
     _check(rc, "nvfp4_paged_decode_attention")
+    return out
+
+
+def paged_decode_attention_append(cache: PagedCache, k_new: torch.Tensor, v_new: torch.Tensor, q: torch.Tensor,
+                                  block_table: torch.Tensor, seq_lens: torch.Tensor, sm_scale: Optional[float] = None,
+                                  out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                                  num_splits: int = 0, stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """Decode step with the new token appended in the same launch: row b of
+    k_new / v_new (BF16 [B][Hkv][128], or token-strided) is quantised into
+    position seq_lens[b] - 1 of sequence b, then attention as paged_decode_attention."""
+    _require(q, "q", torch.bfloat16)
+    _require(block_table, "block_table", torch.int32)
+    _require(seq_lens, "seq_lens", torch.int32)
+    B, Hq = int(q.shape[0]), int(q.shape[1])
+    if q.shape[2] != HEAD_DIM:
+        raise ValueError("head_dim must be 128")
+    row = cache.num_kv_heads * HEAD_DIM
+    for name, x in (("k_new", k_new), ("v_new", v_new)):
+        if not x.is_cuda or x.dtype != torch.bfloat16 or x.shape[0] != B:
+            raise ValueError("%s must be a CUDA bfloat16 tensor with one row per sequence" % name)
+        if B > 0 and (not x[0].is_contiguous() or x[0].numel() != row):
+            raise ValueError("%s: each row must hold %d contiguous values" % (name, row))
+    stride = int(k_new.stride(0)) if B > 0 else row
+    if B > 0 and int(v_new.stride(0)) != stride:
+        raise ValueError("k_new and v_new must share a row stride")
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(HEAD_DIM)
+    if out is None:
+        out = torch.empty_like(q)
+    _require(out, "out", torch.bfloat16)
+    if workspace is None:
+        workspace = alloc_decode_workspace(cache, B, Hq, num_splits)
+    _require(workspace, "workspace", torch.uint8)
+    rc = _lib.nvfp4_paged_decode_attention_append(cache.desc, _ptr(k_new), _ptr(v_new), stride, _ptr(q), B, Hq,
+                                                  _ptr(block_table), int(block_table.shape[1]), _ptr(seq_lens),
+                                                  float(sm_scale), _ptr(out), _ptr(workspace), workspace.numel(),
+                                                  int(num_splits), _stream(stream))
+    _check(rc, "nvfp4_paged_decode_attention_append")
     return out
 
 

@@ -76,6 +76,49 @@ size_t g_prof_every = 1;
 
 }  // namespace
 
+namespace {
+
+int decode_entry(const nvfp4kv_cache *cache, const void *k_new, const void *v_new, int64_t new_stride, const void *q,
+                 int batch, int num_q_heads, const int32_t *block_table, int max_pages_per_seq,
+                 const int32_t *seq_lens, float sm_scale, void *out, void *workspace, size_t workspace_bytes,
+                 int num_splits, cudaStream_t stream) {
+    int rc = check_cache(cache);
+    if (rc) return rc;
+    if (batch < 0 || num_q_heads < 1 || num_q_heads % cache->num_kv_heads || num_splits < 0) return NVFP4KV_EINVAL;
+    if (num_q_heads / cache->num_kv_heads > 16) return NVFP4KV_EUNSUPPORTED;
+    if (!isfinite(sm_scale)) return NVFP4KV_EINVAL;
+    if (batch == 0) return NVFP4KV_OK;
+    if (!q || !block_table || !seq_lens || !out || !workspace) return NVFP4KV_EINVAL;
+    if (max_pages_per_seq < 1) return NVFP4KV_EINVAL;
+    if (!aligned(q, 16) || !aligned(out, 16) || !aligned(workspace, 256) || !aligned(block_table, 4) ||
+        !aligned(seq_lens, 4))
+        return NVFP4KV_EINVAL;
+    if (k_new || v_new) {
+        if (!k_new || !v_new || !aligned(k_new, 16) || !aligned(v_new, 16)) return NVFP4KV_EINVAL;
+        if (new_stride < (int64_t)cache->num_kv_heads * kHeadDim || new_stride % 8) return NVFP4KV_EINVAL;
+    }
+    const int G = num_q_heads / cache->num_kv_heads;
+    cudaError_t e = cudaSuccess;
+    const int grid = num_splits ? num_splits : decode_auto_grid(*cache, G, &e);
+    if (e != cudaSuccess || grid <= 0) return NVFP4KV_ECUDA;
+    if (workspace_bytes < decode_workspace_bytes(*cache, batch, num_q_heads, grid)) return NVFP4KV_EINVAL;
+    unsigned *err = error_word(&e);
+    if (!err) return NVFP4KV_ECUDA;
+    cudaEvent_t before = nullptr, after = nullptr;
+    if (!g_prof_before.empty()) {
+        const size_t call = g_prof_next++;
+        if (call % g_prof_every == 0) {
+            const size_t i = (call / g_prof_every) % g_prof_before.size();
+            before = g_prof_before[i];
+            after = g_prof_after[i];
+        }
+    }
+    return from_cuda(launch_decode(*cache, q, batch, num_q_heads, block_table, max_pages_per_seq, seq_lens, sm_scale,
+                                   out, workspace, grid, err, stream, before, after, k_new, v_new, new_stride));
+}
+
+}  // namespace
+
 extern "C" {
 
 int nvfp4kv_version(void) { return 100; }
@@ -173,35 +216,18 @@ int nvfp4_paged_decode_attention(const nvfp4kv_cache *cache, const void *q, int 
                                  const int32_t *block_table, int max_pages_per_seq, const int32_t *seq_lens,
                                  float sm_scale, void *out, void *workspace, size_t workspace_bytes, int num_splits,
                                  cudaStream_t stream) {
-    int rc = check_cache(cache);
-    if (rc) return rc;
-    if (batch < 0 || num_q_heads < 1 || num_q_heads % cache->num_kv_heads || num_splits < 0) return NVFP4KV_EINVAL;
-    if (num_q_heads / cache->num_kv_heads > 16) return NVFP4KV_EUNSUPPORTED;
-    if (!isfinite(sm_scale)) return NVFP4KV_EINVAL;
-    if (batch == 0) return NVFP4KV_OK;
-    if (!q || !block_table || !seq_lens || !out || !workspace) return NVFP4KV_EINVAL;
-    if (max_pages_per_seq < 1) return NVFP4KV_EINVAL;
-    if (!aligned(q, 16) || !aligned(out, 16) || !aligned(workspace, 256) || !aligned(block_table, 4) ||
-        !aligned(seq_lens, 4))
-        return NVFP4KV_EINVAL;
-    const int G = num_q_heads / cache->num_kv_heads;
-    cudaError_t e = cudaSuccess;
-    const int grid = num_splits ? num_splits : decode_auto_grid(*cache, G, &e);
-    if (e != cudaSuccess || grid <= 0) return NVFP4KV_ECUDA;
-    if (workspace_bytes < decode_workspace_bytes(*cache, batch, num_q_heads, grid)) return NVFP4KV_EINVAL;
-    unsigned *err = error_word(&e);
-    if (!err) return NVFP4KV_ECUDA;
-    cudaEvent_t before = nullptr, after = nullptr;
-    if (!g_prof_before.empty()) {
-        const size_t call = g_prof_next++;
-        if (call % g_prof_every == 0) {
-            const size_t i = (call / g_prof_every) % g_prof_before.size();
-            before = g_prof_before[i];
-            after = g_prof_after[i];
-        }
-    }
-    return from_cuda(launch_decode(*cache, q, batch, num_q_heads, block_table, max_pages_per_seq, seq_lens, sm_scale,
-                                   out, workspace, grid, err, stream, before, after));
+    return decode_entry(cache, nullptr, nullptr, 0, q, batch, num_q_heads, block_table, max_pages_per_seq, seq_lens,
+                        sm_scale, out, workspace, workspace_bytes, num_splits, stream);
+}
+
+int nvfp4_paged_decode_attention_append(const nvfp4kv_cache *cache, const void *k_new, const void *v_new,
+                                        int64_t new_stride, const void *q, int batch, int num_q_heads,
+                                        const int32_t *block_table, int max_pages_per_seq, const int32_t *seq_lens,
+                                        float sm_scale, void *out, void *workspace, size_t workspace_bytes,
+                                        int num_splits, cudaStream_t stream) {
+    if (!k_new || !v_new) return NVFP4KV_EINVAL;
+    return decode_entry(cache, k_new, v_new, new_stride, q, batch, num_q_heads, block_table, max_pages_per_seq,
+                        seq_lens, sm_scale, out, workspace, workspace_bytes, num_splits, stream);
 }
 
 int nvfp4_prefix_dequant(const nvfp4kv_cache *cache, const int32_t *block_table, int max_pages_per_seq,

@@ -55,6 +55,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "quantize.cuh"
 
 namespace nvfp4kv {
 
@@ -113,6 +114,13 @@ struct DecodeArgs {
     float2 *part_ml;  // [slots][kWarps][G]
     int grid;
     unsigned *err;
+    // fused append (nullptr k_new: none): sequence b's new token, row b of
+    // k_new / v_new, is quantised into position seq_lens[b] - 1 first
+    const uint4 *k_new, *v_new;
+    int64_t new_stride16;  // row stride in 16-byte units
+    float gk_q, gv_q;      // tensor scales for the quantisation
+    int dtype, unit_scale;
+    uint8_t *pool_w;       // the pool, writable
 };
 
 __device__ __forceinline__ int clamp_len(int32_t n, int64_t cap) {
@@ -243,8 +251,6 @@ __device__ __forceinline__ void issue_stage(const DecodeArgs &a, uint64_t codes,
     }
 }
 
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
 // (a & m) | (b & ~m)
 __device__ __forceinline__ uint32_t bitsel(uint32_t m, uint32_t a, uint32_t b) {
@@ -582,6 +588,46 @@ __device__ __forceinline__ bool wait_issued(const int *seq, int want, const vola
     return false;
 }
 
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Fused append: the CTA that owns the last unit of a (sequence, kv_head) pair
+// is the only one that reads the sequence's last token, so it quantises that
+// token (16 threads per pair: K and V x 8 blocks) before any of its copies
+// are issued.  Pairs are visited from the one holding unit u0 on.
+__device__ __forceinline__ void fused_append(const DecodeArgs &a, int64_t u0, int64_t u1, int tid) {
+    int lo = 0, hi = a.B - 1;  // the sequence holding unit u0
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if ((int64_t)a.Hkv * a.chunk_prefix[mid] <= u0) lo = mid;
+        else hi = mid - 1;
+    }
+    const int nch0 = (int)(a.chunk_prefix[lo + 1] - a.chunk_prefix[lo]);
+    const int64_t first_pair = (int64_t)lo * a.Hkv + (u0 - (int64_t)a.Hkv * a.chunk_prefix[lo]) / nch0;
+    const int part = tid & 15, which = part >> 3, blk = part & 7;
+    for (int64_t p = first_pair + (tid >> 4);; p += kThreads / 16) {
+        const int b = (int)(p / a.Hkv), kv = (int)(p - (int64_t)b * a.Hkv);
+        if (b >= a.B) break;
+        const int64_t nch = a.chunk_prefix[b + 1] - a.chunk_prefix[b];
+        const int64_t start = (int64_t)a.Hkv * a.chunk_prefix[b] + kv * nch;
+        if (start >= u1) break;
+        if (nch == 0 || start + nch - 1 >= u1) continue;  // its last unit belongs to a later CTA
+        const int t = clamp_len(a.seq_lens[b], (int64_t)a.max_pages * a.P) - 1;
+        const int32_t pg = __ldg(a.block_table + (int64_t)b * a.max_pages + (t >> a.log2P));
+        if (pg < 0 || (int64_t)pg >= a.num_pages) {
+            if (part == 0) flag_error(a.err, kErrPage);
+            continue;
+        }
+        const uint4 *src = (which ? a.v_new : a.k_new) + (int64_t)b * a.new_stride16 + kv * (kHeadDim / 8) + blk * 2;
+        uint8_t *slab = a.pool_w + ((int64_t)pg * a.Hkv + kv) * a.slab;
+        if (a.unit_scale)
+            store_block<true>(slab, a.dtype, t & (a.P - 1), which, blk, src, 1.0f);
+        else
+            store_block<false>(slab, a.dtype, t & (a.P - 1), which, blk, src, which ? a.gv_q : a.gk_q);
+    }
+}
+
 // A CTA streams its contiguous range of 64-token units through a ring of
 // kSlots stages shared by its kWarps warps: unit i of the range is computed
 // by warp i % kWarps from stage i % kSlots, and the warp that used a stage
@@ -615,6 +661,10 @@ __global__ void __launch_bounds__(kThreads, DTYPE == NVFP4KV_DTYPE_NVFP4 && NT =
         }
         *abort_flag = 0;
         fence_mbar_init();
+    }
+    if (a.k_new) {
+        fused_append(a, u0, u1, tid);
+        fence_proxy_async_global();  // the stores above before this CTA's bulk reads of the same rows
     }
     __syncthreads();
 
@@ -1001,7 +1051,8 @@ size_t decode_workspace_bytes(const nvfp4kv_cache &c, int batch, int num_q_heads
 cudaError_t launch_decode(const nvfp4kv_cache &c, const void *q, int batch, int num_q_heads,
                           const int32_t *block_table, int max_pages, const int32_t *seq_lens, float sm_scale,
                           void *out, void *workspace, int grid, unsigned *err, cudaStream_t stream,
-                          cudaEvent_t before, cudaEvent_t after) {
+                          cudaEvent_t before, cudaEvent_t after, const void *k_new, const void *v_new,
+                          int64_t new_stride) {
     const int G = num_q_heads / c.num_kv_heads;
     const int nt = G <= 8 ? 1 : 2;
     cudaError_t e = prepare_kernel(c.dtype, nt, nullptr);
@@ -1041,6 +1092,14 @@ cudaError_t launch_decode(const nvfp4kv_cache &c, const void *q, int batch, int 
     a.part_ml = part_ml;
     a.grid = grid;
     a.err = err;
+    a.k_new = static_cast<const uint4 *>(k_new);
+    a.v_new = static_cast<const uint4 *>(v_new);
+    a.new_stride16 = new_stride / 8;
+    a.gk_q = c.k_global_scale;
+    a.gv_q = c.v_global_scale;
+    a.dtype = c.dtype;
+    a.unit_scale = c.k_global_scale == 1.0f && c.v_global_scale == 1.0f;
+    a.pool_w = static_cast<uint8_t *>(c.pool);
     int smem = 0;
     const void *fn = select_kernel(c.dtype, nt, &smem);
     void *args[] = {&a};

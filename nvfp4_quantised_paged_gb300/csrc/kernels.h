@@ -24,10 +24,13 @@ int decode_auto_grid(const nvfp4kv_cache &c, int group, cudaError_t *status);
 size_t decode_workspace_bytes(const nvfp4kv_cache &c, int batch, int num_q_heads, int grid);
 
 // before / after: optional events recorded around the decode kernel launch.
+// k_new / v_new (nullptr: no fused append): BF16 rows [batch][new_stride]
+// quantised into position seq_lens[b] - 1 of each sequence before attending.
 cudaError_t launch_decode(const nvfp4kv_cache &c, const void *q, int batch, int num_q_heads,
                           const int32_t *block_table, int max_pages, const int32_t *seq_lens, float sm_scale,
                           void *out, void *workspace, int grid, unsigned *err, cudaStream_t stream,
-                          cudaEvent_t before, cudaEvent_t after);
+                          cudaEvent_t before, cudaEvent_t after, const void *k_new = nullptr,
+                          const void *v_new = nullptr, int64_t new_stride = 0);
 
 // Attention of each request's chunk over [its BF16 prefix rows || its chunk], causal in the chunk.
 cudaError_t launch_extend(const void *q, const void *k_prefix, const void *v_prefix, const int32_t *cu_prefix,

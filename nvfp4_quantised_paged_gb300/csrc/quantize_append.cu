@@ -26,6 +26,7 @@
 // against every scale).  For g != 1 the kernel divides with IEEE division.
 #include "common.cuh"
 #include "kernels.h"
+#include "quantize.cuh"
 
 namespace nvfp4kv {
 
@@ -44,66 +45,13 @@ struct AppendArgs {
     int64_t stride16;   // token stride in 16-byte units
     const int64_t *slots;
     float gk, gv;
+    int dtype;
     unsigned *err;
 };
 
-// Round a float to 13 significant bits (half-way cases away from zero); exact
-// values with <= 13 bits are unchanged.
-__device__ __forceinline__ float snap13(float y) {
-    uint32_t b = __float_as_uint(y);
-    b = (b + 0x400u) & ~0x7ffu;
-    return __uint_as_float(b);
-}
-
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
-
-template <bool kUnitScale>
-__device__ __forceinline__ void quantize_block16(const uint4 &a, const uint4 &b, float g, uint2 &codes,
-                                                 uint32_t &scale_byte) {
-    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-    // amax over BF16 magnitudes: unsigned order of |bf16| bit patterns is numeric order
-    uint32_t m = 0;
-#pragma unroll
-    for (int i = 0; i < 8; i++) m = __vmaxu2(m, w[i] & 0x7fff7fffu);
-    const uint32_t amax_bits = (m >> 16) > (m & 0xffffu) ? (m >> 16) : (m & 0xffffu);
-    const float amax = __uint_as_float(amax_bits << 16);
-    const float q = kUnitScale ? __fdiv_rn(amax, 6.0f) : __fdiv_rn(amax, __fmul_rn(6.0f, g));
-    const uint32_t s = f32x2_to_e4m3x2(0.0f, q) & 0xffu;
-    scale_byte = s;
-    const float sd = __half2float(__ushort_as_half((uint16_t)(e4m3x2_to_f16x2(s) & 0xffffu)));
-    uint32_t packed[2] = {0u, 0u};
-    if (sd == 0.0f) {
-        // signed zeros: code 8 where the input is negative
-#pragma unroll
-        for (int i = 0; i < 8; i++) {
-            const uint32_t lo_neg = (w[i] >> 15) & 1u, hi_neg = w[i] >> 31;
-            const uint32_t byte = (lo_neg << 3) | (hi_neg << 7);
-            packed[i / 4] |= byte << (8 * (i % 4));
-        }
-    } else if (kUnitScale) {
-        const float r = __frcp_rn(sd);
-#pragma unroll
-        for (int i = 0; i < 8; i++) {
-            const float lo = snap13(bf16_lo(w[i]) * r);
-            const float hi = snap13(bf16_hi(w[i]) * r);
-            packed[i / 4] |= f32x2_to_e2m1x2(hi, lo) << (8 * (i % 4));
-        }
-    } else {
-        const float d = __fmul_rn(sd, g);
-#pragma unroll
-        for (int i = 0; i < 8; i++) {
-            const float lo = __fdiv_rn(bf16_lo(w[i]), d);
-            const float hi = __fdiv_rn(bf16_hi(w[i]), d);
-            packed[i / 4] |= f32x2_to_e2m1x2(hi, lo) << (8 * (i % 4));
-        }
-    }
-    codes = make_uint2(packed[0], packed[1]);
-}
-
 // Thread id -> (token, kv_head, which, block), block fastest.
 template <bool kUnitScale>
-__global__ void __launch_bounds__(256) append_nvfp4_kernel(AppendArgs a) {
+__global__ void __launch_bounds__(256) append_kernel(AppendArgs a) {
     pdl_launch_dependents();  // a dependent decode plan may launch early; it waits for this kernel
     // the host guarantees num_tokens * Hkv * 16 < 2^31
     const uint32_t id = blockIdx.x * blockDim.x + threadIdx.x;
@@ -121,60 +69,9 @@ __global__ void __launch_bounds__(256) append_nvfp4_kernel(AppendArgs a) {
         return;
     }
     const uint4 *src = (which ? a.v : a.k) + t * a.stride16 + h * (kHeadDim / 8) + blk * 2;
-    const uint4 x0 = __ldg(src), x1 = __ldg(src + 1);
-    uint2 codes;
-    uint32_t sbyte;
-    quantize_block16<kUnitScale>(x0, x1, which ? a.gv : a.gk, codes, sbyte);
     const int64_t page = slot >> a.log2P;
-    const int r = (int)(slot & (a.P - 1));
-    // 16-token groups of 2304 bytes: K codes | K scales | V codes | V scales [8][16]
-    uint8_t *grp = a.pool + (page * a.Hkv + h) * a.slab + (r >> 4) * 2304;
-    const int rr = r & 15;
-    *reinterpret_cast<uint2 *>(grp + (which ? 1152 : 0) + rr * 64 + blk * 8) = codes;
-    grp[which ? 2176 + blk * 16 + rr : 1024 + rr * 8 + blk] = (uint8_t)sbyte;
-}
-
-// FP8 pool: one thread converts one 16-value block to 16 E4M3 bytes.
-template <bool kUnitScale>
-__global__ void __launch_bounds__(256) append_fp8_kernel(AppendArgs a) {
-    pdl_launch_dependents();  // a dependent decode plan may launch early; it waits for this kernel
-    // the host guarantees num_tokens * Hkv * 16 < 2^31
-    const uint32_t id = blockIdx.x * blockDim.x + threadIdx.x;
-    if (id >= (uint32_t)(a.num_tokens * a.Hkv * 16)) return;
-    const int blk = (int)(id & 7);
-    const int which = (int)((id >> 3) & 1);
-    const uint32_t th = id >> 4;
-    const uint32_t t32 = th / (uint32_t)a.Hkv;
-    const int h = (int)(th - t32 * (uint32_t)a.Hkv);
-    const int64_t t = t32;
-    const int64_t slot = __ldg(a.slots + t);
-    if (slot < 0) return;
-    if (slot >= a.num_slots) {
-        if (blk == 0 && which == 0 && h == 0) flag_error(a.err, kErrSlot);
-        return;
-    }
-    const uint4 *src = (which ? a.v : a.k) + t * a.stride16 + h * (kHeadDim / 8) + blk * 2;
-    const uint4 x0 = __ldg(src), x1 = __ldg(src + 1);
-    const uint32_t w[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-    const float g = which ? a.gv : a.gk;
-    uint32_t out[4];
-#pragma unroll
-    for (int i = 0; i < 4; i++) {
-        float e0 = bf16_lo(w[2 * i]), e1 = bf16_hi(w[2 * i]), e2 = bf16_lo(w[2 * i + 1]), e3 = bf16_hi(w[2 * i + 1]);
-        if (!kUnitScale) {
-            e0 = __fdiv_rn(e0, g);
-            e1 = __fdiv_rn(e1, g);
-            e2 = __fdiv_rn(e2, g);
-            e3 = __fdiv_rn(e3, g);
-        }
-        out[i] = f32x2_to_e4m3x2(e1, e0) | (f32x2_to_e4m3x2(e3, e2) << 16);
-    }
-    const int64_t page = slot >> a.log2P;
-    const int r = (int)(slot & (a.P - 1));
-    // 16-token groups of 4096 bytes: K codes [16][128] | V codes [16][128]
-    uint8_t *dst = a.pool + (page * a.Hkv + h) * a.slab + (r >> 4) * 4096 + (which ? 2048 : 0) + (r & 15) * 128 +
-                   blk * 16;
-    *reinterpret_cast<uint4 *>(dst) = make_uint4(out[0], out[1], out[2], out[3]);
+    store_block<kUnitScale>(a.pool + (page * a.Hkv + h) * a.slab, a.dtype, (int)(slot & (a.P - 1)), which, blk, src,
+                            which ? a.gv : a.gk);
 }
 
 }  // namespace
@@ -196,22 +93,16 @@ cudaError_t launch_quantize_append(const nvfp4kv_cache &c, const void *k, const 
     a.slots = slot_mapping;
     a.gk = c.k_global_scale;
     a.gv = c.v_global_scale;
+    a.dtype = c.dtype;
     a.err = err;
     const int64_t threads = num_tokens * c.num_kv_heads * 2 * 8;
     const int block = 256;
     const int64_t grid = ceil_div64(threads, block);
     const bool unit = c.k_global_scale == 1.0f && c.v_global_scale == 1.0f;
-    if (c.dtype == NVFP4KV_DTYPE_NVFP4) {
-        if (unit)
-            append_nvfp4_kernel<true><<<(unsigned)grid, block, 0, stream>>>(a);
-        else
-            append_nvfp4_kernel<false><<<(unsigned)grid, block, 0, stream>>>(a);
-    } else {
-        if (unit)
-            append_fp8_kernel<true><<<(unsigned)grid, block, 0, stream>>>(a);
-        else
-            append_fp8_kernel<false><<<(unsigned)grid, block, 0, stream>>>(a);
-    }
+    if (unit)
+        append_kernel<true><<<(unsigned)grid, block, 0, stream>>>(a);
+    else
+        append_kernel<false><<<(unsigned)grid, block, 0, stream>>>(a);
     return cudaGetLastError();
 }
 
