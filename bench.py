@@ -430,6 +430,53 @@ def time_extend(m, device, steps, warmup, peak_tflops):
     return res
 
 
+def time_agent_decode(m, device, steps, warmup):
+    """Decode of the agent mix's 128 sequences (shared 3,200-token prefix): the plain
+    decode call against the cascade call that attends the shared pages once per kv head."""
+    import torch
+
+    import workloads
+    mix = workloads.agent_mix()
+    w = mix.decode
+    cache = m.PagedCache(w.num_pages, w.page_size, w.num_kv_heads, device=device)
+    fill_cache(m, w, cache, device)
+    dec = list(range(mix.num_decode))
+    q = w.q(device)[dec].contiguous()
+    bt = w.block_table[dec].contiguous().to(device)
+    sl = w.seq_lens[dec].contiguous().to(device)
+    shared = w.shared_prefix_tokens
+    sp = w.block_table[0, :shared // w.page_size].contiguous().to(device)
+    out = torch.empty_like(q)
+    ws = torch.empty(max(m.cascade_workspace_bytes(cache, len(dec), w.num_q_heads, shared), 256),
+                     dtype=torch.uint8, device=device)
+    res = {"workload": "agent-mix decode: 128 sequences of %d-%d tokens sharing %d, q32kv8 p64"
+           % (int(sl.min()), int(sl.max()), shared)}
+    calls = {"plain_us": lambda: m.paged_decode_attention(cache, q, bt, sl, w.sm_scale, out=out, workspace=ws),
+             "cascade_us": lambda: m.cascade_decode_attention(cache, q, sp, shared, bt, sl, w.sm_scale, out=out,
+                                                              workspace=ws)}
+    for key, fn in calls.items():
+        for _ in range(warmup):
+            fn()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        s.record()
+        for _ in range(steps):
+            fn()
+        e.record()
+        torch.cuda.synchronize()
+        res[key] = s.elapsed_time(e) / steps * 1e3
+    assert m.check_device_errors() == 0
+    logical = int(sl.sum()) * w.num_kv_heads * 144
+    unique = (int(sl.sum()) - (len(dec) - 1) * shared) * w.num_kv_heads * 144
+    res.update({"logical_kv_bytes": logical, "unique_kv_bytes": unique,
+                "plain_logical_gb_per_s": logical / res["plain_us"] / 1e3,
+                "cascade_logical_gb_per_s": logical / res["cascade_us"] / 1e3,
+                "cascade_speedup": res["plain_us"] / res["cascade_us"]})
+    del cache
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_ours(args):
     import torch
 
@@ -592,6 +639,7 @@ def run_ours(args):
         comp["append_65k"] = time_append(m, device, 50, 5)
         comp["calibrate_65k"] = time_calibrate(m, device, 50, 5)
         comp["extend_agent_mix"] = time_extend(m, device, 10, 2, load_bf16_peak())
+        comp["decode_agent_mix"] = time_agent_decode(m, device, 20, 3)
         line["comparisons"] = comp
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -184,6 +184,35 @@ NVFP4KV_API int nvfp4_paged_decode_attention(const nvfp4kv_cache *cache, const v
                                  cudaStream_t stream);
 
 /*
+ * Cascade decode: decode attention for sequences that all begin with the same
+ * shared_len tokens, stored once in the pages shared_pages[0 ..
+ * shared_len/P - 1] (and listed first in every sequence's block table).
+ * Source: section A4 (agentic workloads share a long common prefix, kept once
+ * by the radix cache) and section A2, path 3.  The shared pages are read and
+ * dequantised once per kv head and multiplied with the queries of all
+ * sequences together; each sequence's remaining tokens are decoded as in
+ * nvfp4_paged_decode_attention, and the two partial softmaxes are merged by
+ * log-sum-exp.  The result equals nvfp4_paged_decode_attention on the same
+ * arguments up to floating-point summation order.
+ *
+ *   shared_pages  device int32 [shared_len / P] page ids.
+ *   shared_len    tokens of the shared prefix: > 0, a multiple of 64 and of P.
+ *   workspace     device, >= nvfp4kv_cascade_workspace_bytes(...), 256-aligned.
+ * Every seq_lens[b] must be >= shared_len (a shorter one is flagged in the
+ * device error word and only its shared part is attended).  NVFP4 pools only
+ * (NVFP4KV_EUNSUPPORTED for FP8).  Other arguments as
+ * nvfp4_paged_decode_attention.
+ */
+NVFP4KV_API size_t nvfp4kv_cascade_workspace_bytes(const nvfp4kv_cache *cache, int batch, int num_q_heads,
+                                                   int num_splits, int shared_len);
+NVFP4KV_API int nvfp4_cascade_decode_attention(const nvfp4kv_cache *cache, const void *q, int batch,
+                                               int num_q_heads, const int32_t *shared_pages, int shared_len,
+                                               const int32_t *block_table, int max_pages_per_seq,
+                                               const int32_t *seq_lens, float sm_scale, void *out,
+                                               void *workspace, size_t workspace_bytes, int num_splits,
+                                               cudaStream_t stream);
+
+/*
  * Decode step with the new token appended in the same launch.
  * Source: section A2, path 3 (decode reads the NVFP4 cache in-kernel) with
  * path 1's quantise-and-write of the new token's K/V fused in front of it.

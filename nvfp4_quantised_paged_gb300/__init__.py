@@ -68,6 +68,8 @@ def _load_library():
         "nvfp4kv_calibrate_global_scales": (i32, [P, P, i64, i32, i64, P, P]),
         "nvfp4_extend_attention": (i32, [P, P, P, P, P, P, P, i32, i32, i32, i32, f32, P, P]),
         "nvfp4_paged_decode_attention_append": (i32, [D, P, P, i64, P, i32, i32, P, i32, P, f32, P, P, sz, i32, P]),
+        "nvfp4kv_cascade_workspace_bytes": (sz, [D, i32, i32, i32, i32]),
+        "nvfp4_cascade_decode_attention": (i32, [D, P, i32, i32, P, i32, P, i32, P, f32, P, P, sz, i32, P]),
         "nvfp4kv_profile_decode": (i32, [P, P, i32, i32]),
         "nvfp4_paged_decode_attention_noalloc": (i32, [D, P, i32, i32, P, i32, P, f32, P, i32, P]),
     }
@@ -85,7 +87,8 @@ EXPORTED_SYMBOLS = ("nvfp4kv_version", "nvfp4kv_status_string", "nvfp4kv_slab_by
                     "nvfp4_paged_decode_attention", "nvfp4_prefix_dequant", "nvfp4kv_check_device_errors",
                     "nvfp4kv_profile_decode", "nvfp4_paged_decode_attention_noalloc",
                     "nvfp4kv_selftest_bounded_wait", "nvfp4kv_calibrate_global_scales", "nvfp4_extend_attention",
-                    "nvfp4_paged_decode_attention_append")
+                    "nvfp4_paged_decode_attention_append", "nvfp4kv_cascade_workspace_bytes",
+                    "nvfp4_cascade_decode_attention")
 
 NOALLOC_SCRATCH_BYTES = 64 << 20  # NVFP4KV_NOALLOC_SCRATCH_BYTES of the header
 
@@ -277,6 +280,44 @@ def paged_decode_attention_append(cache: PagedCache, k_new: torch.Tensor, v_new:
                                                   float(sm_scale), _ptr(out), _ptr(workspace), workspace.numel(),
                                                   int(num_splits), _stream(stream))
     _check(rc, "nvfp4_paged_decode_attention_append")
+    return out
+
+
+def cascade_workspace_bytes(cache: PagedCache, batch: int, num_q_heads: int, shared_len: int,
+                            num_splits: int = 0) -> int:
+    n = _lib.nvfp4kv_cascade_workspace_bytes(cache.desc, int(batch), int(num_q_heads), int(num_splits),
+                                             int(shared_len))
+    if n == 0 and batch > 0:
+        raise NVFP4KVError(-1, "cascade_workspace_bytes")
+    return int(n)
+
+
+def cascade_decode_attention(cache: PagedCache, q: torch.Tensor, shared_pages: torch.Tensor, shared_len: int,
+                             block_table: torch.Tensor, seq_lens: torch.Tensor, sm_scale: Optional[float] = None,
+                             out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                             num_splits: int = 0, stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """Decode attention for sequences sharing their first shared_len tokens (pages
+    shared_pages, int32 [shared_len / P]); the shared part is attended once per kv
+    head for all sequences, then merged with each sequence's own part."""
+    _require(q, "q", torch.bfloat16)
+    _require(shared_pages, "shared_pages", torch.int32)
+    _require(block_table, "block_table", torch.int32)
+    _require(seq_lens, "seq_lens", torch.int32)
+    B, Hq = int(q.shape[0]), int(q.shape[1])
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(HEAD_DIM)
+    if out is None:
+        out = torch.empty_like(q)
+    _require(out, "out", torch.bfloat16)
+    if workspace is None:
+        n = cascade_workspace_bytes(cache, B, Hq, shared_len, num_splits)
+        workspace = torch.empty(max(n, 256), dtype=torch.uint8, device=cache.pool.device)
+    _require(workspace, "workspace", torch.uint8)
+    rc = _lib.nvfp4_cascade_decode_attention(cache.desc, _ptr(q), B, Hq, _ptr(shared_pages), int(shared_len),
+                                             _ptr(block_table), int(block_table.shape[1]), _ptr(seq_lens),
+                                             float(sm_scale), _ptr(out), _ptr(workspace), workspace.numel(),
+                                             int(num_splits), _stream(stream))
+    _check(rc, "nvfp4_cascade_decode_attention")
     return out
 
 

@@ -81,7 +81,7 @@ namespace {
 int decode_entry(const nvfp4kv_cache *cache, const void *k_new, const void *v_new, int64_t new_stride, const void *q,
                  int batch, int num_q_heads, const int32_t *block_table, int max_pages_per_seq,
                  const int32_t *seq_lens, float sm_scale, void *out, void *workspace, size_t workspace_bytes,
-                 int num_splits, cudaStream_t stream) {
+                 int num_splits, cudaStream_t stream, const int32_t *shared_pages = nullptr, int shared_len = 0) {
     int rc = check_cache(cache);
     if (rc) return rc;
     if (batch < 0 || num_q_heads < 1 || num_q_heads % cache->num_kv_heads || num_splits < 0) return NVFP4KV_EINVAL;
@@ -97,11 +97,19 @@ int decode_entry(const nvfp4kv_cache *cache, const void *k_new, const void *v_ne
         if (!k_new || !v_new || !aligned(k_new, 16) || !aligned(v_new, 16)) return NVFP4KV_EINVAL;
         if (new_stride < (int64_t)cache->num_kv_heads * kHeadDim || new_stride % 8) return NVFP4KV_EINVAL;
     }
+    if (shared_pages) {
+        if (cache->dtype != NVFP4KV_DTYPE_NVFP4) return NVFP4KV_EUNSUPPORTED;
+        if (!aligned(shared_pages, 4) || shared_len <= 0 || shared_len % 64 || shared_len % cache->page_size ||
+            (int64_t)shared_len > (int64_t)max_pages_per_seq * cache->page_size)
+            return NVFP4KV_EINVAL;
+    }
     const int G = num_q_heads / cache->num_kv_heads;
     cudaError_t e = cudaSuccess;
     const int grid = num_splits ? num_splits : decode_auto_grid(*cache, G, &e);
     if (e != cudaSuccess || grid <= 0) return NVFP4KV_ECUDA;
-    if (workspace_bytes < decode_workspace_bytes(*cache, batch, num_q_heads, grid)) return NVFP4KV_EINVAL;
+    size_t need = decode_workspace_bytes(*cache, batch, num_q_heads, grid);
+    if (shared_pages) need += cascade_extra_bytes(*cache, batch, num_q_heads, shared_len);
+    if (workspace_bytes < need) return NVFP4KV_EINVAL;
     unsigned *err = error_word(&e);
     if (!err) return NVFP4KV_ECUDA;
     cudaEvent_t before = nullptr, after = nullptr;
@@ -114,7 +122,8 @@ int decode_entry(const nvfp4kv_cache *cache, const void *k_new, const void *v_ne
         }
     }
     return from_cuda(launch_decode(*cache, q, batch, num_q_heads, block_table, max_pages_per_seq, seq_lens, sm_scale,
-                                   out, workspace, grid, err, stream, before, after, k_new, v_new, new_stride));
+                                   out, workspace, grid, err, stream, before, after, k_new, v_new, new_stride,
+                                   shared_pages, shared_len));
 }
 
 }  // namespace
@@ -218,6 +227,22 @@ int nvfp4_paged_decode_attention(const nvfp4kv_cache *cache, const void *q, int 
                                  cudaStream_t stream) {
     return decode_entry(cache, nullptr, nullptr, 0, q, batch, num_q_heads, block_table, max_pages_per_seq, seq_lens,
                         sm_scale, out, workspace, workspace_bytes, num_splits, stream);
+}
+
+size_t nvfp4kv_cascade_workspace_bytes(const nvfp4kv_cache *cache, int batch, int num_q_heads, int num_splits,
+                                       int shared_len) {
+    const size_t base = nvfp4kv_decode_workspace_bytes(cache, batch, num_q_heads, num_splits);
+    if (!base || shared_len <= 0 || shared_len % 64) return base;
+    return base + cascade_extra_bytes(*cache, batch, num_q_heads, shared_len);
+}
+
+int nvfp4_cascade_decode_attention(const nvfp4kv_cache *cache, const void *q, int batch, int num_q_heads,
+                                   const int32_t *shared_pages, int shared_len, const int32_t *block_table,
+                                   int max_pages_per_seq, const int32_t *seq_lens, float sm_scale, void *out,
+                                   void *workspace, size_t workspace_bytes, int num_splits, cudaStream_t stream) {
+    if (!shared_pages) return NVFP4KV_EINVAL;
+    return decode_entry(cache, nullptr, nullptr, 0, q, batch, num_q_heads, block_table, max_pages_per_seq, seq_lens,
+                        sm_scale, out, workspace, workspace_bytes, num_splits, stream, shared_pages, shared_len);
 }
 
 int nvfp4_paged_decode_attention_append(const nvfp4kv_cache *cache, const void *k_new, const void *v_new,

@@ -182,10 +182,10 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
-inline cudaError_t launch_pdl(const void *fn, unsigned grid, unsigned block, size_t smem, cudaStream_t stream,
+inline cudaError_t launch_pdl(const void *fn, dim3 grid, unsigned block, size_t smem, cudaStream_t stream,
                               void **args) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
+    cfg.gridDim = grid;
     cfg.blockDim = dim3(block);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;

@@ -121,6 +121,7 @@ struct DecodeArgs {
     float gk_q, gv_q;      // tensor scales for the quantisation
     int dtype, unit_scale;
     uint8_t *pool_w;       // the pool, writable
+    int skip;              // tokens at the start of every sequence left to the shared-prefix kernel
 };
 
 __device__ __forceinline__ int clamp_len(int32_t n, int64_t cap) {
@@ -180,7 +181,7 @@ __device__ __forceinline__ uint64_t part_src(const DecodeArgs &a, int64_t u0, in
     const int kv = rem / nch, ch = rem - kv * nch;
     const int n = clamp_len(a.seq_lens[lo], (int64_t)a.max_pages * a.P);
     const int span = a.P < kChunk ? a.P : kChunk;
-    const int t = ch * kChunk + part * span;
+    const int t = a.skip + ch * kChunk + part * span;
     if (t >= n) return 0;
     const int32_t pg = __ldg(a.block_table + (int64_t)lo * a.max_pages + (t >> a.log2P));
     if (pg < 0 || (int64_t)pg >= a.num_pages) return kBadPage;
@@ -765,7 +766,7 @@ __global__ void __launch_bounds__(kThreads, DTYPE == NVFP4KV_DTYPE_NVFP4 && NT =
         }
         const int mask = ok ? valid[slot] : 0;
         if (mask) {
-            const int left = cc.n - cc.ch * kChunk;
+            const int left = cc.n - a.skip - cc.ch * kChunk;
             const uint8_t *st = ring + slot * S::kStage;
             if (DTYPE == NVFP4KV_DTYPE_NVFP4 && left >= kChunk && mask == (1 << kGroups) - 1) {
                 const int vt[kGroups] = {16, 16, 16, 16};  // a whole chunk: no masking
@@ -815,9 +816,9 @@ __global__ void __launch_bounds__(kThreads, DTYPE == NVFP4KV_DTYPE_NVFP4 && NT =
     }
 }
 
-// Plan: chunk_prefix[b] = sum over b' < b of ceil(len(b') / 64); one CTA.
+// Plan: chunk_prefix[b] = sum over b' < b of ceil((len(b') - skip) / 64); one CTA.
 __global__ void __launch_bounds__(1024) plan_kernel(const int32_t *seq_lens, int B, int64_t max_tokens,
-                                                    int64_t *prefix, unsigned *err) {
+                                                    int64_t *prefix, unsigned *err, int skip) {
     __shared__ int64_t warp_sums[32];
     pdl_launch_dependents();  // let the decode kernel launch; it waits for this one to finish
     pdl_wait();               // seq_lens may come from earlier work on the stream
@@ -827,8 +828,8 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t *seq_lens, int
     int64_t local = 0;
     for (int b = lo; b < hi; b++) {
         const int32_t n = seq_lens[b];
-        if (n < 0 || (int64_t)n > max_tokens) flag_error(err, kErrSeqLen);
-        const int64_t m = n < 0 ? 0 : ((int64_t)n > max_tokens ? max_tokens : n);
+        if (n < skip || (int64_t)n > max_tokens) flag_error(err, kErrSeqLen);
+        const int64_t m = n < skip ? 0 : ((int64_t)n > max_tokens ? max_tokens : n) - skip;
         local += (m + kChunk - 1) / kChunk;
     }
     // block-wide exclusive scan of `local`
@@ -855,7 +856,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t *seq_lens, int
     for (int b = lo; b < hi; b++) {
         prefix[b] = run;
         const int32_t n = seq_lens[b];
-        const int64_t m = n < 0 ? 0 : ((int64_t)n > max_tokens ? max_tokens : n);
+        const int64_t m = n < skip ? 0 : ((int64_t)n > max_tokens ? max_tokens : n) - skip;
         run += (m + kChunk - 1) / kChunk;
     }
     if (tid == 1023) prefix[B] = warp_sums[31];
@@ -866,6 +867,9 @@ struct ReduceArgs {
     const int64_t *chunk_prefix;
     const float *part_acc;
     const float2 *part_ml;
+    const float *casc_acc;  // shared-prefix partials [casc_splits][B * Hkv][G] (nullptr: none)
+    const float2 *casc_ml;
+    int casc_splits;
     float gv;
     __nv_bfloat16 *out;
 };
@@ -898,60 +902,68 @@ __global__ void __launch_bounds__(32 * kReduceWarps) reduce_kernel(ReduceArgs a,
         const int b = (int)(row / a.Hq), h = (int)(row % a.Hq);
         const int kv = h / a.G, hh = h % a.G;
         nch = a.chunk_prefix[b + 1] - a.chunk_prefix[b];
+        const int64_t p = (int64_t)b * a.Hkv + kv;
+        const int64_t ncasc = a.casc_ml ? a.casc_splits : 0;
+        int64_t c0 = 0, c1 = -1, off = 0;
+        const int64_t U = (int64_t)a.Hkv * a.chunk_prefix[a.B];
         if (nch > 0) {
-            const int64_t U = (int64_t)a.Hkv * a.chunk_prefix[a.B];
-            const int64_t off = (int64_t)a.Hkv * a.chunk_prefix[b] + (int64_t)kv * nch;
-            const int64_t c0 = ((off + 1) * a.grid - 1) / U;
-            const int64_t c1 = ((off + nch) * a.grid - 1) / U;
-            const int64_t p = (int64_t)b * a.Hkv + kv;
-            // Candidate partials: (CTA cc, warp w) for cc in [c0, c1].  Warp w of
-            // CTA cc left one iff the CTA's units of this pair include one with
-            // index (within the CTA's range) = w mod kWarps; an empty CTA (possible
-            // when grid > U) left none.
-            auto has_partial = [&](int64_t cc, int w) {
-                const int64_t cu0 = cc * U / a.grid, cu1 = (cc + 1) * U / a.grid;
-                const int64_t lo = (off > cu0 ? off : cu0) - cu0;
-                const int64_t hi = (off + nch < cu1 ? off + nch : cu1) - cu0;
-                if (hi <= lo) return false;
-                return hi - lo > (int64_t)((w - lo % kWarps + kWarps) % kWarps);
-            };
-            const int64_t ncand = (c1 - c0 + 1) * kWarps;
-            for (int64_t base = sub; base < ncand; base += 4 * wpr) {
-                float2 ml[4];
-                float4 v[4];
+            off = (int64_t)a.Hkv * a.chunk_prefix[b] + (int64_t)kv * nch;
+            c0 = ((off + 1) * a.grid - 1) / U;
+            c1 = ((off + nch) * a.grid - 1) / U;
+        }
+        // Candidate partials: first the ncasc shared-prefix partials of the pair,
+        // then (CTA cc, warp w) for cc in [c0, c1].  Warp w of CTA cc left one iff
+        // the CTA's units of this pair include one with index (within the CTA's
+        // range) = w mod kWarps; an empty CTA (possible when grid > U) left none.
+        auto has_partial = [&](int64_t cc, int w) {
+            const int64_t cu0 = cc * U / a.grid, cu1 = (cc + 1) * U / a.grid;
+            const int64_t lo = (off > cu0 ? off : cu0) - cu0;
+            const int64_t hi = (off + nch < cu1 ? off + nch : cu1) - cu0;
+            if (hi <= lo) return false;
+            return hi - lo > (int64_t)((w - lo % kWarps + kWarps) % kWarps);
+        };
+        const int64_t ncand = ncasc + (c1 - c0 + 1) * kWarps;
+        for (int64_t base = sub; base < ncand; base += 4 * wpr) {
+            float2 ml[4];
+            float4 v[4];
 #pragma unroll
-                for (int k = 0; k < 4; k++) {
-                    const int64_t q = base + (int64_t)k * wpr;
-                    ml[k] = make_float2(kNegInf, 0.f);
-                    v[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-                    const int64_t cc = c0 + q / kWarps;
-                    const int w = (int)(q % kWarps);
-                    if (q < ncand && has_partial(cc, w)) {
+            for (int k = 0; k < 4; k++) {
+                const int64_t q = base + (int64_t)k * wpr;
+                ml[k] = make_float2(kNegInf, 0.f);
+                v[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (q < ncasc) {
+                    const int64_t idx = (q * a.B * a.Hkv + p) * a.G + hh;
+                    ml[k] = a.casc_ml[idx];
+                    v[k] = reinterpret_cast<const float4 *>(a.casc_acc + idx * kHeadDim)[lane];
+                } else if (q < ncand) {
+                    const int64_t cc = c0 + (q - ncasc) / kWarps;
+                    const int w = (int)((q - ncasc) % kWarps);
+                    if (has_partial(cc, w)) {
                         const int64_t idx = ((cc + p) * kWarps + w) * a.G + hh;
                         ml[k] = a.part_ml[idx];
                         v[k] = reinterpret_cast<const float4 *>(a.part_acc + idx * kHeadDim)[lane];
                     }
                 }
-                float mx = m_w;
-#pragma unroll
-                for (int k = 0; k < 4; k++) mx = fmaxf(mx, ml[k].x);
-                const float f0 = lse_factor(m_w, mx);
-                l_w *= f0;
-                acc.x *= f0;
-                acc.y *= f0;
-                acc.z *= f0;
-                acc.w *= f0;
-#pragma unroll
-                for (int k = 0; k < 4; k++) {
-                    const float f = lse_factor(ml[k].x, mx);
-                    l_w += f * ml[k].y;
-                    acc.x += f * v[k].x;
-                    acc.y += f * v[k].y;
-                    acc.z += f * v[k].z;
-                    acc.w += f * v[k].w;
-                }
-                m_w = mx;
             }
+            float mx = m_w;
+#pragma unroll
+            for (int k = 0; k < 4; k++) mx = fmaxf(mx, ml[k].x);
+            const float f0 = lse_factor(m_w, mx);
+            l_w *= f0;
+            acc.x *= f0;
+            acc.y *= f0;
+            acc.z *= f0;
+            acc.w *= f0;
+#pragma unroll
+            for (int k = 0; k < 4; k++) {
+                const float f = lse_factor(ml[k].x, mx);
+                l_w += f * ml[k].y;
+                acc.x += f * v[k].x;
+                acc.y += f * v[k].y;
+                acc.z += f * v[k].z;
+                acc.w += f * v[k].w;
+            }
+            m_w = mx;
         }
     }
     if (wpr > 1) {
@@ -1041,6 +1053,8 @@ int decode_auto_grid(const nvfp4kv_cache &c, int group, cudaError_t *status) {
     return e == cudaSuccess ? grid : 0;
 }
 
+// Workspace: chunk prefix | per-warp partials (m, l) | their acc; a cascade
+// call appends the shared-prefix partials (m, l) | their acc.
 size_t decode_workspace_bytes(const nvfp4kv_cache &c, int batch, int num_q_heads, int grid) {
     const int G = num_q_heads / c.num_kv_heads;
     const size_t slots = ((size_t)grid + (size_t)batch * c.num_kv_heads) * kWarps;
@@ -1048,11 +1062,16 @@ size_t decode_workspace_bytes(const nvfp4kv_cache &c, int batch, int num_q_heads
            sizeof(float) * slots * G * kHeadDim;
 }
 
+size_t cascade_extra_bytes(const nvfp4kv_cache &c, int batch, int num_q_heads, int shared_len) {
+    const size_t n = (size_t)cascade_splits(c, batch, num_q_heads, shared_len) * batch * num_q_heads;
+    return align256(sizeof(float2) * n) + sizeof(float) * n * kHeadDim;
+}
+
 cudaError_t launch_decode(const nvfp4kv_cache &c, const void *q, int batch, int num_q_heads,
                           const int32_t *block_table, int max_pages, const int32_t *seq_lens, float sm_scale,
                           void *out, void *workspace, int grid, unsigned *err, cudaStream_t stream,
                           cudaEvent_t before, cudaEvent_t after, const void *k_new, const void *v_new,
-                          int64_t new_stride) {
+                          int64_t new_stride, const int32_t *shared_pages, int shared_len) {
     const int G = num_q_heads / c.num_kv_heads;
     const int nt = G <= 8 ? 1 : 2;
     cudaError_t e = prepare_kernel(c.dtype, nt, nullptr);
@@ -1062,11 +1081,22 @@ cudaError_t launch_decode(const nvfp4kv_cache &c, const void *q, int batch, int 
     int64_t *prefix = reinterpret_cast<int64_t *>(ws);
     float2 *part_ml = reinterpret_cast<float2 *>(ws + align256(sizeof(int64_t) * ((size_t)batch + 1)));
     float *part_acc = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(part_ml) + align256(sizeof(float2) * slots * G));
+    const int csplits = shared_pages ? cascade_splits(c, batch, num_q_heads, shared_len) : 0;
+    float2 *casc_ml = reinterpret_cast<float2 *>(part_acc + slots * G * kHeadDim);
+    float *casc_acc = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(casc_ml) +
+                                                align256(sizeof(float2) * (size_t)csplits * batch * num_q_heads));
+    const int skip = shared_pages ? shared_len : 0;
 
     {
         int64_t max_tokens = (int64_t)max_pages * c.page_size;
-        void *pargs[] = {&seq_lens, &batch, &max_tokens, &prefix, &err};
+        int skip_arg = skip;
+        void *pargs[] = {&seq_lens, &batch, &max_tokens, &prefix, &err, &skip_arg};
         e = launch_pdl(reinterpret_cast<const void *>(&plan_kernel), 1, 1024, 0, stream, pargs);
+        if (e != cudaSuccess) return e;
+    }
+    if (shared_pages) {  // attention of every sequence's queries over the shared prefix, once per kv head
+        e = launch_shared_prefix(c, q, batch, num_q_heads, shared_pages, shared_len, csplits, sm_scale, casc_ml,
+                                 casc_acc, err, stream);
         if (e != cudaSuccess) return e;
     }
 
@@ -1100,6 +1130,7 @@ cudaError_t launch_decode(const nvfp4kv_cache &c, const void *q, int batch, int 
     a.dtype = c.dtype;
     a.unit_scale = c.k_global_scale == 1.0f && c.v_global_scale == 1.0f;
     a.pool_w = static_cast<uint8_t *>(c.pool);
+    a.skip = skip;
     int smem = 0;
     const void *fn = select_kernel(c.dtype, nt, &smem);
     void *args[] = {&a};
@@ -1117,12 +1148,15 @@ cudaError_t launch_decode(const nvfp4kv_cache &c, const void *q, int batch, int 
     r.chunk_prefix = prefix;
     r.part_acc = part_acc;
     r.part_ml = part_ml;
+    r.casc_ml = shared_pages ? casc_ml : nullptr;
+    r.casc_acc = shared_pages ? casc_acc : nullptr;
+    r.casc_splits = csplits;
     r.gv = c.v_global_scale;
     r.out = static_cast<__nv_bfloat16 *>(out);
     const int64_t rows = (int64_t)batch * num_q_heads;
     // warps per output row from the average number of partials per pair
     const int64_t pairs = (int64_t)batch * c.num_kv_heads;
-    const int64_t avg_parts = (grid + 2 * pairs - 1) / pairs * kWarps;
+    const int64_t avg_parts = (grid + 2 * pairs - 1) / pairs * kWarps + csplits;
     int wpr = avg_parts <= 4 ? 1 : avg_parts <= 8 ? 2 : avg_parts <= 16 ? 4 : 8;
     const int64_t rows_per_cta = kReduceWarps / wpr;
     void *rargs[] = {&r, &wpr};

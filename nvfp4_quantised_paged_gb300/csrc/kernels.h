@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
+#include <vector_types.h>
 
 #include "nvfp4kv.h"
 
@@ -30,7 +31,20 @@ cudaError_t launch_decode(const nvfp4kv_cache &c, const void *q, int batch, int 
                           const int32_t *block_table, int max_pages, const int32_t *seq_lens, float sm_scale,
                           void *out, void *workspace, int grid, unsigned *err, cudaStream_t stream,
                           cudaEvent_t before, cudaEvent_t after, const void *k_new = nullptr,
-                          const void *v_new = nullptr, int64_t new_stride = 0);
+                          const void *v_new = nullptr, int64_t new_stride = 0,
+                          const int32_t *shared_pages = nullptr, int shared_len = 0);
+
+// Number of slices the shared prefix is cut into (each leaves one partial per
+// row), and the extra workspace bytes of a cascade call.
+int cascade_splits(const nvfp4kv_cache &c, int batch, int num_q_heads, int shared_len);
+size_t cascade_extra_bytes(const nvfp4kv_cache &c, int batch, int num_q_heads, int shared_len);
+
+// Partials (m, l, acc) of every sequence's query heads over the shared prefix
+// (shared_len tokens in pages shared_pages[]), `splits` slices of it, one
+// partial per (slice, sequence, kv head, head).
+cudaError_t launch_shared_prefix(const nvfp4kv_cache &c, const void *q, int batch, int num_q_heads,
+                                 const int32_t *shared_pages, int shared_len, int splits, float sm_scale,
+                                 float2 *casc_ml, float *casc_acc, unsigned *err, cudaStream_t stream);
 
 // Attention of each request's chunk over [its BF16 prefix rows || its chunk], causal in the chunk.
 cudaError_t launch_extend(const void *q, const void *k_prefix, const void *v_prefix, const int32_t *cu_prefix,

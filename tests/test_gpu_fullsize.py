@@ -94,10 +94,16 @@ def test_agent_mix_full_size(m):
     torch.cuda.synchronize()
     assert m.check_device_errors() == 0
     lens = w.seq_lens[dec]
+    shared = w.shared_prefix_tokens
+    casc = m.cascade_decode_attention(cache, q[dec].contiguous(), bt[0, :shared // w.page_size].contiguous().cuda(),
+                                      shared, bt.cuda(), lens.contiguous().cuda(), w.sm_scale)
+    torch.cuda.synchronize()
+    assert m.check_device_errors() == 0
     shortest, longest = int(torch.argmin(lens)), int(torch.argmax(lens))
     for b, kv in [(shortest, 1), (longest, 6), (77, 0)]:
         ref = oracle_unit(w, q, b, kv)
         check_attention(out[b, kv * w.group:(kv + 1) * w.group], ref, "agent b=%d kv=%d" % (b, kv))
+        check_attention(casc[b, kv * w.group:(kv + 1) * w.group], ref, "agent cascade b=%d kv=%d" % (b, kv))
 
     # extend requests: dequantise every cached prefix, then append the chunks
     rows = mix.extend_rows()
