@@ -424,7 +424,7 @@ def time_extend(m, device, steps, warmup, peak_tflops):
     res.update({"algorithmic_flops": flops, "extend_tflops": flops / res["extend_us"] / 1e6,
                 "extend_frac_of_bf16_peak": flops / res["extend_us"] / 1e6 / peak_tflops,
                 "bf16_peak_tflops": peak_tflops,
-                "note": "mma.sync BF16 tensor-core kernel; peak = measured cuBLAS BF16 burst"})
+                "note": "tcgen05 (TMEM accumulators) BF16 kernel; peak = measured cuBLAS BF16 burst"})
     del cache
     torch.cuda.empty_cache()
     return res

@@ -7,35 +7,51 @@
 // writes it, in BF16) -- and the current chunk's own K/V.  Chunk token i
 // attends to the whole prefix and to chunk tokens 0..i.
 //
-// GB300 design: a flash-attention forward with BF16 mma.sync (m16n8k16,
-// FP32 accumulation).  One CTA = 4 warps = 64 query rows of one (request,
-// kv head), row = chunk token * G + query head of the group, so the G heads
-// that share a KV head share every K/V tile.  K/V tiles of 64 keys (16 KB
-// each) are double-buffered in shared memory by cp.async (rows past the end
-// zero-filled) in a 16-byte-chunk XOR swizzle that makes the ldmatrix reads
-// conflict-free; S = Q K^T takes K through ldmatrix, P.V takes V through
-// ldmatrix.trans, and the S accumulators become the P operand in registers.
-// Base-2 online softmax with a lazily updated running max (rescale only when
-// a score exceeds it by 2^8).  Prefix tiles come first, then the chunk tiles
-// up to the CTA's last token, masked causally.
+// GB300 design: a flash-attention forward on the 5th-generation tensor cores.
+// One CTA = 4 warps = 128 query rows of one (request, kv head), row = chunk
+// token * G + query head of the group, so the G heads that share a KV head
+// share every K/V tile.  Per 64-key tile:
+//   * K and V (BF16) arrive by cp.async in the canonical 128-byte-swizzle
+//     layout (rows past the end zero-filled), double-buffered;
+//   * one thread issues S = Q K^T as eight tcgen05.mma (M 128, N 64, K 16)
+//     with Q and K read from shared memory by descriptor, accumulating in
+//     TMEM columns 0..63;
+//   * each thread owns one query row = one TMEM lane: it loads its 64 scores
+//     (tcgen05.ld), masks, runs the base-2 online softmax with a lazily updated
+//     running max (the O accumulator in TMEM is rescaled only when a score
+//     exceeds the max by 2^8), rounds P to BF16 and writes its row of the P
+//     tile in the same swizzled layout; the row sum adds the rounded values,
+//     so numerator and denominator see the same weights;
+//   * the issuing thread then runs O += P V as four tcgen05.mma (M 128, N 128,
+//     K 16, V as an MN-major operand) into TMEM columns 64..191.
+// A tcgen05.commit on one mbarrier after each S tells the threads that S and
+// every earlier MMA are done, which also frees the P tile and the K/V stage
+// of the previous tile.  Two CTAs share an SM (112 KB of shared memory and
+// 256 TMEM columns each), so one CTA's softmax overlaps the other's MMAs.
+// Every wait is bounded; a timeout is reported in the device error word.
 #include "common.cuh"
 #include "kernels.h"
+#include "tcgen05.cuh"
 
 namespace nvfp4kv {
 
 namespace {
 
-constexpr int kEWarps = 4;
-constexpr int kEThreads = 32 * kEWarps;
-constexpr int kQRows = 16 * kEWarps;      // query rows per CTA
+constexpr int kEThreads = 128;            // one thread per query row
+constexpr int kQRows = 128;               // query rows per CTA
 constexpr int kKeys = 64;                 // keys per K/V tile
-constexpr int kRowBytes = kHeadDim * 2;   // one BF16 row
-constexpr int kTileBytes = kKeys * kRowBytes;
-constexpr int kStageBytes = 2 * kTileBytes;  // K tile | V tile
-constexpr int kESmem = 2 * kStageBytes;      // double buffer
+constexpr int kQBytes = kQRows * 256;     // Q: 2 column blocks of [128][64] BF16
+constexpr int kKVBlock = kKeys * 128;     // one column block of a K or V tile
+constexpr int kKVTile = 2 * kKVBlock;     // a whole K (or V) tile
+constexpr int kStageBytes = 2 * kKVTile;  // K | V
+constexpr int kPBytes = kQRows * 128;     // P: [128][64] BF16
+constexpr int kOffQ = 0, kOffStage = kQBytes, kOffP = kOffStage + 2 * kStageBytes;
+constexpr int kESmem = kOffP + kPBytes;   // 112 KB
+constexpr uint32_t kTmemCols = 256;       // S: columns 0..63, O: 64..191
+constexpr uint32_t kColO = 64;
 constexpr float kRescale = 8.0f;
 constexpr float kNegInfE = -__builtin_huge_valf();
-constexpr uint32_t kOnesBf16x2 = 0x3f803f80u;
+constexpr uint32_t kWaitLimitE = 1u << 24;
 
 struct ExtendArgs {
     const uint16_t *q;                 // BF16 [total_q][Hq][128]
@@ -48,49 +64,21 @@ struct ExtendArgs {
     unsigned *err;
 };
 
-// Byte offset of 16-byte chunk `chunk` (0..15) of row `row` in a swizzled tile.
-__device__ __forceinline__ uint32_t swz(int row, int chunk) {
-    return (uint32_t)(row * kRowBytes + ((chunk ^ (row & 7)) << 4));
-}
-
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool valid) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0)
                  : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
-
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr));
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async_cta() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// D = A(16x16 bf16, row) * B(16x8 bf16, col) + D, FP32 accumulate.
-__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                               uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-    uint32_t r;
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-    return r;
-}
-
-__global__ void __launch_bounds__(kEThreads, 3) extend_kernel(ExtendArgs a) {
-    extern __shared__ __align__(128) uint8_t smem[];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int g = lane >> 2, c = lane & 3;
+__global__ void __launch_bounds__(kEThreads, 2) extend_kernel(ExtendArgs a) {
+    extern __shared__ __align__(1024) uint8_t smem[];
+    __shared__ __align__(8) uint64_t bar_mma;
+    __shared__ uint32_t tmem_base;
+    const int tid = threadIdx.x, warp = tid >> 5;
     const int r = blockIdx.z, kv = blockIdx.y;
     const int q0 = a.cu_q[r], p0 = a.cu_prefix[r];
     int L = a.cu_q[r + 1] - q0;
@@ -106,164 +94,192 @@ __global__ void __launch_bounds__(kEThreads, 3) extend_kernel(ExtendArgs a) {
     const int rows = L * a.G;
     const int row0 = blockIdx.x * kQRows;
     if (row0 >= rows) return;
-    const int row_end = min(row0 + kQRows, rows);
-    const int t_last = (row_end - 1) / a.G;  // last chunk token of this CTA
+    const int t_last = (min(row0 + kQRows, rows) - 1) / a.G;  // last chunk token of this CTA
     const int nt_pre = (np + kKeys - 1) / kKeys;
     const int nt = nt_pre + t_last / kKeys + 1;
 
-    // this thread's two query rows (g and g + 8 of its warp's 16)
-    const int ra = row0 + 16 * warp + g, rb = ra + 8;
-    const bool va = ra < rows, vb = rb < rows;
-    const int ta = va ? ra / a.G : 0, tb = vb ? rb / a.G : 0;
-
-    // ---- Q fragments (A operand, 8 k-steps over head_dim)
-    uint32_t qf[8][4];
-    {
-        const uint32_t *qa = reinterpret_cast<const uint32_t *>(
-            a.q + ((int64_t)(q0 + ta) * a.Hq + kv * a.G + ra % a.G) * kHeadDim);
-        const uint32_t *qb = reinterpret_cast<const uint32_t *>(
-            a.q + ((int64_t)(q0 + tb) * a.Hq + kv * a.G + rb % a.G) * kHeadDim);
-#pragma unroll
-        for (int ks = 0; ks < 8; ks++) {
-            qf[ks][0] = va ? __ldg(qa + 8 * ks + c) : 0u;
-            qf[ks][1] = vb ? __ldg(qb + 8 * ks + c) : 0u;
-            qf[ks][2] = va ? __ldg(qa + 8 * ks + 4 + c) : 0u;
-            qf[ks][3] = vb ? __ldg(qb + 8 * ks + 4 + c) : 0u;
-        }
-    }
-
     const uint32_t sbase = smem_u32(smem);
-    // cp.async of tile i into stage s: 1024 16-byte chunks of K and of V, 8 + 8 per thread
+    const uint32_t sQ = sbase + kOffQ, sP = sbase + kOffP;
+
+    // ---- Q tile: 128 rows x 16 chunks of 16 bytes
+#pragma unroll 4
+    for (int it = 0; it < 16; it++) {
+        const int idx = tid + it * kEThreads;
+        const int row = idx >> 4, c16 = idx & 15;
+        const int R = row0 + row;
+        const bool ok = R < rows;
+        const int64_t src = ok ? (((int64_t)q0 + R / a.G) * a.Hq + kv * a.G + R % a.G) * kHeadDim + c16 * 8 : 0;
+        cp_async16(sQ + (c16 >> 3) * (kQRows * 128) + sw128_off(row, c16 & 7), a.q + src, ok);
+    }
+    // K/V tile i into stage s: 64 keys x 16 chunks, K and V
     auto issue = [&](int i, int s) {
         const bool pre = i < nt_pre;
         const int base = pre ? i * kKeys : (i - nt_pre) * kKeys;
         const int limit = pre ? np : L;
         const uint16_t *kb = pre ? a.k_pre : a.k_new;
-        const uint16_t *vsrc = pre ? a.v_pre : a.v_new;
-        const int64_t row_origin = pre ? p0 : q0;
+        const uint16_t *vb = pre ? a.v_pre : a.v_new;
+        const int64_t origin = pre ? p0 : q0;
+        const uint32_t st = sbase + kOffStage + s * kStageBytes;
 #pragma unroll
         for (int it = 0; it < 8; it++) {
             const int idx = tid + it * kEThreads;  // 0..1023
-            const int key = idx >> 4, chunk = idx & 15;
+            const int key = idx >> 4, c16 = idx & 15;
             const bool ok = base + key < limit;
-            // rows past the end are zero-filled; their (unread) source is the tensor base
-            const int64_t grow = ok ? ((row_origin + base + key) * a.Hkv + kv) * kHeadDim + chunk * 8 : 0;
-            const uint32_t dst = sbase + s * kStageBytes + swz(key, chunk);
-            cp_async16(dst, kb + grow, ok);
-            cp_async16(dst + kTileBytes, vsrc + grow, ok);
+            const int64_t g = ok ? ((origin + base + key) * a.Hkv + kv) * kHeadDim + c16 * 8 : 0;
+            const uint32_t off = (c16 >> 3) * kKVBlock + sw128_off(key, c16 & 7);
+            cp_async16(st + off, kb + g, ok);
+            cp_async16(st + kKVTile + off, vb + g, ok);
         }
     };
-
-    float o[16][4];
-#pragma unroll
-    for (int i = 0; i < 16; i++) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-    // row sums of the BF16-rounded probabilities, from an all-ones B operand:
-    // ol[0] (row g) and ol[2] (row g + 8), so numerator and denominator see
-    // the same rounded weights
-    float ol[4] = {0.f, 0.f, 0.f, 0.f};
-    float m_a = kNegInfE, m_b = kNegInfE;
-
     issue(0, 0);
     cp_async_commit();
-    for (int i = 0; i < nt; i++) {
-        if (i + 1 < nt) issue(i + 1, (i + 1) & 1);
-        cp_async_commit();
-        cp_async_wait1();
+
+    if (warp == 0) tc_alloc(&tmem_base, kTmemCols);
+    if (tid == 0) {
+        mbar_init(&bar_mma, 1);
+        fence_mbar_init();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base;
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;  // this warp's TMEM lanes
+
+    // this thread's query row
+    const int R = row0 + tid;
+    const bool row_ok = R < rows;
+    const int token = row_ok ? R / a.G : 0;
+
+    constexpr uint32_t idesc_s = idesc_bf16_f32(128, kKeys, false);
+    constexpr uint32_t idesc_o = idesc_bf16_f32(128, kHeadDim, true);
+    float m_run = kNegInfE, l_run = 0.f;
+    uint32_t phase = 0;
+    bool aborted = false;
+
+    for (int i = 0; i < nt && !aborted; i++) {
+        const int s_cur = i & 1;
+        cp_async_wait_all();
+        fence_proxy_async_cta();  // the copies before the tensor core reads them
         __syncthreads();
-        const uint32_t kt = sbase + (i & 1) * kStageBytes, vt = kt + kTileBytes;
+        const uint32_t sK = sbase + kOffStage + s_cur * kStageBytes, sV = sK + kKVTile;
+        if (tid == 0) {
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < 8; kk++) {  // S = Q K^T over head_dim, 16 at a time
+                const uint32_t blk = (uint32_t)(kk >> 2), sub = (uint32_t)(kk & 3) * 32;
+                tc_mma_bf16(tmem, smem_desc_sw128(sQ + blk * (kQRows * 128) + sub, 16, 1024),
+                            smem_desc_sw128(sK + blk * kKVBlock + sub, 16, 1024), idesc_s, kk > 0);
+            }
+            tc_commit(&bar_mma);
+        }
+        // S of this tile (and every earlier MMA) done: the other stage and P are free
+        const bool ok = mbar_wait_bounded(&bar_mma, phase, kWaitLimitE, nullptr);
+        if (__syncthreads_or(!ok)) {  // all threads take the same decision
+            if (tid == 0) flag_error(a.err, kErrTimeout);
+            aborted = true;
+            break;
+        }
+        phase ^= 1u;
+        tc_fence_after();
+        if (i + 1 < nt) issue(i + 1, s_cur ^ 1);
+        cp_async_commit();
+
+        // ---- softmax of this thread's row
+        uint32_t sr[2][32];
+        tc_ld32(tmem + lane_base + 0, sr[0]);
+        tc_ld32(tmem + lane_base + 32, sr[1]);
+        tc_wait_ld();
         const bool pre = i < nt_pre;
         const int base = pre ? i * kKeys : (i - nt_pre) * kKeys;
-
-        // ---- S = Q K^T (16 rows x 64 keys per warp)
-        float s[8][4];
+        const int limit = pre ? np : token + 1;  // keys [0, limit) of this tile's source are visible
+        float x[64];
+        float mx = kNegInfE;
 #pragma unroll
-        for (int n = 0; n < 8; n++) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
-#pragma unroll
-        for (int ks = 0; ks < 8; ks++) {
-#pragma unroll
-            for (int j = 0; j < 4; j++) {
-                const int m = lane >> 3;
-                const int key = 16 * j + (m >> 1) * 8 + (lane & 7);
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4(kt + swz(key, 2 * ks + (m & 1)), b0, b1, b2, b3);
-                mma_bf16_16816(s[2 * j], qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3], b0, b1);
-                mma_bf16_16816(s[2 * j + 1], qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3], b2, b3);
-            }
+        for (int j = 0; j < 64; j++) {
+            x[j] = base + j < limit ? __uint_as_float(sr[j >> 5][j & 31]) * a.score_log2 : kNegInfE;
+            mx = fmaxf(mx, x[j]);
         }
-
-        // ---- mask, online softmax (base 2)
-        float mx_a = kNegInfE, mx_b = kNegInfE;
-#pragma unroll
-        for (int n = 0; n < 8; n++) {
-#pragma unroll
-            for (int e = 0; e < 2; e++) {
-                const int key = base + 8 * n + 2 * c + e;
-                const bool oka = pre ? key < np : key <= ta;
-                const bool okb = pre ? key < np : key <= tb;
-                s[n][e] = oka ? s[n][e] * a.score_log2 : kNegInfE;
-                s[n][2 + e] = okb ? s[n][2 + e] * a.score_log2 : kNegInfE;
-                mx_a = fmaxf(mx_a, s[n][e]);
-                mx_b = fmaxf(mx_b, s[n][2 + e]);
-            }
-        }
-        mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 1));
-        mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 2));
-        mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 1));
-        mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 2));
-        const bool need = mx_a > m_a + kRescale || mx_b > m_b + kRescale;
+        const bool need = mx > m_run + kRescale;
         if (__any_sync(0xffffffffu, need)) {
-            const float na = fmaxf(m_a, mx_a), nb = fmaxf(m_b, mx_b);
-            const float fa = na == kNegInfE ? 1.f : ex2(m_a - na), fb = nb == kNegInfE ? 1.f : ex2(m_b - nb);
-            m_a = na;
-            m_b = nb;
-            ol[0] *= fa;
-            ol[1] *= fa;
-            ol[2] *= fb;
-            ol[3] *= fb;
+            const float m_new = need ? fmaxf(m_run, mx) : m_run;
+            const float alpha = need ? (m_run == kNegInfE ? 0.f : ex2(m_run - m_new)) : 1.f;
+            if (i > 0) {  // O holds earlier tiles: rescale this warp's rows in TMEM
 #pragma unroll
-            for (int d = 0; d < 16; d++) {
-                o[d][0] *= fa;
-                o[d][1] *= fa;
-                o[d][2] *= fb;
-                o[d][3] *= fb;
+                for (int cblk = 0; cblk < 4; cblk++) {
+                    uint32_t ov[32];
+                    tc_ld32(tmem + lane_base + kColO + 32 * cblk, ov);
+                    tc_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 32; j++) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * alpha);
+                    tc_st32(tmem + lane_base + kColO + 32 * cblk, ov);
+                }
+                tc_wait_st();
+            }
+            l_run *= alpha;
+            m_run = m_new;
+        }
+        // P row (BF16, the rounded values also summed into l) into the swizzled P tile
+#pragma unroll
+        for (int c = 0; c < 8; c++) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; e++) {
+                const __nv_bfloat162 pr = __floats2bfloat162_rn(ex2(x[8 * c + 2 * e] - m_run),
+                                                                 ex2(x[8 * c + 2 * e + 1] - m_run));
+                const float2 back = __bfloat1622float2(pr);
+                l_run += back.x + back.y;
+                w[e] = *reinterpret_cast<const uint32_t *>(&pr);
+            }
+            *reinterpret_cast<uint4 *>(smem + kOffP + sw128_off(tid, c)) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        fence_proxy_async_cta();  // P (and the O rescale) before the tensor core reads them
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < 4; kk++)  // O += P V over this tile's 64 keys
+                tc_mma_bf16(tmem + kColO, smem_desc_sw128(sP + kk * 32, 16, 1024),
+                            smem_desc_sw128(sV + kk * 16 * 128, kKVBlock, 1024), idesc_o, (i > 0 || kk > 0) ? 1u : 0u);
+        }
+    }
+    if (!aborted) {
+        if (tid == 0) tc_commit(&bar_mma);
+        const bool ok = mbar_wait_bounded(&bar_mma, phase, kWaitLimitE, nullptr);
+        if (__syncthreads_or(!ok)) {
+            if (tid == 0) flag_error(a.err, kErrTimeout);
+            aborted = true;
+        }
+        tc_fence_after();
+    }
+    if (!aborted) {
+        // ---- O / l -> BF16 row of the output
+        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+        uint4 *dst = reinterpret_cast<uint4 *>(a.out + (((int64_t)q0 + token) * a.Hq + kv * a.G + R % a.G) * kHeadDim);
+#pragma unroll
+        for (int cblk = 0; cblk < 4; cblk++) {
+            uint32_t ov[32];
+            tc_ld32(tmem + lane_base + kColO + 32 * cblk, ov);
+            tc_wait_ld();
+            if (row_ok) {
+#pragma unroll
+                for (int q4 = 0; q4 < 4; q4++) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int e = 0; e < 4; e++) {
+                        const __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(ov[8 * q4 + 2 * e]) * inv,
+                                                                        __uint_as_float(ov[8 * q4 + 2 * e + 1]) * inv);
+                        w[e] = *reinterpret_cast<const uint32_t *>(&h);
+                    }
+                    dst[4 * cblk + q4] = make_uint4(w[0], w[1], w[2], w[3]);
+                }
             }
         }
-        uint32_t pa[4][4];  // P as the A operand of 4 k-steps of 16 keys
-#pragma unroll
-        for (int n = 0; n < 8; n++) {
-            const float p0 = ex2(s[n][0] - m_a), p1 = ex2(s[n][1] - m_a);
-            const float p2 = ex2(s[n][2] - m_b), p3 = ex2(s[n][3] - m_b);
-            pa[n >> 1][(n & 1) * 2 + 0] = pack_bf16(p0, p1);
-            pa[n >> 1][(n & 1) * 2 + 1] = pack_bf16(p2, p3);
-        }
-
-        // ---- O += P V (16 rows x 128 dims per warp)
-#pragma unroll
-        for (int kk = 0; kk < 4; kk++) {
-#pragma unroll
-            for (int nd = 0; nd < 16; nd += 2) {
-                const int m = lane >> 3;
-                const int key = 16 * kk + (m & 1) * 8 + (lane & 7);
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4_t(vt + swz(key, nd + (m >> 1)), b0, b1, b2, b3);
-                mma_bf16_16816(o[nd], pa[kk][0], pa[kk][1], pa[kk][2], pa[kk][3], b0, b1);
-                mma_bf16_16816(o[nd + 1], pa[kk][0], pa[kk][1], pa[kk][2], pa[kk][3], b2, b3);
-            }
-            mma_bf16_16816(ol, pa[kk][0], pa[kk][1], pa[kk][2], pa[kk][3], kOnesBf16x2, kOnesBf16x2);
-        }
-        __syncthreads();  // the stage is refilled by the next iteration's copies
     }
-
-    // ---- normalise and store
-    const float l_a = ol[0], l_b = ol[2];
-    const float ia = l_a > 0.f ? 1.f / l_a : 0.f, ib = l_b > 0.f ? 1.f / l_b : 0.f;
-    uint32_t *oa = reinterpret_cast<uint32_t *>(a.out + ((int64_t)(q0 + ta) * a.Hq + kv * a.G + ra % a.G) * kHeadDim);
-    uint32_t *ob = reinterpret_cast<uint32_t *>(a.out + ((int64_t)(q0 + tb) * a.Hq + kv * a.G + rb % a.G) * kHeadDim);
-#pragma unroll
-    for (int d = 0; d < 16; d++) {
-        if (va) oa[4 * d + c] = pack_bf16(o[d][0] * ia, o[d][1] * ia);
-        if (vb) ob[4 * d + c] = pack_bf16(o[d][2] * ib, o[d][3] * ib);
-    }
+    cp_async_wait_all();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tc_dealloc(tmem, kTmemCols);
 }
 
 }  // namespace
