@@ -17,17 +17,19 @@
 //     with Q and K read from shared memory by descriptor, accumulating in
 //     TMEM columns 0..63;
 //   * each thread owns one query row = one TMEM lane: it loads its 64 scores
-//     (tcgen05.ld), masks, runs the base-2 online softmax with a lazily updated
-//     running max (the O accumulator in TMEM is rescaled only when a score
-//     exceeds the max by 2^8), rounds P to BF16 and writes its row of the P
-//     tile in the same swizzled layout; the row sum adds the rounded values,
-//     so numerator and denominator see the same weights;
-//   * the issuing thread then runs O += P V as four tcgen05.mma (M 128, N 128,
-//     K 16, V as an MN-major operand) into TMEM columns 64..191.
+//     (tcgen05.ld), masks them on edge tiles only, runs the base-2 online
+//     softmax with a lazily updated running max (O and the row sums in TMEM
+//     are rescaled only when a score exceeds the max by 2^8), forms
+//     P = 2^(s * scale - m) with one FFMA per score, rounds it to BF16 and
+//     stores its row of P into TMEM (tcgen05.st);
+//   * the issuing thread then runs O += P V as four tcgen05.mma with P read
+//     from TMEM (M 128, N 128, K 16, V as an MN-major operand) into TMEM
+//     columns 96..223, and the row sums as four more with an all-ones B
+//     operand, so numerator and denominator see the same rounded P.
 // A tcgen05.commit on one mbarrier after each S tells the threads that S and
-// every earlier MMA are done, which also frees the P tile and the K/V stage
-// of the previous tile.  Two CTAs share an SM (112 KB of shared memory and
-// 256 TMEM columns each), so one CTA's softmax overlaps the other's MMAs.
+// every earlier MMA are done, which also frees P and the K/V stage of the
+// previous tile.  Two CTAs share an SM (98 KB of shared memory and 256 TMEM
+// columns each), so one CTA's softmax overlaps the other's MMAs.
 // Every wait is bounded; a timeout is reported in the device error word.
 #include "common.cuh"
 #include "kernels.h"
@@ -44,11 +46,13 @@ constexpr int kQBytes = kQRows * 256;     // Q: 2 column blocks of [128][64] BF1
 constexpr int kKVBlock = kKeys * 128;     // one column block of a K or V tile
 constexpr int kKVTile = 2 * kKVBlock;     // a whole K (or V) tile
 constexpr int kStageBytes = 2 * kKVTile;  // K | V
-constexpr int kPBytes = kQRows * 128;     // P: [128][64] BF16
-constexpr int kOffQ = 0, kOffStage = kQBytes, kOffP = kOffStage + 2 * kStageBytes;
-constexpr int kESmem = kOffP + kPBytes;   // 112 KB
-constexpr uint32_t kTmemCols = 256;       // S: columns 0..63, O: 64..191
-constexpr uint32_t kColO = 64;
+constexpr int kOnesBytes = 16 * 128;     // all-ones B operand [16][64] for the row sums
+constexpr int kOffQ = 0, kOffStage = kQBytes, kOffOnes = kOffStage + 2 * kStageBytes;
+constexpr int kOffBar = kOffOnes + kOnesBytes;
+constexpr int kESmem = kOffBar + 16;      // 98 KB
+// TMEM columns: S 0..63 (FP32), P 64..95 (BF16 pairs), O 96..223, row sums 224..239
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kColP = 64, kColO = 96, kColL = 224;
 constexpr float kRescale = 8.0f;
 constexpr float kNegInfE = -__builtin_huge_valf();
 constexpr uint32_t kWaitLimitE = 1u << 24;
@@ -76,8 +80,8 @@ __device__ __forceinline__ void fence_proxy_async_cta() {
 
 __global__ void __launch_bounds__(kEThreads, 2) extend_kernel(ExtendArgs a) {
     extern __shared__ __align__(1024) uint8_t smem[];
-    __shared__ __align__(8) uint64_t bar_mma;
-    __shared__ uint32_t tmem_base;
+    uint64_t &bar_mma = *reinterpret_cast<uint64_t *>(smem + kOffBar);
+    uint32_t &tmem_base = *reinterpret_cast<uint32_t *>(smem + kOffBar + 8);
     const int tid = threadIdx.x, warp = tid >> 5;
     const int r = blockIdx.z, kv = blockIdx.y;
     const int q0 = a.cu_q[r], p0 = a.cu_prefix[r];
@@ -99,7 +103,7 @@ __global__ void __launch_bounds__(kEThreads, 2) extend_kernel(ExtendArgs a) {
     const int nt = nt_pre + t_last / kKeys + 1;
 
     const uint32_t sbase = smem_u32(smem);
-    const uint32_t sQ = sbase + kOffQ, sP = sbase + kOffP;
+    const uint32_t sQ = sbase + kOffQ;
 
     // ---- Q tile: 128 rows x 16 chunks of 16 bytes
 #pragma unroll 4
@@ -133,6 +137,10 @@ __global__ void __launch_bounds__(kEThreads, 2) extend_kernel(ExtendArgs a) {
     };
     issue(0, 0);
     cp_async_commit();
+    for (int idx = tid; idx < kOnesBytes / 16; idx += kEThreads) {  // BF16 1.0 everywhere
+        const uint32_t one2 = 0x3f803f80u;
+        *reinterpret_cast<uint4 *>(smem + kOffOnes + idx * 16) = make_uint4(one2, one2, one2, one2);
+    }
 
     if (warp == 0) tc_alloc(&tmem_base, kTmemCols);
     if (tid == 0) {
@@ -152,7 +160,9 @@ __global__ void __launch_bounds__(kEThreads, 2) extend_kernel(ExtendArgs a) {
 
     constexpr uint32_t idesc_s = idesc_bf16_f32(128, kKeys, false);
     constexpr uint32_t idesc_o = idesc_bf16_f32(128, kHeadDim, true);
-    float m_run = kNegInfE, l_run = 0.f;
+    constexpr uint32_t idesc_l = idesc_bf16_f32(128, 16, false);
+    const uint32_t sOnes = sbase + kOffOnes;
+    float m_run = kNegInfE;
     uint32_t phase = 0;
     bool aborted = false;
 
@@ -184,63 +194,70 @@ __global__ void __launch_bounds__(kEThreads, 2) extend_kernel(ExtendArgs a) {
         if (i + 1 < nt) issue(i + 1, s_cur ^ 1);
         cp_async_commit();
 
-        // ---- softmax of this thread's row
+        // ---- softmax of this thread's row (base 2; masked scores are -inf)
         uint32_t sr[2][32];
         tc_ld32(tmem + lane_base + 0, sr[0]);
         tc_ld32(tmem + lane_base + 32, sr[1]);
         tc_wait_ld();
-        const bool pre = i < nt_pre;
-        const int base = pre ? i * kKeys : (i - nt_pre) * kKeys;
-        const int limit = pre ? np : token + 1;  // keys [0, limit) of this tile's source are visible
-        float x[64];
-        float mx = kNegInfE;
+        float sc[64];
 #pragma unroll
-        for (int j = 0; j < 64; j++) {
-            x[j] = base + j < limit ? __uint_as_float(sr[j >> 5][j & 31]) * a.score_log2 : kNegInfE;
-            mx = fmaxf(mx, x[j]);
+        for (int j = 0; j < 64; j++) sc[j] = __uint_as_float(sr[j >> 5][j & 31]);
+        {
+            const bool pre = i < nt_pre;
+            const int base = pre ? i * kKeys : (i - nt_pre) * kKeys;
+            const int visible = (pre ? np : token + 1) - base;  // keys [0, visible) of the tile are seen
+            if (__any_sync(0xffffffffu, visible < kKeys)) {     // an edge tile: mask
+#pragma unroll
+                for (int j = 0; j < 64; j++)
+                    if (j >= visible) sc[j] = kNegInfE;
+            }
         }
+        float smax = sc[0];
+#pragma unroll
+        for (int j = 1; j < 64; j++) smax = fmaxf(smax, sc[j]);
+        const float mx = smax * a.score_log2;  // the scale is positive
         const bool need = mx > m_run + kRescale;
         if (__any_sync(0xffffffffu, need)) {
             const float m_new = need ? fmaxf(m_run, mx) : m_run;
             const float alpha = need ? (m_run == kNegInfE ? 0.f : ex2(m_run - m_new)) : 1.f;
-            if (i > 0) {  // O holds earlier tiles: rescale this warp's rows in TMEM
+            if (i > 0) {  // O and the row sums hold earlier tiles: rescale this warp's rows in TMEM
 #pragma unroll
-                for (int cblk = 0; cblk < 4; cblk++) {
+                for (int cblk = 0; cblk < 5; cblk++) {  // O (4 x 32 columns), then the sums
                     uint32_t ov[32];
-                    tc_ld32(tmem + lane_base + kColO + 32 * cblk, ov);
+                    const uint32_t col = cblk < 4 ? kColO + 32 * cblk : kColL;
+                    tc_ld32(tmem + lane_base + col, ov);
                     tc_wait_ld();
 #pragma unroll
                     for (int j = 0; j < 32; j++) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * alpha);
-                    tc_st32(tmem + lane_base + kColO + 32 * cblk, ov);
+                    tc_st32(tmem + lane_base + col, ov);
                 }
                 tc_wait_st();
             }
-            l_run *= alpha;
             m_run = m_new;
         }
-        // P row (BF16, the rounded values also summed into l) into the swizzled P tile
+        // P row = 2^(s * scale - m), rounded to BF16, into this lane's P columns of TMEM
+        const float neg_m = -m_run;
+        uint32_t pw[32];
 #pragma unroll
-        for (int c = 0; c < 8; c++) {
-            uint32_t w[4];
-#pragma unroll
-            for (int e = 0; e < 4; e++) {
-                const __nv_bfloat162 pr = __floats2bfloat162_rn(ex2(x[8 * c + 2 * e] - m_run),
-                                                                 ex2(x[8 * c + 2 * e + 1] - m_run));
-                const float2 back = __bfloat1622float2(pr);
-                l_run += back.x + back.y;
-                w[e] = *reinterpret_cast<const uint32_t *>(&pr);
-            }
-            *reinterpret_cast<uint4 *>(smem + kOffP + sw128_off(tid, c)) = make_uint4(w[0], w[1], w[2], w[3]);
+        for (int c = 0; c < 32; c++) {
+            const __nv_bfloat162 pr =
+                __floats2bfloat162_rn(ex2(fmaf(sc[2 * c], a.score_log2, neg_m)), ex2(fmaf(sc[2 * c + 1], a.score_log2, neg_m)));
+            pw[c] = *reinterpret_cast<const uint32_t *>(&pr);
         }
-        fence_proxy_async_cta();  // P (and the O rescale) before the tensor core reads them
+        tc_st32(tmem + lane_base + kColP, pw);
+        tc_wait_st();
         tc_fence_before();
         __syncthreads();
         if (tid == 0) {
             tc_fence_after();
 #pragma unroll
-            for (int kk = 0; kk < 4; kk++)  // O += P V over this tile's 64 keys
-                tc_mma_bf16(tmem + kColO, smem_desc_sw128(sP + kk * 32, 16, 1024),
-                            smem_desc_sw128(sV + kk * 16 * 128, kKVBlock, 1024), idesc_o, (i > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < 4; kk++) {  // O += P V over this tile's 64 keys; sums += P 1
+                const uint32_t pa = tmem + kColP + kk * 8;  // P from TMEM: 8 columns = 16 keys
+                const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
+                tc_mma_bf16_tmem_a(tmem + kColO, pa, smem_desc_sw128(sV + kk * 16 * 128, kKVBlock, 1024), idesc_o,
+                                   acc);
+                tc_mma_bf16_tmem_a(tmem + kColL, pa, smem_desc_sw128(sOnes + kk * 32, 16, 1024), idesc_l, acc);
+            }
         }
     }
     if (!aborted) {
@@ -254,6 +271,10 @@ __global__ void __launch_bounds__(kEThreads, 2) extend_kernel(ExtendArgs a) {
     }
     if (!aborted) {
         // ---- O / l -> BF16 row of the output
+        uint32_t lv[32];
+        tc_ld32(tmem + lane_base + kColL, lv);
+        tc_wait_ld();
+        const float l_run = __uint_as_float(lv[0]);
         const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
         uint4 *dst = reinterpret_cast<uint4 *>(a.out + (((int64_t)q0 + token) * a.Hq + kv * a.G + R % a.G) * kHeadDim);
 #pragma unroll
