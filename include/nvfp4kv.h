@@ -303,15 +303,20 @@ NVFP4KV_API int nvfp4_prefix_dequant(const nvfp4kv_cache *cache, const int32_t *
  *                   (the nvfp4_prefix_dequant workspace layout).
  *   k_chunk, v_chunk    device BF16 [total_q][num_kv_heads][128], rows as q.
  *   cu_prefix_lens, cu_q_lens  device int32 [num_reqs + 1], non-decreasing.
+ *   total_prefix_tokens, total_q_tokens  host: rows of k_prefix / v_prefix
+ *                   and of q, k_chunk, v_chunk (the kernel's copies stay
+ *                   inside them: rows past a request are read but masked).
  *   max_q_len       host bound on every chunk length (grid size); a longer
  *                   chunk is cut to it and flagged in the device error word.
  *   out             device BF16 [total_q][num_q_heads][128].
  * All data pointers 16-byte aligned.  Computes in BF16 x BF16 -> FP32 on the
  * tensor cores (probabilities rounded to BF16).  num_reqs == 0 is a no-op.
+ * Needs the driver's tensor-map encoder (NVFP4KV_ECUDA if it is missing).
  */
 NVFP4KV_API int nvfp4_extend_attention(const void *q, const void *k_prefix, const void *v_prefix,
-                                       const int32_t *cu_prefix_lens, const void *k_chunk, const void *v_chunk,
-                                       const int32_t *cu_q_lens, int num_reqs, int max_q_len, int num_q_heads,
+                                       const int32_t *cu_prefix_lens, int64_t total_prefix_tokens,
+                                       const void *k_chunk, const void *v_chunk, const int32_t *cu_q_lens,
+                                       int64_t total_q_tokens, int num_reqs, int max_q_len, int num_q_heads,
                                        int num_kv_heads, float sm_scale, void *out, cudaStream_t stream);
 
 /* Synchronises `stream`, then reads and clears the current device's error

@@ -66,7 +66,7 @@ def _load_library():
         "nvfp4kv_check_device_errors": (i32, [P]),
         "nvfp4kv_selftest_bounded_wait": (i32, [i32, ctypes.c_uint, P, P]),
         "nvfp4kv_calibrate_global_scales": (i32, [P, P, i64, i32, i64, P, P]),
-        "nvfp4_extend_attention": (i32, [P, P, P, P, P, P, P, i32, i32, i32, i32, f32, P, P]),
+        "nvfp4_extend_attention": (i32, [P, P, P, P, i64, P, P, P, i64, i32, i32, i32, i32, f32, P, P]),
         "nvfp4_paged_decode_attention_append": (i32, [D, P, P, i64, P, i32, i32, P, i32, P, f32, P, P, sz, i32, P]),
         "nvfp4kv_cascade_workspace_bytes": (sz, [D, i32, i32, i32, i32]),
         "nvfp4_cascade_decode_attention": (i32, [D, P, i32, i32, P, i32, P, i32, P, f32, P, P, sz, i32, P]),
@@ -423,9 +423,9 @@ def extend_attention(q: torch.Tensor, k_prefix: torch.Tensor, v_prefix: torch.Te
     # an empty prefix still needs a valid aligned pointer
     kp = k_prefix if k_prefix.numel() else torch.zeros((1, hkv, HEAD_DIM), dtype=torch.bfloat16, device=q.device)
     vp = v_prefix if v_prefix.numel() else kp
-    rc = _lib.nvfp4_extend_attention(_ptr(q), _ptr(kp), _ptr(vp), _ptr(cu_prefix_lens), _ptr(k_chunk), _ptr(v_chunk),
-                                     _ptr(cu_q_lens), R, int(max_q_len), hq, hkv, float(sm_scale), _ptr(out),
-                                     _stream(stream))
+    rc = _lib.nvfp4_extend_attention(_ptr(q), _ptr(kp), _ptr(vp), _ptr(cu_prefix_lens), int(kp.shape[0]),
+                                     _ptr(k_chunk), _ptr(v_chunk), _ptr(cu_q_lens), int(q.shape[0]), R,
+                                     int(max_q_len), hq, hkv, float(sm_scale), _ptr(out), _stream(stream))
     _check(rc, "nvfp4_extend_attention")
     return out
 

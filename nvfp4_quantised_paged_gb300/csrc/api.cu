@@ -172,11 +172,14 @@ int nvfp4_kv_quantize_append(const nvfp4kv_cache *cache, const void *k, const vo
 }
 
 int nvfp4_extend_attention(const void *q, const void *k_prefix, const void *v_prefix, const int32_t *cu_prefix_lens,
-                           const void *k_chunk, const void *v_chunk, const int32_t *cu_q_lens, int num_reqs,
-                           int max_q_len, int num_q_heads, int num_kv_heads, float sm_scale, void *out,
-                           cudaStream_t stream) {
-    if (num_reqs < 0 || max_q_len < 0 || num_kv_heads < 1 || num_q_heads < 1 || num_q_heads % num_kv_heads)
+                           int64_t total_prefix_tokens, const void *k_chunk, const void *v_chunk,
+                           const int32_t *cu_q_lens, int64_t total_q_tokens, int num_reqs, int max_q_len,
+                           int num_q_heads, int num_kv_heads, float sm_scale, void *out, cudaStream_t stream) {
+    if (num_reqs < 0 || max_q_len < 0 || num_kv_heads < 1 || num_q_heads < 1 || num_q_heads % num_kv_heads ||
+        total_prefix_tokens < 0 || total_q_tokens < 0)
         return NVFP4KV_EINVAL;
+    if (total_prefix_tokens >= ((int64_t)1 << 31) || total_q_tokens >= ((int64_t)1 << 31))
+        return NVFP4KV_EUNSUPPORTED;
     if (!isfinite(sm_scale)) return NVFP4KV_EINVAL;
     if (num_reqs == 0 || max_q_len == 0) return NVFP4KV_OK;
     if (!q || !k_chunk || !v_chunk || !out || !cu_prefix_lens || !cu_q_lens || !k_prefix || !v_prefix)
@@ -190,8 +193,9 @@ int nvfp4_extend_attention(const void *q, const void *k_prefix, const void *v_pr
     cudaError_t e;
     unsigned *err = error_word(&e);
     if (!err) return NVFP4KV_ECUDA;
-    return from_cuda(launch_extend(q, k_prefix, v_prefix, cu_prefix_lens, k_chunk, v_chunk, cu_q_lens, num_reqs,
-                                   max_q_len, num_q_heads, num_kv_heads, sm_scale, out, err, stream));
+    return from_cuda(launch_extend(q, k_prefix, v_prefix, cu_prefix_lens, total_prefix_tokens, k_chunk, v_chunk,
+                                   cu_q_lens, total_q_tokens, num_reqs, max_q_len, num_q_heads, num_kv_heads, sm_scale,
+                                   out, err, stream));
 }
 
 int nvfp4kv_calibrate_global_scales(const void *k, const void *v, int64_t num_tokens, int num_kv_heads,

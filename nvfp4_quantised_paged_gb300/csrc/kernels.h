@@ -48,9 +48,9 @@ cudaError_t launch_shared_prefix(const nvfp4kv_cache &c, const void *q, int batc
 
 // Attention of each request's chunk over [its BF16 prefix rows || its chunk], causal in the chunk.
 cudaError_t launch_extend(const void *q, const void *k_prefix, const void *v_prefix, const int32_t *cu_prefix,
-                          const void *k_chunk, const void *v_chunk, const int32_t *cu_q, int num_reqs, int max_q_len,
-                          int num_q_heads, int num_kv_heads, float sm_scale, void *out, unsigned *err,
-                          cudaStream_t stream);
+                          int64_t total_prefix, const void *k_chunk, const void *v_chunk, const int32_t *cu_q,
+                          int64_t total_q, int num_reqs, int max_q_len, int num_q_heads, int num_kv_heads,
+                          float sm_scale, void *out, unsigned *err, cudaStream_t stream);
 
 // g_K, g_V = amax / (6 * 448) of K and V (1.0 for an all-zero tensor) into scales[0..1].
 cudaError_t launch_calibrate(const void *k, const void *v, int64_t num_tokens, int num_kv_heads, int64_t token_stride,
