@@ -408,18 +408,24 @@ def time_extend(m, device, steps, warmup, peak_tflops):
 
     res = {"workload": "agent-mix extends: 8 x 512-token chunks over prefixes of %s tokens, q32kv8"
            % "/".join(str(int(x)) for x in pl)}
-    for key, wd in (("extend_us", False), ("path2_us", True)):
+    def dequant_only():
+        m.prefix_dequant(cache, bt, pl_d, cu_p_d, total, k_ws=kw, v_ws=vw)
+
+    for key, fn in (("extend_us", lambda: run(False)), ("path2_us", lambda: run(True)), ("dequant_us", dequant_only)):
         for _ in range(warmup):
-            run(wd)
+            fn()
         s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
         s.record()
         for _ in range(steps):
-            run(wd)
+            fn()
         e.record()
         torch.cuda.synchronize()
         res[key] = s.elapsed_time(e) / steps * 1e3
     assert m.check_device_errors() == 0
+    dq_bytes = total * w.num_kv_heads * (144 + 2 * 2 * 128)  # NVFP4 in, BF16 K and V out
+    res["dequant_gb_per_s"] = dq_bytes / res["dequant_us"] / 1e3
+    res["dequant_algorithmic_bytes"] = dq_bytes
     flops = extend_flops([int(x) for x in pl], L, w.num_q_heads // w.num_kv_heads, w.num_kv_heads)
     res.update({"algorithmic_flops": flops, "extend_tflops": flops / res["extend_us"] / 1e6,
                 "extend_frac_of_bf16_peak": flops / res["extend_us"] / 1e6 / peak_tflops,

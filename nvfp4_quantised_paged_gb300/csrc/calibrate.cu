@@ -39,9 +39,39 @@ __global__ void __launch_bounds__(256) amax_kernel(const uint4 *k, const uint4 *
                                                    int64_t stride16, int row16, unsigned *out) {
     pdl_launch_dependents();
     const int64_t n = num_tokens * row16;
+    // flat index i = t * row16 + j over the 16-byte vectors; (t, j) advance by
+    // a fixed step without divisions, four vectors of K and of V in flight
+    const int64_t step = (int64_t)gridDim.x * blockDim.x;
+    const int64_t step_t = step / row16;
+    const int step_j = (int)(step - step_t * row16);
+    int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    int64_t t = i / row16;
+    int j = (int)(i - t * row16);
     uint32_t mk = 0, mv = 0;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t t = i / row16, j = i - t * row16;
+    auto advance = [&]() {
+        i += step;
+        t += step_t;
+        j += step_j;
+        if (j >= row16) {
+            j -= row16;
+            t++;
+        }
+    };
+    while (i + 3 * step < n) {
+        uint4 xk[4], xv[4];
+#pragma unroll
+        for (int u = 0; u < 4; u++) {
+            xk[u] = __ldg(k + t * stride16 + j);
+            xv[u] = __ldg(v + t * stride16 + j);
+            advance();
+        }
+#pragma unroll
+        for (int u = 0; u < 4; u++) {
+            mk = max(mk, amax8(xk[u]));
+            mv = max(mv, amax8(xv[u]));
+        }
+    }
+    for (; i < n; advance()) {
         mk = max(mk, amax8(__ldg(k + t * stride16 + j)));
         mv = max(mv, amax8(__ldg(v + t * stride16 + j)));
     }

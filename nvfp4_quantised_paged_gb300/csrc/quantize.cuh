@@ -70,9 +70,8 @@ __device__ __forceinline__ void quantize_block16(const uint4 &a, const uint4 &b,
 // (K codes | K scales | V codes | V scales [8][16]); FP8 slabs are groups of
 // 4096 bytes (K codes [16][128] | V codes [16][128]).
 template <bool kUnitScale>
-__device__ __forceinline__ void store_block(uint8_t *slab_base, int dtype, int r, int which, int blk,
-                                            const uint4 *src, float g) {
-    const uint4 x0 = __ldg(src), x1 = __ldg(src + 1);
+__device__ __forceinline__ void store_block_values(uint8_t *slab_base, int dtype, int r, int which, int blk,
+                                                   const uint4 &x0, const uint4 &x1, float g) {
     if (dtype == NVFP4KV_DTYPE_NVFP4) {
         uint2 codes;
         uint32_t sbyte;
@@ -98,6 +97,14 @@ __device__ __forceinline__ void store_block(uint8_t *slab_base, int dtype, int r
         uint8_t *dst = slab_base + (r >> 4) * 4096 + (which ? 2048 : 0) + (r & 15) * 128 + blk * 16;
         *reinterpret_cast<uint4 *>(dst) = make_uint4(out[0], out[1], out[2], out[3]);
     }
+}
+
+// The same, loading the 16 values from src[0..1] first.
+template <bool kUnitScale>
+__device__ __forceinline__ void store_block(uint8_t *slab_base, int dtype, int r, int which, int blk,
+                                            const uint4 *src, float g) {
+    const uint4 x0 = __ldg(src), x1 = __ldg(src + 1);
+    store_block_values<kUnitScale>(slab_base, dtype, r, which, blk, x0, x1, g);
 }
 
 }  // namespace nvfp4kv

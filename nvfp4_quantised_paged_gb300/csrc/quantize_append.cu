@@ -62,16 +62,18 @@ __global__ void __launch_bounds__(256) append_kernel(AppendArgs a) {
     const uint32_t t32 = th / (uint32_t)a.Hkv;
     const int h = (int)(th - t32 * (uint32_t)a.Hkv);
     const int64_t t = t32;
+    // the values and the slot are loaded together (both always in bounds)
+    const uint4 *src = (which ? a.v : a.k) + t * a.stride16 + h * (kHeadDim / 8) + blk * 2;
+    const uint4 x0 = __ldg(src), x1 = __ldg(src + 1);
     const int64_t slot = __ldg(a.slots + t);
     if (slot < 0) return;
     if (slot >= a.num_slots) {
         if (blk == 0 && which == 0 && h == 0) flag_error(a.err, kErrSlot);
         return;
     }
-    const uint4 *src = (which ? a.v : a.k) + t * a.stride16 + h * (kHeadDim / 8) + blk * 2;
     const int64_t page = slot >> a.log2P;
-    store_block<kUnitScale>(a.pool + (page * a.Hkv + h) * a.slab, a.dtype, (int)(slot & (a.P - 1)), which, blk, src,
-                            which ? a.gv : a.gk);
+    store_block_values<kUnitScale>(a.pool + (page * a.Hkv + h) * a.slab, a.dtype, (int)(slot & (a.P - 1)), which,
+                                   blk, x0, x1, which ? a.gv : a.gk);
 }
 
 }  // namespace
