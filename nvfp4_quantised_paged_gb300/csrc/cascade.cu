@@ -12,33 +12,46 @@
 // the decode reduction (log-sum-exp), so the result is the decode attention
 // of each whole sequence.
 //
-// One CTA = 4 warps = 64 query rows (row = sequence * G + head) of one kv head
-// and one contiguous slice of the shared prefix.  Each 64-token stage is
-// fetched raw (4 NVFP4 groups, cp.async) into a double buffer, dequantised by
-// all threads into FP16 K and V tiles (e2m1 x e4m3 products are exact FP16
-// values) in a 16-byte-chunk XOR swizzle, and consumed by FP16 mma.sync
-// (S = Q K^T through ldmatrix, O += P V through ldmatrix.trans), with the same
-// per-head power-of-two pre-scale of Q and base-2 lazy-rescale softmax as the
-// decode kernel.
+// One CTA = 4 warps = 128 query rows (row = sequence * G + head, one TMEM lane
+// each) of one kv head and one contiguous slice of the shared prefix.  Per
+// 64-token stage: thread 0 fetches the four raw NVFP4 groups with 1-D bulk
+// copies into a double buffer; all threads dequantise them (e2m1 x e4m3 is an
+// exact FP16 value) into FP16 K and V tiles in the tensor core's 128-byte
+// swizzle layout; thread 0 issues S = Q K^T as tcgen05.mma (FP16 inputs, FP32
+// accumulator in TMEM; Q pre-scaled per row by a power of two, exact, undone
+// in the score factor); each thread runs the base-2 lazy-rescale softmax of
+// its row from tcgen05.ld and stores P (FP16) into TMEM; thread 0 runs
+// O += P V and the row sums (all-ones operand) with P read from TMEM.
+// Two CTAs share an SM.  Every wait is bounded.
 #include "common.cuh"
 #include "kernels.h"
+#include "tcgen05.cuh"
 
 namespace nvfp4kv {
 
 namespace {
 
-constexpr int kCThreads = 128;
-constexpr int kCRows = 64;                  // query rows per CTA
+constexpr int kCThreads = 128;              // one thread per query row
+constexpr int kCRows = 128;                 // query rows per CTA
 constexpr int kCKeys = 64;                  // tokens per stage
 constexpr int kCGroupBytes = 2304;          // one 16-token NVFP4 group
 constexpr int kCRaw = 4 * kCGroupBytes;     // one raw stage
-constexpr int kCRowBytes = 256;             // one FP16 row of 128 dims
-constexpr int kCTile = kCKeys * kCRowBytes;
-constexpr int kCKOff = 2 * kCRaw, kCVOff = kCKOff + kCTile, kCSmem = kCVOff + kCTile;
+constexpr int kCKVBlock = kCKeys * 128;     // one column block of a K or V tile
+constexpr int kCKVTile = 2 * kCKVBlock;
+constexpr int kCOffQ = 0;                                   // FP16 Q: 2 blocks of [128][64]
+constexpr int kCOffRaw = kCOffQ + kCRows * 256;             // raw stages [2]
+constexpr int kCOffKV = 53248;                              // K | V FP16 tiles (1024-aligned)
+constexpr int kCOffOnes = kCOffKV + 2 * kCKVTile;           // FP16 1.0 [16][64]
+constexpr int kCOffBar = kCOffOnes + 16 * 128;              // bar_s, bar_pv, raw_full[2]
+constexpr int kCOffTmem = kCOffBar + 32;
+constexpr int kCSmem = kCOffTmem + 16;
+static_assert(kCOffRaw + 2 * kCRaw <= kCOffKV, "raw stages overlap the tiles");
+constexpr uint32_t kCTmemCols = 256;        // S 0..63, P 64..95, O 96..223, row sums 224..239
+constexpr uint32_t kCColP = 64, kCColO = 96, kCColL = 224;
 constexpr float kCNegInf = -__builtin_huge_valf();
-constexpr uint32_t kCOnesF16x2 = 0x3c003c00u;
+constexpr uint32_t kCWaitLimit = 1u << 24;
 constexpr int kCMaxSplits = 16;
-constexpr int kCTargetCtas = 608;           // about 4 CTAs per SM of a 152-SM GPU
+constexpr int kCTargetCtas = 152;           // about one CTA per SM of a 152-SM GPU: fewer slices, fewer partials to merge
 
 struct SharedArgs {
     const uint8_t *pool;
@@ -54,115 +67,116 @@ struct SharedArgs {
     unsigned *err;
 };
 
-__device__ __forceinline__ uint32_t cswz(int row, int chunk) {
-    return (uint32_t)(row * kCRowBytes + ((chunk ^ (row & 7)) << 4));
-}
-
-__device__ __forceinline__ void c_cp_async16(uint32_t dst, const void *src, bool valid) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0)
-                 : "memory");
-}
-
-__device__ __forceinline__ void c_ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3,
-                                          bool trans) {
-    if (trans)
-        asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-                     : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                     : "r"(addr));
-    else
-        asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-                     : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                     : "r"(addr));
-}
-
 __device__ __forceinline__ float c_bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float c_bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
-// Q of one row as FP16 A-operand words (dims 16ks + 2c, +1 and 16ks + 2c + 8, +9)
-// after a power-of-two pre-scale that puts the head's largest |q| in
-// [2^14, 2^15); returns the score factor that undoes it.
-__device__ __forceinline__ float load_q_row(const uint32_t *qrow, bool valid, int c, float score_log2,
-                                            uint32_t (&w)[8][2]) {
-    uint32_t raw[8][2];
-    uint32_t m = 0;
-#pragma unroll
-    for (int ks = 0; ks < 8; ks++) {
-        raw[ks][0] = valid ? __ldg(qrow + 8 * ks + c) : 0u;
-        raw[ks][1] = valid ? __ldg(qrow + 8 * ks + 4 + c) : 0u;
-        m = __vmaxu2(m, raw[ks][0] & 0x7fff7fffu);
-        m = __vmaxu2(m, raw[ks][1] & 0x7fff7fffu);
-    }
-    m = max(m >> 16, m & 0xffffu);
-    m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
-    m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
-    int kq = 0;
-    if (m != 0) {
-        const int e = (int)((m >> 7) & 0xff) - 127;
-        kq = min(126, max(-126, 14 - e));
-    }
-    const float s = __uint_as_float((uint32_t)(kq + 127) << 23);
-#pragma unroll
-    for (int ks = 0; ks < 8; ks++)
-#pragma unroll
-        for (int h = 0; h < 2; h++) w[ks][h] = f32x2_to_f16x2(c_bf16_hi(raw[ks][h]) * s, c_bf16_lo(raw[ks][h]) * s);
-    return score_log2 * __uint_as_float((uint32_t)(127 - kq) << 23);
-}
-
-__global__ void __launch_bounds__(kCThreads, 3) shared_prefix_kernel(SharedArgs a) {
-    extern __shared__ __align__(128) uint8_t smem[];
+__global__ void __launch_bounds__(kCThreads, 2) shared_prefix_kernel(SharedArgs a) {
+    extern __shared__ __align__(1024) uint8_t smem[];
+    uint64_t &bar_s = *reinterpret_cast<uint64_t *>(smem + kCOffBar);
+    uint64_t &bar_pv = *reinterpret_cast<uint64_t *>(smem + kCOffBar + 8);
+    uint64_t *raw_full = reinterpret_cast<uint64_t *>(smem + kCOffBar + 16);
+    uint32_t &tmem_base = *reinterpret_cast<uint32_t *>(smem + kCOffTmem);
     pdl_launch_dependents();
     pdl_wait();  // q and the cache may come from earlier work on the stream
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int g = lane >> 2, c = lane & 3;
+    const int tid = threadIdx.x, warp = tid >> 5;
     const int kv = blockIdx.y, split = blockIdx.z;
     const int rows = a.B * a.G;
     const int row0 = blockIdx.x * kCRows;
     const int t_begin = split * a.tiles_per_split;
     const int t_end = min(a.ntiles, t_begin + a.tiles_per_split);
     if (row0 >= rows || t_begin >= t_end) return;
-
-    const int ra = row0 + 16 * warp + g, rb = ra + 8;
-    const bool va = ra < rows, vb = rb < rows;
-    const int ba = va ? ra / a.G : 0, ha = va ? ra % a.G : 0;
-    const int bb = vb ? rb / a.G : 0, hb = vb ? rb % a.G : 0;
-    uint32_t qa[8][2], qb[8][2];
-    const float fa = load_q_row(a.q + ((int64_t)ba * a.Hq + kv * a.G + ha) * (kHeadDim / 2), va, c, a.score_log2, qa);
-    const float fb = load_q_row(a.q + ((int64_t)bb * a.Hq + kv * a.G + hb) * (kHeadDim / 2), vb, c, a.score_log2, qb);
-
+    const int nt = t_end - t_begin;
     const uint32_t sbase = smem_u32(smem);
-    // raw stage of tile i into slot s: 4 groups x 144 chunks of 16 bytes
-    auto issue = [&](int i, int s) {
-        for (int idx = tid; idx < 4 * 144; idx += kCThreads) {
-            const int gi = idx / 144, ci = idx - gi * 144;
-            const int t = i * kCKeys + 16 * gi;
+
+    // raw stage of tile i (0-based in this slice) into slot s: four groups, thread 0
+    auto issue_raw = [&](int i, int s) {
+        mbar_arrive_expect_tx(&raw_full[s], kCRaw);
+        for (int gi = 0; gi < 4; gi++) {
+            const int t = (t_begin + i) * kCKeys + 16 * gi;
             const int32_t pg = __ldg(a.shared_pages + (t >> a.log2P));
-            const bool ok = pg >= 0 && (int64_t)pg < a.num_pages;
-            if (!ok && ci == 0) flag_error(a.err, kErrPage);
-            const uint8_t *src = ok ? a.pool + ((int64_t)pg * a.Hkv + kv) * a.slab +
-                                          ((t & (a.P - 1)) >> 4) * kCGroupBytes + ci * 16
-                                    : a.pool;
-            c_cp_async16(sbase + s * kCRaw + gi * kCGroupBytes + ci * 16, src, ok);
+            const uint8_t *src = a.pool;
+            if (pg >= 0 && (int64_t)pg < a.num_pages)
+                src = a.pool + ((int64_t)pg * a.Hkv + kv) * a.slab + ((t & (a.P - 1)) >> 4) * kCGroupBytes;
+            else
+                flag_error(a.err, kErrPage);  // the group is fetched from the pool start, i.e. garbage
+            bulk_g2s(smem + kCOffRaw + s * kCRaw + gi * kCGroupBytes, src, kCGroupBytes, &raw_full[s]);
         }
     };
+    if (tid == 0) {
+        mbar_init(&bar_s, 1);
+        mbar_init(&bar_pv, 1);
+        mbar_init(&raw_full[0], 1);
+        mbar_init(&raw_full[1], 1);
+        fence_mbar_init();
+        issue_raw(0, 0);
+        if (nt > 1) issue_raw(1, 1);
+    }
+    if (warp == 0) tc_alloc(&tmem_base, kCTmemCols);
 
-    float o[16][4], ol[4] = {0.f, 0.f, 0.f, 0.f};
+    // ---- this thread's query row, FP16 after a power-of-two pre-scale that puts
+    // its largest |q| in [2^14, 2^15); the score factor undoes it
+    const int R = row0 + tid;
+    const bool row_ok = R < rows;
+    const int b = row_ok ? R / a.G : 0, h = row_ok ? R % a.G : 0;
+    float fac;
+    {
+        const uint4 *qrow = reinterpret_cast<const uint4 *>(a.q + ((int64_t)b * a.Hq + kv * a.G + h) * (kHeadDim / 2));
+        uint4 w[16];
+        uint32_t m = 0;
 #pragma unroll
-    for (int i = 0; i < 16; i++) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-    float m_a = kCNegInf, m_b = kCNegInf;
+        for (int i = 0; i < 16; i++) {
+            w[i] = row_ok ? __ldg(qrow + i) : make_uint4(0, 0, 0, 0);
+            m = __vmaxu2(m, w[i].x & 0x7fff7fffu);
+            m = __vmaxu2(m, w[i].y & 0x7fff7fffu);
+            m = __vmaxu2(m, w[i].z & 0x7fff7fffu);
+            m = __vmaxu2(m, w[i].w & 0x7fff7fffu);
+        }
+        m = max(m >> 16, m & 0xffffu);
+        int kq = 0;
+        if (m != 0) kq = min(126, max(-126, 14 - ((int)((m >> 7) & 0xff) - 127)));
+        const float sc = __uint_as_float((uint32_t)(kq + 127) << 23);
+        fac = a.score_log2 * __uint_as_float((uint32_t)(127 - kq) << 23);
+#pragma unroll
+        for (int i = 0; i < 16; i++) {  // chunk i = dims 8i .. 8i+7
+            const uint32_t x[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
+            uint32_t f[4];
+#pragma unroll
+            for (int e = 0; e < 4; e++) f[e] = f32x2_to_f16x2(c_bf16_hi(x[e]) * sc, c_bf16_lo(x[e]) * sc);
+            *reinterpret_cast<uint4 *>(smem + kCOffQ + (i >> 3) * (kCRows * 128) + sw128_off(tid, i & 7)) =
+                make_uint4(f[0], f[1], f[2], f[3]);
+        }
+    }
+    for (int idx = tid; idx < 16 * 128 / 16; idx += kCThreads) {  // FP16 1.0 everywhere
+        const uint32_t one2 = 0x3c003c00u;
+        *reinterpret_cast<uint4 *>(smem + kCOffOnes + idx * 16) = make_uint4(one2, one2, one2, one2);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base;
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const uint32_t sQ = sbase + kCOffQ, sK = sbase + kCOffKV, sV = sK + kCKVTile, sOnes = sbase + kCOffOnes;
+    constexpr uint32_t idesc_s = idesc_f16_f32(128, kCKeys, false);
+    constexpr uint32_t idesc_o = idesc_f16_f32(128, kHeadDim, true);
+    constexpr uint32_t idesc_l = idesc_f16_f32(128, 16, false);
+    float m_run = kCNegInf;
+    bool aborted = false;
 
-    issue(t_begin, 0);
-    asm volatile("cp.async.commit_group;" ::: "memory");
-    if (t_begin + 1 < t_end) issue(t_begin + 1, 1);
-    asm volatile("cp.async.commit_group;" ::: "memory");
-    for (int i = t_begin; i < t_end; i++) {
-        const int slot = (i - t_begin) & 1;
-        asm volatile("cp.async.wait_group 1;" ::: "memory");
-        __syncthreads();
-        // ---- dequantise the raw stage into FP16 K and V tiles
-        const uint8_t *raw = smem + slot * kCRaw;
+    for (int i = 0; i < nt; i++) {
+        const int slot = i & 1;
+        bool ok = mbar_wait_bounded(&raw_full[slot], (uint32_t)((i >> 1) & 1), kCWaitLimit, nullptr);
+        if (i > 0) ok = ok && mbar_wait_bounded(&bar_pv, (uint32_t)((i - 1) & 1), kCWaitLimit, nullptr);
+        if (__syncthreads_or(!ok)) {  // the raw stage landed and P V of the previous tile is done
+            if (tid == 0) flag_error(a.err, kErrTimeout);
+            aborted = true;
+            break;
+        }
+        tc_fence_after();
+        // ---- dequantise the raw stage into the FP16 K and V tiles
+        const uint8_t *raw = smem + kCOffRaw + slot * kCRaw;
 #pragma unroll
         for (int it = 0; it < 8; it++) {
-            const int u = tid + it * kCThreads;  // 0..1023: K units then V units
+            const int u = tid + it * kCThreads;  // K units then V units
             const int which = u >> 9, key = (u >> 3) & 63, blk = u & 7;
             const uint8_t *grp = raw + (key >> 4) * kCGroupBytes;
             const int rr = key & 15;
@@ -174,102 +188,115 @@ __global__ void __launch_bounds__(kCThreads, 3) shared_prefix_kernel(SharedArgs 
             e2m1x8_to_f16x2x4(codes.y, f[4], f[5], f[6], f[7]);
 #pragma unroll
             for (int j = 0; j < 8; j++) f[j] = hmul2(f[j], s2);
-            uint8_t *tile = smem + (which ? kCVOff : kCKOff);
-            *reinterpret_cast<uint4 *>(tile + cswz(key, 2 * blk)) = make_uint4(f[0], f[1], f[2], f[3]);
-            *reinterpret_cast<uint4 *>(tile + cswz(key, 2 * blk + 1)) = make_uint4(f[4], f[5], f[6], f[7]);
+            uint8_t *tile = smem + kCOffKV + which * kCKVTile + (blk >> 2) * kCKVBlock;
+            *reinterpret_cast<uint4 *>(tile + sw128_off(key, (blk & 3) * 2)) = make_uint4(f[0], f[1], f[2], f[3]);
+            *reinterpret_cast<uint4 *>(tile + sw128_off(key, (blk & 3) * 2 + 1)) = make_uint4(f[4], f[5], f[6], f[7]);
         }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the tiles for the tensor core
+        tc_fence_before();
         __syncthreads();
-        if (i + 2 < t_end) issue(i + 2, slot);  // the raw slot has been consumed
-        asm volatile("cp.async.commit_group;" ::: "memory");
+        if (tid == 0) {
+            tc_fence_after();
+            if (i + 2 < nt) issue_raw(i + 2, slot);  // this raw slot has been dequantised
+#pragma unroll
+            for (int kk = 0; kk < 8; kk++) {  // S = Q K^T over head_dim, 16 at a time
+                const uint32_t blk = (uint32_t)(kk >> 2), sub = (uint32_t)(kk & 3) * 32;
+                tc_mma_bf16(tmem, smem_desc_sw128(sQ + blk * (kCRows * 128) + sub, 16, 1024),
+                            smem_desc_sw128(sK + blk * kCKVBlock + sub, 16, 1024), idesc_s, kk > 0);
+            }
+            tc_commit(&bar_s);
+        }
+        ok = mbar_wait_bounded(&bar_s, (uint32_t)(i & 1), kCWaitLimit, nullptr);
+        if (__syncthreads_or(!ok)) {
+            if (tid == 0) flag_error(a.err, kErrTimeout);
+            aborted = true;
+            break;
+        }
+        tc_fence_after();
 
-        // ---- S = Q K^T (16 rows x 64 keys per warp)
-        const uint32_t kt = sbase + kCKOff, vt = sbase + kCVOff;
-        float s[8][4];
+        // ---- softmax of this thread's row (every shared token is visible)
+        uint32_t sr[2][32];
+        tc_ld32(tmem + lane_base + 0, sr[0]);
+        tc_ld32(tmem + lane_base + 32, sr[1]);
+        tc_wait_ld();
+        float smax = __uint_as_float(sr[0][0]);
 #pragma unroll
-        for (int n = 0; n < 8; n++) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
+        for (int j = 1; j < 64; j++) smax = fmaxf(smax, __uint_as_float(sr[j >> 5][j & 31]));
+        const float mx = smax * fac;
+        const bool need = mx > m_run + 8.0f;
+        if (__any_sync(0xffffffffu, need)) {
+            const float m_new = need ? fmaxf(m_run, mx) : m_run;
+            const float alpha = need ? (m_run == kCNegInf ? 0.f : ex2(m_run - m_new)) : 1.f;
+            if (i > 0) {  // O and the row sums hold earlier tiles
 #pragma unroll
-        for (int ks = 0; ks < 8; ks++) {
+                for (int cblk = 0; cblk < 5; cblk++) {
+                    uint32_t ov[32];
+                    const uint32_t col = cblk < 4 ? kCColO + 32 * cblk : kCColL;
+                    tc_ld32(tmem + lane_base + col, ov);
+                    tc_wait_ld();
 #pragma unroll
-            for (int j = 0; j < 4; j++) {
-                const int m = lane >> 3;
-                const int key = 16 * j + (m >> 1) * 8 + (lane & 7);
-                uint32_t b0, b1, b2, b3;
-                c_ldsm_x4(kt + cswz(key, 2 * ks + (m & 1)), b0, b1, b2, b3, false);
-                mma_f16_16816(s[2 * j], qa[ks][0], qb[ks][0], qa[ks][1], qb[ks][1], b0, b1);
-                mma_f16_16816(s[2 * j + 1], qa[ks][0], qb[ks][0], qa[ks][1], qb[ks][1], b2, b3);
+                    for (int j = 0; j < 32; j++) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * alpha);
+                    tc_st32(tmem + lane_base + col, ov);
+                }
+                tc_wait_st();
+            }
+            m_run = m_new;
+        }
+        const float neg_m = -m_run;
+        uint32_t pw[32];
+#pragma unroll
+        for (int c = 0; c < 32; c++)
+            pw[c] = f32x2_to_f16x2(ex2(fmaf(__uint_as_float(sr[(2 * c + 1) >> 5][(2 * c + 1) & 31]), fac, neg_m)),
+                                   ex2(fmaf(__uint_as_float(sr[(2 * c) >> 5][(2 * c) & 31]), fac, neg_m)));
+        tc_st32(tmem + lane_base + kCColP, pw);
+        tc_wait_st();
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < 4; kk++) {  // O += P V; row sums += P 1
+                const uint32_t pa = tmem + kCColP + kk * 8;
+                const uint32_t accf = (i > 0 || kk > 0) ? 1u : 0u;
+                tc_mma_bf16_tmem_a(tmem + kCColO, pa, smem_desc_sw128(sV + kk * 16 * 128, kCKVBlock, 1024), idesc_o,
+                                   accf);
+                tc_mma_bf16_tmem_a(tmem + kCColL, pa, smem_desc_sw128(sOnes + kk * 32, 16, 1024), idesc_l, accf);
+            }
+            tc_commit(&bar_pv);
+        }
+    }
+    if (!aborted) {
+        const bool ok = mbar_wait_bounded(&bar_pv, (uint32_t)((nt - 1) & 1), kCWaitLimit, nullptr);
+        if (__syncthreads_or(!ok)) {
+            if (tid == 0) flag_error(a.err, kErrTimeout);
+            aborted = true;
+        }
+        tc_fence_after();
+    }
+    if (!aborted) {
+        // ---- this slice's partial of the row: (m, l) and the unnormalised acc
+        uint32_t lv[32];
+        tc_ld32(tmem + lane_base + kCColL, lv);
+        tc_wait_ld();
+        const int64_t idx = ((int64_t)split * a.B * a.Hkv + (int64_t)b * a.Hkv + kv) * a.G + h;
+        if (row_ok) a.ml[idx] = make_float2(m_run, __uint_as_float(lv[0]));
+        float4 *dst = reinterpret_cast<float4 *>(a.acc + idx * kHeadDim);
+#pragma unroll
+        for (int cblk = 0; cblk < 4; cblk++) {
+            uint32_t ov[32];
+            tc_ld32(tmem + lane_base + kCColO + 32 * cblk, ov);
+            tc_wait_ld();
+            if (row_ok) {
+#pragma unroll
+                for (int j = 0; j < 8; j++)
+                    dst[8 * cblk + j] = make_float4(__uint_as_float(ov[4 * j]), __uint_as_float(ov[4 * j + 1]),
+                                                    __uint_as_float(ov[4 * j + 2]), __uint_as_float(ov[4 * j + 3]));
             }
         }
-        // ---- online softmax, base 2 (every key of the shared prefix is valid)
-        float mx_a = kCNegInf, mx_b = kCNegInf;
-#pragma unroll
-        for (int n = 0; n < 8; n++) {
-            s[n][0] *= fa;
-            s[n][1] *= fa;
-            s[n][2] *= fb;
-            s[n][3] *= fb;
-            mx_a = fmaxf(mx_a, fmaxf(s[n][0], s[n][1]));
-            mx_b = fmaxf(mx_b, fmaxf(s[n][2], s[n][3]));
-        }
-        mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 1));
-        mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 2));
-        mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 1));
-        mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 2));
-        if (__any_sync(0xffffffffu, mx_a > m_a + 8.0f || mx_b > m_b + 8.0f)) {
-            const float na = fmaxf(m_a, mx_a), nb = fmaxf(m_b, mx_b);
-            const float ca = m_a == kCNegInf ? 0.f : ex2(m_a - na), cb = m_b == kCNegInf ? 0.f : ex2(m_b - nb);
-            m_a = na;
-            m_b = nb;
-            ol[0] *= ca;
-            ol[1] *= ca;
-            ol[2] *= cb;
-            ol[3] *= cb;
-#pragma unroll
-            for (int d = 0; d < 16; d++) {
-                o[d][0] *= ca;
-                o[d][1] *= ca;
-                o[d][2] *= cb;
-                o[d][3] *= cb;
-            }
-        }
-        uint32_t pa[4][4];
-#pragma unroll
-        for (int n = 0; n < 8; n++) {
-            pa[n >> 1][(n & 1) * 2 + 0] = f32x2_to_f16x2(ex2(s[n][1] - m_a), ex2(s[n][0] - m_a));
-            pa[n >> 1][(n & 1) * 2 + 1] = f32x2_to_f16x2(ex2(s[n][3] - m_b), ex2(s[n][2] - m_b));
-        }
-        // ---- O += P V, and the row sums of the same FP16 P
-#pragma unroll
-        for (int kk = 0; kk < 4; kk++) {
-#pragma unroll
-            for (int nd = 0; nd < 16; nd += 2) {
-                const int m = lane >> 3;
-                const int key = 16 * kk + (m & 1) * 8 + (lane & 7);
-                uint32_t b0, b1, b2, b3;
-                c_ldsm_x4(vt + cswz(key, nd + (m >> 1)), b0, b1, b2, b3, true);
-                mma_f16_16816(o[nd], pa[kk][0], pa[kk][1], pa[kk][2], pa[kk][3], b0, b1);
-                mma_f16_16816(o[nd + 1], pa[kk][0], pa[kk][1], pa[kk][2], pa[kk][3], b2, b3);
-            }
-            mma_f16_16816(ol, pa[kk][0], pa[kk][1], pa[kk][2], pa[kk][3], kCOnesF16x2, kCOnesF16x2);
-        }
-        __syncthreads();  // the tiles are rewritten by the next stage
     }
-
-    // ---- partials of this slice: (m, l) and unnormalised acc per row
-    const int64_t pairs = (int64_t)a.B * a.Hkv;
-    if (va) {
-        const int64_t idx = ((int64_t)split * pairs + (int64_t)ba * a.Hkv + kv) * a.G + ha;
-        if (c == 0) a.ml[idx] = make_float2(m_a, ol[0]);
-        float *dst = a.acc + idx * kHeadDim;
-#pragma unroll
-        for (int d = 0; d < 16; d++) *reinterpret_cast<float2 *>(dst + 8 * d + 2 * c) = make_float2(o[d][0], o[d][1]);
-    }
-    if (vb) {
-        const int64_t idx = ((int64_t)split * pairs + (int64_t)bb * a.Hkv + kv) * a.G + hb;
-        if (c == 0) a.ml[idx] = make_float2(m_b, ol[2]);
-        float *dst = a.acc + idx * kHeadDim;
-#pragma unroll
-        for (int d = 0; d < 16; d++) *reinterpret_cast<float2 *>(dst + 8 * d + 2 * c) = make_float2(o[d][2], o[d][3]);
-    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tc_dealloc(tmem, kCTmemCols);
 }
 
 }  // namespace

@@ -31,6 +31,12 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool b_mn_ma
            ((uint32_t)(M >> 4) << 24);
 }
 
+// Instruction descriptor, kind::f16 with FP16 inputs and FP32 accumulation.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, bool b_mn_major) {
+    return (1u << 4) | ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// D (+)= A B for kind::f16 (the instruction descriptor fixes the input type).
 __device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                             uint32_t accumulate) {
     asm volatile(
