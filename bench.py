@@ -55,6 +55,8 @@ def parse_args():
     p.add_argument("--num-splits", type=int, default=0)
     p.add_argument("--batch", type=int, default=64,
                    help="sequences of the 32K workload (64 = the benchmark; smaller = a profiling case)")
+    p.add_argument("--comparison", choices=["extend", "agent_decode"], default=None,
+                   help="run only this comparison (its own JSON line; a profiling case) and exit")
     return p.parse_args()
 
 
@@ -654,9 +656,25 @@ def run_ours(args):
         print(json.dumps(line), flush=True)
 
 
+def run_comparison(args):
+    """One comparison on its own, for a profiler to capture its kernels."""
+    import torch
+
+    import nvfp4_quantised_paged_gb300 as m
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    if args.comparison == "extend":
+        res = time_extend(m, device, args.steps, args.warmup, load_bf16_peak())
+    else:
+        res = time_agent_decode(m, device, args.steps, args.warmup)
+    print(json.dumps({"comparison": args.comparison, **res}), flush=True)
+
+
 def main():
     args = parse_args()
-    if args.impl == "reference":
+    if args.comparison:
+        run_comparison(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)
