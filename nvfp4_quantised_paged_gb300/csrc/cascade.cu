@@ -76,8 +76,12 @@ __global__ void __launch_bounds__(kCThreads, 2) shared_prefix_kernel(SharedArgs 
     uint64_t &bar_pv = *reinterpret_cast<uint64_t *>(smem + kCOffBar + 8);
     uint64_t *raw_full = reinterpret_cast<uint64_t *>(smem + kCOffBar + 16);
     uint32_t &tmem_base = *reinterpret_cast<uint32_t *>(smem + kCOffTmem);
+    // q and the cache may come from earlier work on the stream.  The decode
+    // kernel launched behind this one reads the plan's results without a wait
+    // of its own: every CTA here first waits for the plan to complete, then
+    // lets the decode grid launch.
+    pdl_wait();
     pdl_launch_dependents();
-    pdl_wait();  // q and the cache may come from earlier work on the stream
     const int tid = threadIdx.x, warp = tid >> 5;
     const int kv = blockIdx.y, split = blockIdx.z;
     const int rows = a.B * a.G;

@@ -122,6 +122,7 @@ struct DecodeArgs {
     int dtype, unit_scale;
     uint8_t *pool_w;       // the pool, writable
     int skip;              // tokens at the start of every sequence left to the shared-prefix kernel
+    int after_shared;      // launched behind the shared-prefix kernel (see decode_kernel)
 };
 
 __device__ __forceinline__ int clamp_len(int32_t n, int64_t cap) {
@@ -640,12 +641,21 @@ __global__ void __launch_bounds__(kThreads, DTYPE == NVFP4KV_DTYPE_NVFP4 && NT =
     extern __shared__ __align__(128) uint8_t smem[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     pdl_launch_dependents();  // the reduction may be scheduled once every CTA runs
-    pdl_wait();               // chunk_prefix comes from the plan kernel
+    // chunk_prefix comes from the plan kernel.  Behind the shared-prefix
+    // kernel, this grid starts only once every CTA of that kernel has waited
+    // for the plan to complete (and flush) and then triggered, so the plan's
+    // results are in global memory already and the wait moves to the exit:
+    // the decode then runs beside the shared-prefix kernel, and its own
+    // completion, which the reduction waits for, implies that kernel's.
+    if (!a.after_shared) pdl_wait();
 
     const int64_t U = (int64_t)a.Hkv * a.chunk_prefix[a.B];
     const int64_t c = blockIdx.x;
     const int64_t u0 = c * U / a.grid, u1 = (c + 1) * U / a.grid;
-    if (u0 >= u1) return;
+    if (u0 >= u1) {
+        if (a.after_shared) pdl_wait();
+        return;
+    }
     const int nstages = (int)(u1 - u0);
 
     uint8_t *ring = smem;
@@ -814,6 +824,7 @@ __global__ void __launch_bounds__(kThreads, DTYPE == NVFP4KV_DTYPE_NVFP4 && NT =
             if (last >= 0) mbar_wait_bounded(&full[s], (uint32_t)((last / kSlots) & 1), kWaitLimit, nullptr);
         }
     }
+    if (a.after_shared) pdl_wait();
 }
 
 // Plan: chunk_prefix[b] = sum over b' < b of ceil((len(b') - skip) / 64); one CTA.
@@ -1131,6 +1142,7 @@ cudaError_t launch_decode(const nvfp4kv_cache &c, const void *q, int batch, int 
     a.unit_scale = c.k_global_scale == 1.0f && c.v_global_scale == 1.0f;
     a.pool_w = static_cast<uint8_t *>(c.pool);
     a.skip = skip;
+    a.after_shared = shared_pages ? 1 : 0;
     int smem = 0;
     const void *fn = select_kernel(c.dtype, nt, &smem);
     void *args[] = {&a};
