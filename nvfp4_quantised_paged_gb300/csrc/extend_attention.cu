@@ -8,30 +8,36 @@
 // attends to the whole prefix and to chunk tokens 0..i.
 //
 // GB300 design: a flash-attention forward on the 5th-generation tensor cores.
-// One CTA = 4 warps = 128 query rows of one (request, kv head), row = chunk
-// token * G + query head of the group, so the G heads that share a KV head
-// share every K/V tile.  Per 64-key tile:
-//   * thread 0 loads K and V with four TMA boxes (3-D tensor maps, 128-byte
-//     swizzle = the tensor core's canonical operand layout) into one of two
-//     stages, completing on that stage's mbarrier;
-//   * thread 0 issues S = Q K^T as eight tcgen05.mma (M 128, N 64, K 16) with
-//     Q and K read from shared memory by descriptor, accumulating in TMEM
-//     columns 0..63, and commits to an mbarrier;
-//   * each thread owns one query row = one TMEM lane: it loads its 64 scores
-//     (tcgen05.ld), masks them on edge tiles only, runs the base-2 online
-//     softmax with a lazily updated running max (O and the row sums in TMEM
-//     are rescaled only when a score exceeds the max by 2^8), forms
-//     P = 2^(s * scale - m) with one FFMA per score, rounds it to BF16 and
-//     stores its row of P into TMEM (tcgen05.st);
-//   * thread 0 then runs O += P V as four tcgen05.mma with P read from TMEM
-//     (M 128, N 128, K 16, V as an MN-major operand) into TMEM columns
-//     96..223, and the row sums as four more with an all-ones B operand, so
-//     numerator and denominator see the same rounded P.
-// The commit after the next S means S and every earlier MMA are done, which
-// also frees P and the previous K/V stage (refilled right then).  Two CTAs
-// share an SM (99 KB of shared memory and 256 TMEM columns each), so one
-// CTA's softmax overlaps the other's MMAs.  Every wait is bounded; a timeout
-// is reported in the device error word and taken by all threads together.
+// A dependent chain of tcgen05.mma (the K = 16 steps of one product into one
+// accumulator) runs at the tensor core's rate only when each instruction is
+// large: M 128 x N 64 steps are latency-bound at about a third of it, N 128
+// close to it.  So K/V tiles are 128 keys, and each CTA holds two 128-row
+// query tiles whose four products per K/V tile (S0, S1, O0 += P0 V, O1 +=
+// P1 V) are independent chains that the tensor core overlaps.
+//
+// One CTA = 256 query rows of one (request, kv head), row = chunk token * G +
+// query head of the group, so the G heads that share a KV head share every
+// K/V tile; one CTA per SM (192 KB of shared memory, all 512 TMEM columns).
+// Nine warps:
+//   * warpgroup w (warps 4w .. 4w + 3, w = 0, 1), one thread per row of query
+//     tile w = one TMEM lane, runs the softmax of that tile: wait for S_w(j)
+//     (128 scores per row, FP32 in TMEM columns 128w ..), load it, mask edge
+//     tiles only, base-2 online softmax with a lazily updated running max
+//     (O_w in TMEM is rescaled only when a score exceeds the max by 2^8),
+//     P = 2^(s * scale - m) rounded to BF16 and stored over the first half of
+//     S_w's columns, the row sum of the rounded P kept in a register (the
+//     numerator and the denominator see the same P); then signal P_w(j);
+//   * one thread of warp 8 drives the TMA loads (3-D tensor maps, 128-byte
+//     swizzle = the tensor core's canonical operand layout) and the MMAs, per
+//     K/V tile j: S0(j) = Q0 K(j)^T and S1(j) = Q1 K(j)^T (eight M 128 x N 128
+//     x K 16 steps each), then O_w += P_w(j) V(j) as P_w(j) arrives (eight
+//     steps over the 128 keys, P read from TMEM, V an MN-major operand).
+//     S_w(j + 1) waits for O_w += P_w(j) V(j), whose P shares its columns, so
+//     while warpgroup 0 works on tile j + 1 the tensor core runs the products
+//     of query tile 1, and the other way round.
+// K and V have two-slot rings each; K(j + 2) is requested once S1(j) is done,
+// V(j + 1) once O1 += P1(j - 1) V(j - 1) is done.  Every wait is bounded; a
+// timeout is recorded in the device error word and ends every warp's loop.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -42,26 +48,32 @@ namespace nvfp4kv {
 
 namespace {
 
-constexpr int kEThreads = 128;            // one thread per query row
-constexpr int kQRows = 128;               // query rows per CTA
-constexpr int kKeys = 64;                 // keys per K/V tile
-constexpr int kQBytes = kQRows * 256;     // Q: 2 column blocks of [128][64] BF16
-constexpr int kKVBlock = kKeys * 128;     // one column block of a K or V tile (one TMA box)
-constexpr int kKVTile = 2 * kKVBlock;     // a whole K (or V) tile
-constexpr int kStageBytes = 2 * kKVTile;  // K | V
-constexpr int kOnesBytes = 16 * 128;      // all-ones B operand [16][64] for the row sums
-constexpr int kOffQ = 0, kOffStage = kQBytes, kOffOnes = kOffStage + 2 * kStageBytes;
-constexpr int kOffBar = kOffOnes + kOnesBytes;  // bar_mma, full[2]
-constexpr int kOffTmem = kOffBar + 24;
-constexpr int kOffOrder = kOffTmem + 8;   // int[128]: requests by decreasing prefix length
-constexpr int kESmem = kOffOrder + 4 * 128;
-// TMEM columns: S 0..63 (FP32), P 64..95 (BF16 pairs), O 96..223, row sums 224..239
-constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kColP = 64, kColO = 96, kColL = 224;
+constexpr int kWGs = 2;                        // softmax warpgroups = query tiles per CTA
+constexpr int kQRows = 128;                    // rows per query tile (one TMEM lane each)
+constexpr int kCtaRows = kWGs * kQRows;
+constexpr int kSoftThreads = kWGs * kQRows;
+constexpr int kEThreads = kSoftThreads + 32;   // + the load / MMA warp
+constexpr int kKeys = 128;                     // keys per K/V tile
+constexpr int kQBytes = kQRows * 256;          // a query tile: 2 column blocks of [128][64] BF16
+constexpr int kKVBlock = kKeys * 128;          // one column block of a K or V tile (one TMA box)
+constexpr int kKVTile = 2 * kKVBlock;          // a whole K (or V) tile, 32 KB
+constexpr int kOffQ = 0;                                   // Q0 | Q1
+constexpr int kOffK = kWGs * kQBytes;                      // K slots [2]
+constexpr int kOffV = kOffK + 2 * kKVTile;                 // V slots [2]
+constexpr int kOffBar = kOffV + 2 * kKVTile;
+// mbarriers: k_full[2] v_full[2] s_done[2] p_full[2] pv_done[2] drain
+constexpr int kNumBars = 11;
+constexpr int kOffTmem = kOffBar + kNumBars * 8;
+constexpr int kOffAbort = kOffTmem + 4;
+constexpr int kOffOrder = kOffBar + 128;       // int[256]: requests by decreasing prefix length
+constexpr int kOrderMax = 256;
+constexpr int kESmem = kOffOrder + 4 * kOrderMax;
+// TMEM columns: S_w at 128w (FP32; P_w as BF16 pairs over its first 64 columns), O_w at 256 + 128w
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColO = 256;
 constexpr float kRescale = 8.0f;
 constexpr float kNegInfE = -__builtin_huge_valf();
 constexpr uint32_t kWaitLimitE = 1u << 24;
-constexpr int kOrderMax = kEThreads;      // requests ordered by prefix length up to this many
 
 struct ExtendArgs {
     const uint16_t *q;                 // BF16 [total_q][Hq][128]
@@ -72,7 +84,7 @@ struct ExtendArgs {
     unsigned *err;
 };
 
-// K/V tensors [rows][Hkv][128] BF16 as 3-D TMA maps with 64 x 1 x 64 boxes, 128-byte swizzle.
+// K/V tensors [rows][Hkv][128] BF16 as 3-D TMA maps with 64 x 1 x 128 boxes, 128-byte swizzle.
 struct ExtendMaps {
     CUtensorMap k_pre, v_pre, k_new, v_new;
 };
@@ -91,12 +103,31 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
-__global__ void __launch_bounds__(kEThreads, 2) extend_kernel(const __grid_constant__ ExtendMaps maps, ExtendArgs a) {
+
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// (a.x + b.x, a.y + b.y) in one instruction
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;"
+        : "=l"(d)
+        : "l"((uint64_t)__float_as_uint(a.x) | ((uint64_t)__float_as_uint(a.y) << 32)),
+          "l"((uint64_t)__float_as_uint(b.x) | ((uint64_t)__float_as_uint(b.y) << 32)));
+    return make_float2(__uint_as_float((uint32_t)d), __uint_as_float((uint32_t)(d >> 32)));
+}
+
+__global__ void __launch_bounds__(kEThreads, 1) extend_kernel(const __grid_constant__ ExtendMaps maps, ExtendArgs a) {
     extern __shared__ __align__(1024) uint8_t smem[];
-    uint64_t &bar_mma = *reinterpret_cast<uint64_t *>(smem + kOffBar);
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kOffBar + 8);  // [2]: stage landed
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBar);
+    uint64_t *k_full = bars, *v_full = bars + 2, *s_done = bars + 4, *p_full = bars + 6, *pv_done = bars + 8;
+    uint64_t *drain = bars + 10;
     uint32_t &tmem_base = *reinterpret_cast<uint32_t *>(smem + kOffTmem);
-    const int tid = threadIdx.x, warp = tid >> 5;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffAbort);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // Requests in order of decreasing prefix length (the longest CTAs start
     // first, so the tail of the grid holds short ones): blockIdx.z is the
     // rank; thread j ranks request j.
@@ -129,198 +160,304 @@ __global__ void __launch_bounds__(kEThreads, 2) extend_kernel(const __grid_const
         L = a.max_q_len;
     }
     const int rows = L * a.G;
-    const int row0 = blockIdx.x * kQRows;
+    const int row0 = blockIdx.x * kCtaRows;
     if (row0 >= rows) return;
-    const int t_last = (min(row0 + kQRows, rows) - 1) / a.G;  // last chunk token of this CTA
+    const int nwg = row0 + kQRows < rows ? 2 : 1;               // query tiles holding rows
+    const int t_last = (min(row0 + kCtaRows, rows) - 1) / a.G;  // last chunk token of this CTA
     const int nt_pre = (np + kKeys - 1) / kKeys;
     const int nt = nt_pre + t_last / kKeys + 1;
 
     const uint32_t sbase = smem_u32(smem);
-    const uint32_t sQ = sbase + kOffQ;
 
-    // ---- Q tile: 128 rows x 16 chunks of 16 bytes
+    // ---- query tiles: 128 rows x 16 chunks of 16 bytes each, by their warpgroups
+    if (tid < kSoftThreads) {
+        const int w = tid >> 7, t = tid & 127;
+        const uint32_t sQ = sbase + kOffQ + w * kQBytes;
 #pragma unroll 4
-    for (int it = 0; it < 16; it++) {
-        const int idx = tid + it * kEThreads;
-        const int row = idx >> 4, c16 = idx & 15;
-        const int R = row0 + row;
-        const bool ok = R < rows;
-        const int64_t src = ok ? (((int64_t)q0 + R / a.G) * a.Hq + kv * a.G + R % a.G) * kHeadDim + c16 * 8 : 0;
-        cp_async16(sQ + (c16 >> 3) * (kQRows * 128) + sw128_off(row, c16 & 7), a.q + src, ok);
+        for (int it = 0; it < 16; it++) {
+            const int idx = t + it * kQRows;
+            const int row = idx >> 4, c16 = idx & 15;
+            const int R = row0 + w * kQRows + row;
+            const bool ok = R < rows;
+            const int64_t src = ok ? (((int64_t)q0 + R / a.G) * a.Hq + kv * a.G + R % a.G) * kHeadDim + c16 * 8 : 0;
+            cp_async16(sQ + (c16 >> 3) * (kQRows * 128) + sw128_off(row, c16 & 7), a.q + src, ok);
+        }
     }
-    // K/V tile i into stage s: four TMA boxes (K and V, head_dim 0..63 and
-    // 64..127) completing on full[s]; rows past the tensor are zero-filled,
-    // rows of a neighbouring request are masked by the softmax
-    auto issue = [&](int i, int s) {  // thread 0
-        const bool pre = i < nt_pre;
-        const int row = pre ? p0 + i * kKeys : q0 + (i - nt_pre) * kKeys;
-        const CUtensorMap *mk = pre ? &maps.k_pre : &maps.k_new;
-        const CUtensorMap *mv = pre ? &maps.v_pre : &maps.v_new;
-        const uint32_t st = sbase + kOffStage + s * kStageBytes;
-        mbar_arrive_expect_tx(&full[s], kStageBytes);
-        tma_load_3d(st, mk, 0, kv, row, &full[s]);
-        tma_load_3d(st + kKVBlock, mk, 64, kv, row, &full[s]);
-        tma_load_3d(st + kKVTile, mv, 0, kv, row, &full[s]);
-        tma_load_3d(st + kKVTile + kKVBlock, mv, 64, kv, row, &full[s]);
-    };
     asm volatile("cp.async.commit_group;" ::: "memory");
-    for (int idx = tid; idx < kOnesBytes / 16; idx += kEThreads) {  // BF16 1.0 everywhere
-        const uint32_t one2 = 0x3f803f80u;
-        *reinterpret_cast<uint4 *>(smem + kOffOnes + idx * 16) = make_uint4(one2, one2, one2, one2);
-    }
+    // K (or V) of tile j into slot s: two TMA boxes (head_dim 0..63 and
+    // 64..127) of 128 rows; rows past the tensor are zero-filled, rows of a
+    // neighbouring request are masked by the softmax
+    auto tile_row = [&](int j) { return j < nt_pre ? p0 + j * kKeys : q0 + (j - nt_pre) * kKeys; };
+    auto load_k = [&](int j, int s) {
+        const CUtensorMap *m = j < nt_pre ? &maps.k_pre : &maps.k_new;
+        const uint32_t dst = sbase + kOffK + s * kKVTile;
+        mbar_arrive_expect_tx(&k_full[s], kKVTile);
+        tma_load_3d(dst, m, 0, kv, tile_row(j), &k_full[s]);
+        tma_load_3d(dst + kKVBlock, m, 64, kv, tile_row(j), &k_full[s]);
+    };
+    auto load_v = [&](int j, int s) {
+        const CUtensorMap *m = j < nt_pre ? &maps.v_pre : &maps.v_new;
+        const uint32_t dst = sbase + kOffV + s * kKVTile;
+        mbar_arrive_expect_tx(&v_full[s], kKVTile);
+        tma_load_3d(dst, m, 0, kv, tile_row(j), &v_full[s]);
+        tma_load_3d(dst + kKVBlock, m, 64, kv, tile_row(j), &v_full[s]);
+    };
 
     if (warp == 0) tc_alloc(&tmem_base, kTmemCols);
-    if (tid == 0) {
-        mbar_init(&bar_mma, 1);
-        mbar_init(&full[0], 1);
-        mbar_init(&full[1], 1);
+    if (tid == kSoftThreads) {
+        for (int j = 0; j < kNumBars; j++) mbar_init(&bars[j], (j == 6 || j == 7) ? kQRows : 1);
+        *abort_flag = 0;
         fence_mbar_init();
-        issue(0, 0);
+        for (int j = 0; j < 2 && j < nt; j++) {
+            load_k(j, j);
+            load_v(j, j);
+        }
     }
     asm volatile("cp.async.wait_group 0;" ::: "memory");
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // Q and the ones tile for the tensor core
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // Q for the tensor core
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_base;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;  // this warp's TMEM lanes
 
-    // this thread's query row
-    const int R = row0 + tid;
-    const bool row_ok = R < rows;
-    const int token = row_ok ? R / a.G : 0;
-
-    constexpr uint32_t idesc_s = idesc_bf16_f32(128, kKeys, false);
-    constexpr uint32_t idesc_o = idesc_bf16_f32(128, kHeadDim, true);
-    constexpr uint32_t idesc_l = idesc_bf16_f32(128, 16, false);
-    const uint32_t sOnes = sbase + kOffOnes;
-    float m_run = kNegInfE;
-    uint32_t phase = 0;
-    bool aborted = false;
-
-    for (int i = 0; i < nt && !aborted; i++) {
-        const int s_cur = i & 1;
-        const uint32_t sK = sbase + kOffStage + s_cur * kStageBytes, sV = sK + kKVTile;
-        if (tid == 0 && mbar_wait_bounded(&full[s_cur], (uint32_t)((i >> 1) & 1), kWaitLimitE, nullptr)) {
-            tc_fence_after();
+    if (warp == kSoftThreads / 32) {
+        // ---------------- load / MMA thread
+        if (lane == 0) {
+            constexpr uint32_t idesc_s = idesc_bf16_f32(128, kKeys, false);
+            constexpr uint32_t idesc_o = idesc_bf16_f32(128, kHeadDim, true);
+            auto mma_s = [&](int w, int s) {  // S_w = Q_w K(slot s)^T over head_dim, 16 at a time
+                const uint32_t sQ = sbase + kOffQ + w * kQBytes, sK = sbase + kOffK + s * kKVTile;
 #pragma unroll
-            for (int kk = 0; kk < 8; kk++) {  // S = Q K^T over head_dim, 16 at a time
-                const uint32_t blk = (uint32_t)(kk >> 2), sub = (uint32_t)(kk & 3) * 32;
-                tc_mma_bf16(tmem, smem_desc_sw128(sQ + blk * (kQRows * 128) + sub, 16, 1024),
-                            smem_desc_sw128(sK + blk * kKVBlock + sub, 16, 1024), idesc_s, kk > 0);
-            }
-            tc_commit(&bar_mma);
-        }
-        // S of this tile (and every earlier MMA) done: the other stage and P are free
-        const bool ok = mbar_wait_bounded(&bar_mma, phase, kWaitLimitE, nullptr);
-        if (__syncthreads_or(!ok)) {  // all threads take the same decision
-            if (tid == 0) flag_error(a.err, kErrTimeout);
-            aborted = true;
-            break;
-        }
-        phase ^= 1u;
-        tc_fence_after();
-        if (tid == 0 && i + 1 < nt) issue(i + 1, s_cur ^ 1);  // its stage held tile i - 1, now done
-
-        // ---- softmax of this thread's row (base 2; masked scores are -inf)
-        uint32_t sr[2][32];
-        tc_ld32(tmem + lane_base + 0, sr[0]);
-        tc_ld32(tmem + lane_base + 32, sr[1]);
-        tc_wait_ld();
-        float sc[64];
-#pragma unroll
-        for (int j = 0; j < 64; j++) sc[j] = __uint_as_float(sr[j >> 5][j & 31]);
-        {
-            const bool pre = i < nt_pre;
-            const int base = pre ? i * kKeys : (i - nt_pre) * kKeys;
-            const int visible = (pre ? np : token + 1) - base;  // keys [0, visible) of the tile are seen
-            if (__any_sync(0xffffffffu, visible < kKeys)) {     // an edge tile: mask
-#pragma unroll
-                for (int j = 0; j < 64; j++)
-                    if (j >= visible) sc[j] = kNegInfE;
-            }
-        }
-        float smax = sc[0];
-#pragma unroll
-        for (int j = 1; j < 64; j++) smax = fmaxf(smax, sc[j]);
-        const float mx = smax * a.score_log2;  // the scale is positive
-        const bool need = mx > m_run + kRescale;
-        if (__any_sync(0xffffffffu, need)) {
-            const float m_new = need ? fmaxf(m_run, mx) : m_run;
-            const float alpha = need ? (m_run == kNegInfE ? 0.f : ex2(m_run - m_new)) : 1.f;
-            if (i > 0) {  // O and the row sums hold earlier tiles: rescale this warp's rows in TMEM
-#pragma unroll
-                for (int cblk = 0; cblk < 5; cblk++) {  // O (4 x 32 columns), then the sums
-                    uint32_t ov[32];
-                    const uint32_t col = cblk < 4 ? kColO + 32 * cblk : kColL;
-                    tc_ld32(tmem + lane_base + col, ov);
-                    tc_wait_ld();
-#pragma unroll
-                    for (int j = 0; j < 32; j++) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * alpha);
-                    tc_st32(tmem + lane_base + col, ov);
+                for (int kk = 0; kk < 8; kk++) {
+                    const uint32_t blk = (uint32_t)(kk >> 2), sub = (uint32_t)(kk & 3) * 32;
+                    tc_mma_bf16(tmem + 128u * w, smem_desc_sw128(sQ + blk * (kQRows * 128) + sub, 16, 1024),
+                                smem_desc_sw128(sK + blk * kKVBlock + sub, 16, 1024), idesc_s, kk > 0);
                 }
-                tc_wait_st();
-            }
-            m_run = m_new;
-        }
-        // P row = 2^(s * scale - m), rounded to BF16, into this lane's P columns of TMEM
-        const float neg_m = -m_run;
-        uint32_t pw[32];
+                tc_commit(&s_done[w]);
+            };
+            auto mma_pv = [&](int w, int j, int s) {  // O_w += P_w V(slot s) over the tile's 128 keys
+                const uint32_t sV = sbase + kOffV + s * kKVTile;
 #pragma unroll
-        for (int c = 0; c < 32; c++) {
-            const __nv_bfloat162 pr =
-                __floats2bfloat162_rn(ex2(fmaf(sc[2 * c], a.score_log2, neg_m)), ex2(fmaf(sc[2 * c + 1], a.score_log2, neg_m)));
-            pw[c] = *reinterpret_cast<const uint32_t *>(&pr);
-        }
-        tc_st32(tmem + lane_base + kColP, pw);
-        tc_wait_st();
-        tc_fence_before();
-        __syncthreads();
-        if (tid == 0) {
-            tc_fence_after();
+                for (int kk = 0; kk < 8; kk++)  // P from TMEM: 8 columns = 16 keys
+                    tc_mma_bf16_tmem_a(tmem + kColO + 128u * w, tmem + 128u * w + kk * 8,
+                                       smem_desc_sw128(sV + kk * 16 * 128, kKVBlock, 1024), idesc_o,
+                                       (j > 0 || kk > 0) ? 1u : 0u);
+                tc_commit(&pv_done[w]);
+            };
+            // Issue whatever is ready, for either query tile, so that the tensor core
+            // always holds the next product of one tile while the other's softmax runs:
+            //   S_w(t) once K(t) has landed and O_w += P_w(t - 1) V(t - 1) is complete;
+            //   O_w += P_w(t) V(t) once P_w(t) is stored and V(t) has landed;
+            //   K(t) into slot t % 2 once both S(t - 2) are done (their P V issued);
+            //   V(t) into slot t % 2 once both P(t - 2) V(t - 2) are complete.
+            // Each barrier is polled only where it cannot be two phases ahead.
+            int tw[kWGs] = {0, 0};                 // next tile of query tile w
+            bool at_pv[kWGs] = {false, false};     // its next product is P V (else S)
+            int pv_seen[kWGs] = {0, 0};            // its P V of tiles < pv_seen are known complete
+            int k_next = nt > 1 ? 2 : 1, v_next = k_next;  // next K / V tiles to request
+            bool ok = true;
+            uint32_t idle = 0;
+            for (;;) {
+                bool progress = false, finished = true;
 #pragma unroll
-            for (int kk = 0; kk < 4; kk++) {  // O += P V over this tile's 64 keys; sums += P 1
-                const uint32_t pa = tmem + kColP + kk * 8;  // P from TMEM: 8 columns = 16 keys
-                const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
-                tc_mma_bf16_tmem_a(tmem + kColO, pa, smem_desc_sw128(sV + kk * 16 * 128, kKVBlock, 1024), idesc_o,
-                                   acc);
-                tc_mma_bf16_tmem_a(tmem + kColL, pa, smem_desc_sw128(sOnes + kk * 32, 16, 1024), idesc_l, acc);
-            }
-        }
-    }
-    if (!aborted) {
-        if (tid == 0) tc_commit(&bar_mma);
-        const bool ok = mbar_wait_bounded(&bar_mma, phase, kWaitLimitE, nullptr);
-        if (__syncthreads_or(!ok)) {
-            if (tid == 0) flag_error(a.err, kErrTimeout);
-            aborted = true;
-        }
-        tc_fence_after();
-    }
-    if (!aborted) {
-        // ---- O / l -> BF16 row of the output
-        uint32_t lv[32];
-        tc_ld32(tmem + lane_base + kColL, lv);
-        tc_wait_ld();
-        const float l_run = __uint_as_float(lv[0]);
-        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-        uint4 *dst = reinterpret_cast<uint4 *>(a.out + (((int64_t)q0 + token) * a.Hq + kv * a.G + R % a.G) * kHeadDim);
-#pragma unroll
-        for (int cblk = 0; cblk < 4; cblk++) {
-            uint32_t ov[32];
-            tc_ld32(tmem + lane_base + kColO + 32 * cblk, ov);
-            tc_wait_ld();
-            if (row_ok) {
-#pragma unroll
-                for (int q4 = 0; q4 < 4; q4++) {
-                    uint32_t w[4];
-#pragma unroll
-                    for (int e = 0; e < 4; e++) {
-                        const __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(ov[8 * q4 + 2 * e]) * inv,
-                                                                        __uint_as_float(ov[8 * q4 + 2 * e + 1]) * inv);
-                        w[e] = *reinterpret_cast<const uint32_t *>(&h);
+                for (int w = 0; w < kWGs; w++) {
+                    const int t = tw[w];
+                    if (w >= nwg || t >= nt) continue;
+                    finished = false;
+                    if (!at_pv[w]) {
+                        if (t > 0 && pv_seen[w] < t) {
+                            if (!mbar_test_wait(&pv_done[w], (uint32_t)((t - 1) & 1))) continue;
+                            pv_seen[w] = t;
+                        }
+                        if (!mbar_test_wait(&k_full[t & 1], (uint32_t)((t >> 1) & 1))) continue;
+                        tc_fence_after();
+                        mma_s(w, t & 1);
+                        at_pv[w] = true;
+                    } else {
+                        if (!mbar_test_wait(&p_full[w], (uint32_t)(t & 1))) continue;
+                        if (!mbar_test_wait(&v_full[t & 1], (uint32_t)((t >> 1) & 1))) continue;
+                        tc_fence_after();
+                        mma_pv(w, t, t & 1);
+                        at_pv[w] = false;
+                        tw[w] = t + 1;
                     }
-                    dst[4 * cblk + q4] = make_uint4(w[0], w[1], w[2], w[3]);
+                    progress = true;
+                }
+                if (finished) break;
+                int min_tw = tw[0], min_seen = pv_seen[0];
+                if (nwg > 1) {
+                    min_tw = min(min_tw, tw[1]);
+                    min_seen = min(min_seen, pv_seen[1]);
+                }
+                if (k_next < nt && min_tw >= k_next - 1) {
+                    load_k(k_next, k_next & 1);
+                    k_next++;
+                    progress = true;
+                }
+                if (v_next < nt && min_seen >= v_next - 1) {
+                    load_v(v_next, v_next & 1);
+                    v_next++;
+                    progress = true;
+                }
+                if (progress) {
+                    idle = 0;
+                } else {
+                    if (++idle > kWaitLimitE || *abort_flag) {
+                        ok = false;
+                        break;
+                    }
+                    __nanosleep(20);  // leave the issue slots to the softmax warps
+                }
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                flag_error(a.err, kErrTimeout);
+                // no copy or MMA may still be running when the CTA frees its memory
+                for (int t = max(0, k_next - 2); t < k_next; t++)
+                    mbar_wait_bounded(&k_full[t & 1], (uint32_t)((t >> 1) & 1), kWaitLimitE, nullptr);
+                for (int t = max(0, v_next - 2); t < v_next; t++)
+                    mbar_wait_bounded(&v_full[t & 1], (uint32_t)((t >> 1) & 1), kWaitLimitE, nullptr);
+                tc_commit(drain);
+                mbar_wait_bounded(drain, 0, kWaitLimitE, nullptr);
+            }
+        }
+        __syncwarp();
+    } else if ((tid >> 7) < nwg) {
+        // ---------------- softmax of this thread's query row
+        const int w = tid >> 7;
+        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;  // this warp's TMEM lanes
+        const uint32_t colS = 128u * w, colO = kColO + 128u * w;
+        const int R = row0 + w * kQRows + (tid & 127);
+        const bool row_ok = R < rows;
+        const int token = row_ok ? R / a.G : 0;
+        float m_run = kNegInfE, l_run = 0.f;
+        bool ok = true;
+        for (int j = 0; j < nt; j++) {
+            // S_w(j) done; its commit also covers O_w += P_w(j - 1) V(j - 1)
+            ok = __all_sync(0xffffffffu, mbar_wait_bounded(&s_done[w], (uint32_t)(j & 1), kWaitLimitE, abort_flag));
+            if (!ok) break;
+            tc_fence_after();
+            const bool pre = j < nt_pre;
+            const int base = pre ? j * kKeys : (j - nt_pre) * kKeys;
+            const int visible = (pre ? np : token + 1) - base;   // keys [0, visible) of the tile are seen
+            const bool edge = __any_sync(0xffffffffu, visible < kKeys);  // mask on edge tiles only
+            // the row's 64 scores of half h (masked scores are -inf)
+            auto load_half = [&](int h, float (&sc)[64]) {
+                uint32_t sr[2][32];
+                tc_ld32(tmem + lane_base + colS + 64 * h, sr[0]);
+                tc_ld32(tmem + lane_base + colS + 64 * h + 32, sr[1]);
+                tc_wait_ld();
+#pragma unroll
+                for (int c = 0; c < 64; c++) sc[c] = __uint_as_float(sr[c >> 5][c & 31]);
+                if (edge) {
+#pragma unroll
+                    for (int c = 0; c < 64; c++)
+                        if (64 * h + c >= visible) sc[c] = kNegInfE;
+                }
+            };
+            // P = 2^(s * scale - m) of one half, rounded to BF16 pairs; ls += the rounded values
+            auto make_p = [&](const float (&sc)[64], float neg_m, uint32_t (&pw)[32], float2 (&ls)[2]) {
+#pragma unroll
+                for (int c = 0; c < 32; c++) {
+                    const __nv_bfloat162 pr = __floats2bfloat162_rn(ex2(fmaf(sc[2 * c], a.score_log2, neg_m)),
+                                                                    ex2(fmaf(sc[2 * c + 1], a.score_log2, neg_m)));
+                    pw[c] = *reinterpret_cast<const uint32_t *>(&pr);
+                    ls[c & 1] = add2(ls[c & 1], make_float2(__uint_as_float(pw[c] << 16),
+                                                            __uint_as_float(pw[c] & 0xffff0000u)));
+                }
+            };
+            auto half_max = [&](const float (&sc)[64]) {
+                float m8[8];
+#pragma unroll
+                for (int e = 0; e < 8; e++) m8[e] = max3(sc[e], sc[8 + e], sc[16 + e]);
+#pragma unroll
+                for (int e = 0; e < 8; e++) m8[e] = max3(m8[e], sc[24 + e], sc[32 + e]);
+#pragma unroll
+                for (int e = 0; e < 8; e++) m8[e] = max3(m8[e], sc[40 + e], sc[48 + e]);
+#pragma unroll
+                for (int e = 0; e < 8; e++) m8[e] = fmaxf(m8[e], sc[56 + e]);
+                return max3(max3(m8[0], m8[1], m8[2]), max3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
+            };
+            // One pass with the running max as it stands (the lazy rescale lets it
+            // lag the true max by up to 2^8): P of half 0 stays in registers until
+            // half 1 shows whether the max must move; only then does it go over the
+            // scores in TMEM.  If it must (the first tile, rarely later), O and the
+            // row sum are rescaled and P is formed again from the scores in TMEM.
+            uint32_t pw0[32], pw1[32];
+            float2 ls[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+            float smax;
+            {
+                float sc[64];
+                load_half(0, sc);
+                smax = half_max(sc);
+                make_p(sc, -m_run, pw0, ls);
+                load_half(1, sc);
+                smax = fmaxf(smax, half_max(sc));
+                const float mx = smax * a.score_log2;  // the scale is positive
+                const bool need = mx > m_run + kRescale;
+                if (!__any_sync(0xffffffffu, need)) {
+                    make_p(sc, -m_run, pw1, ls);
+                } else {
+                    const float m_new = need ? fmaxf(m_run, mx) : m_run;
+                    const float alpha = need ? (m_run == kNegInfE ? 0.f : ex2(m_run - m_new)) : 1.f;
+                    if (j > 0) {  // O_w holds tiles 0 .. j - 1 (complete): rescale this warp's rows
+#pragma unroll
+                        for (int cblk = 0; cblk < 4; cblk++) {
+                            uint32_t ov[32];
+                            tc_ld32(tmem + lane_base + colO + 32 * cblk, ov);
+                            tc_wait_ld();
+#pragma unroll
+                            for (int e = 0; e < 32; e++) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+                            tc_st32(tmem + lane_base + colO + 32 * cblk, ov);
+                        }
+                        tc_wait_st();
+                    }
+                    l_run *= alpha;
+                    m_run = m_new;
+                    ls[0] = ls[1] = make_float2(0.f, 0.f);
+                    make_p(sc, -m_run, pw1, ls);
+                    load_half(0, sc);
+                    make_p(sc, -m_run, pw0, ls);
+                }
+            }
+            l_run += (ls[0].x + ls[0].y) + (ls[1].x + ls[1].y);
+            tc_st32(tmem + lane_base + colS, pw0);       // over scores 0 .. 31 (read already)
+            tc_st32(tmem + lane_base + colS + 32, pw1);  // over scores 32 .. 63
+            tc_wait_st();
+            tc_fence_before();
+            mbar_arrive(&p_full[w]);
+        }
+        // O_w is complete after O_w += P_w(nt - 1) V(nt - 1); the previous one is
+        // done already (S_w(nt - 1) waited for it), so one parity wait suffices
+        if (ok)
+            ok = __all_sync(0xffffffffu,
+                            mbar_wait_bounded(&pv_done[w], (uint32_t)((nt - 1) & 1), kWaitLimitE, abort_flag));
+        if (!ok) {
+            *abort_flag = 1;
+            if (lane == 0) flag_error(a.err, kErrTimeout);
+        } else {
+            // ---- O / l -> BF16 row of the output
+            tc_fence_after();
+            const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+            uint4 *dst =
+                reinterpret_cast<uint4 *>(a.out + (((int64_t)q0 + token) * a.Hq + kv * a.G + R % a.G) * kHeadDim);
+#pragma unroll
+            for (int cblk = 0; cblk < 4; cblk++) {
+                uint32_t ov[32];
+                tc_ld32(tmem + lane_base + colO + 32 * cblk, ov);
+                tc_wait_ld();
+                if (row_ok) {
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; q4++) {
+                        uint32_t wv[4];
+#pragma unroll
+                        for (int e = 0; e < 4; e++) {
+                            const __nv_bfloat162 hv = __floats2bfloat162_rn(
+                                __uint_as_float(ov[8 * q4 + 2 * e]) * inv, __uint_as_float(ov[8 * q4 + 2 * e + 1]) * inv);
+                            wv[e] = *reinterpret_cast<const uint32_t *>(&hv);
+                        }
+                        dst[4 * cblk + q4] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+                    }
                 }
             }
         }
@@ -350,7 +487,7 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// [rows][Hkv][128] BF16 at `base` as a 3-D map with 64 x 1 x 64 boxes.
+// [rows][Hkv][128] BF16 at `base` as a 3-D map with 64 x 1 x 128 boxes.
 bool make_kv_map(CUtensorMap *map, const void *base, int64_t rows, int Hkv) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
@@ -397,7 +534,7 @@ cudaError_t launch_extend(const void *q, const void *k_prefix, const void *v_pre
     a.score_log2 = (float)((double)sm_scale * 1.4426950408889634);
     a.out = static_cast<uint16_t *>(out);
     a.err = err;
-    const int64_t qtiles = ceil_div64((int64_t)max_q_len * a.G, kQRows);
+    const int64_t qtiles = ceil_div64((int64_t)max_q_len * a.G, kCtaRows);
     dim3 grid((unsigned)qtiles, (unsigned)num_kv_heads, (unsigned)num_reqs);
     extend_kernel<<<grid, kEThreads, kESmem, stream>>>(maps, a);
     return cudaGetLastError();

@@ -1,5 +1,6 @@
 """Extend attention (section A2, path 2) on the GPU against the fp64 oracle:
-ragged prefixes and chunks across tile boundaries, GQA groups 1-8, empty
+ragged prefixes and chunks across the 128-key tile and 256-row CTA
+boundaries, GQA groups 1-8, query tiles left empty, empty
 prefixes and chunks, and the whole path -- prefix dequantised from the NVFP4
 cache by prefix_dequant, then attended together with the chunk."""
 
@@ -50,6 +51,8 @@ def _case(m, prefix_lens, chunk_lens, Hq, Hkv, seed, max_q_len=None):
     ([300, 0, 129], [7, 70, 33], 40, 8),
     ([1000], [512], 32, 8),
     ([77, 5], [0, 130], 8, 1),
+    ([127, 256, 257, 0], [129, 64, 255, 1], 32, 8),
+    ([128, 383], [96, 33], 16, 2),
 ])
 def test_extend_matches_oracle(m, prefix_lens, chunk_lens, Hq, Hkv):
     out, ref = _case(m, prefix_lens, chunk_lens, Hq, Hkv, sum(prefix_lens) + sum(chunk_lens) + Hq)
