@@ -299,14 +299,11 @@ __global__ void __launch_bounds__(kEThreads, 1) extend_kernel(const __grid_const
                     v_next++;
                     progress = true;
                 }
-                if (progress) {
+                if (progress) {  // polls without sleeping: a sleep here lands on the critical path
                     idle = 0;
-                } else {
-                    if (++idle > kWaitLimitE || *abort_flag) {
-                        ok = false;
-                        break;
-                    }
-                    __nanosleep(20);  // leave the issue slots to the softmax warps
+                } else if (++idle > kWaitLimitE || *abort_flag) {
+                    ok = false;
+                    break;
                 }
             }
             if (!ok) {
