@@ -110,14 +110,24 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
     return d;
 }
 
-// (a.x + b.x, a.y + b.y) in one instruction
-__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+// (a.x * b + c, a.y * b + c) in one instruction
+__device__ __forceinline__ float2 fma2(float2 a, float b, float c) {
     uint64_t d;
-    asm("add.rn.f32x2 %0, %1, %2;"
+    const uint64_t bb = (uint64_t)__float_as_uint(b) | ((uint64_t)__float_as_uint(b) << 32);
+    const uint64_t cc = (uint64_t)__float_as_uint(c) | ((uint64_t)__float_as_uint(c) << 32);
+    asm("fma.rn.f32x2 %0, %1, %2, %3;"
         : "=l"(d)
-        : "l"((uint64_t)__float_as_uint(a.x) | ((uint64_t)__float_as_uint(a.y) << 32)),
-          "l"((uint64_t)__float_as_uint(b.x) | ((uint64_t)__float_as_uint(b.y) << 32)));
+        : "l"((uint64_t)__float_as_uint(a.x) | ((uint64_t)__float_as_uint(a.y) << 32)), "l"(bb), "l"(cc));
     return make_float2(__uint_as_float((uint32_t)d), __uint_as_float((uint32_t)(d >> 32)));
+}
+
+// s0 += low BF16 of w, s1 += high BF16 of w (exact products by 1.0, FP32 sums)
+__device__ __forceinline__ void add_bf16x2(float &s0, float &s1, uint32_t w) {
+    const unsigned short one = 0x3f80;
+    asm("{ .reg .b16 lo, hi; mov.b32 {lo, hi}, %2;\n"
+        "fma.rn.f32.bf16 %0, lo, %3, %0; fma.rn.f32.bf16 %1, hi, %3, %1; }"
+        : "+f"(s0), "+f"(s1)
+        : "r"(w), "h"(one));
 }
 
 __global__ void __launch_bounds__(kEThreads, 1) extend_kernel(const __grid_constant__ ExtendMaps maps, ExtendArgs a) {
@@ -353,14 +363,13 @@ __global__ void __launch_bounds__(kEThreads, 1) extend_kernel(const __grid_const
                 }
             };
             // P = 2^(s * scale - m) of one half, rounded to BF16 pairs; ls += the rounded values
-            auto make_p = [&](const float (&sc)[64], float neg_m, uint32_t (&pw)[32], float2 (&ls)[2]) {
+            auto make_p = [&](const float (&sc)[64], float neg_m, uint32_t (&pw)[32], float (&ls)[4]) {
 #pragma unroll
                 for (int c = 0; c < 32; c++) {
-                    const __nv_bfloat162 pr = __floats2bfloat162_rn(ex2(fmaf(sc[2 * c], a.score_log2, neg_m)),
-                                                                    ex2(fmaf(sc[2 * c + 1], a.score_log2, neg_m)));
+                    const float2 e = fma2(make_float2(sc[2 * c], sc[2 * c + 1]), a.score_log2, neg_m);
+                    const __nv_bfloat162 pr = __floats2bfloat162_rn(ex2(e.x), ex2(e.y));
                     pw[c] = *reinterpret_cast<const uint32_t *>(&pr);
-                    ls[c & 1] = add2(ls[c & 1], make_float2(__uint_as_float(pw[c] << 16),
-                                                            __uint_as_float(pw[c] & 0xffff0000u)));
+                    add_bf16x2(ls[2 * (c & 1)], ls[2 * (c & 1) + 1], pw[c]);
                 }
             };
             auto half_max = [&](const float (&sc)[64]) {
@@ -381,7 +390,7 @@ __global__ void __launch_bounds__(kEThreads, 1) extend_kernel(const __grid_const
             // scores in TMEM.  If it must (the first tile, rarely later), O and the
             // row sum are rescaled and P is formed again from the scores in TMEM.
             uint32_t pw0[32], pw1[32];
-            float2 ls[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+            float ls[4] = {0.f, 0.f, 0.f, 0.f};
             float smax;
             {
                 float sc[64];
@@ -411,13 +420,13 @@ __global__ void __launch_bounds__(kEThreads, 1) extend_kernel(const __grid_const
                     }
                     l_run *= alpha;
                     m_run = m_new;
-                    ls[0] = ls[1] = make_float2(0.f, 0.f);
+                    ls[0] = ls[1] = ls[2] = ls[3] = 0.f;
                     make_p(sc, -m_run, pw1, ls);
                     load_half(0, sc);
                     make_p(sc, -m_run, pw0, ls);
                 }
             }
-            l_run += (ls[0].x + ls[0].y) + (ls[1].x + ls[1].y);
+            l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
             tc_st32(tmem + lane_base + colS, pw0);       // over scores 0 .. 31 (read already)
             tc_st32(tmem + lane_base + colS + 32, pw1);  // over scores 32 .. 63
             tc_wait_st();
