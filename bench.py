@@ -512,7 +512,7 @@ def run_ours(args):
     out = torch.empty_like(q)
     stream = torch.cuda.current_stream()
 
-    def step():   # one launch sequence: plan, decode with the new token appended in-kernel, reduce
+    def step():   # one call: plan, decode with the new token appended in-kernel (and the reduction, or a reduction kernel)
         m.paged_decode_attention_append(cache, new_k, new_v, q, bt, sl, w.sm_scale, out=out, workspace=ws,
                                         num_splits=args.num_splits)
 
@@ -619,7 +619,7 @@ def run_ours(args):
         "algorithmic_bytes_per_step": step_bytes,
         "e2e": {"value": world * step_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-        "gpu_launches": 3 * K,
+        "gpu_launches": m.decode_launch_count(cache, B, Hq, args.num_splits) * K,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic, "peak_kind": peak_kind,
                      "kernel": "decode_kernel<nvfp4>", "us_per_launch": dec_us,

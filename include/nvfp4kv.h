@@ -156,6 +156,14 @@ NVFP4KV_API size_t nvfp4kv_decode_workspace_bytes(const nvfp4kv_cache *cache, in
  * current device for this cache. */
 NVFP4KV_API int nvfp4kv_decode_auto_splits(const nvfp4kv_cache *cache, int num_q_heads);
 
+/* Kernel launches one nvfp4_paged_decode_attention (shared_len = 0) or
+ * nvfp4_cascade_decode_attention (shared_len > 0) call of this shape makes:
+ * the plan, the decode kernel and the log-sum-exp reduction, plus the
+ * shared-prefix kernel for a cascade call; the fused append variant makes as
+ * many.  0 if the arguments are invalid (or batch = 0: nothing is launched). */
+NVFP4KV_API int nvfp4kv_decode_launch_count(const nvfp4kv_cache *cache, int batch, int num_q_heads, int num_splits,
+                                            int shared_len);
+
 /*
  * Paged GQA decode attention over the cache, one query token per sequence.
  * Source: section A2, path 3 and Fig. 3 (packed K/V tiles and block scales

@@ -61,6 +61,7 @@ def _load_library():
         "nvfp4_kv_quantize_append": (i32, [D, P, P, i64, i64, P, P]),
         "nvfp4kv_decode_workspace_bytes": (sz, [D, i32, i32, i32]),
         "nvfp4kv_decode_auto_splits": (i32, [D, i32]),
+        "nvfp4kv_decode_launch_count": (i32, [D, i32, i32, i32, i32]),
         "nvfp4_paged_decode_attention": (i32, [D, P, i32, i32, P, i32, P, f32, P, P, sz, i32, P]),
         "nvfp4_prefix_dequant": (i32, [D, P, i32, P, P, i32, i64, P, P, P]),
         "nvfp4kv_check_device_errors": (i32, [P]),
@@ -84,6 +85,7 @@ _lib = _load_library()
 
 EXPORTED_SYMBOLS = ("nvfp4kv_version", "nvfp4kv_status_string", "nvfp4kv_slab_bytes", "nvfp4kv_pool_bytes",
                     "nvfp4_kv_quantize_append", "nvfp4kv_decode_workspace_bytes", "nvfp4kv_decode_auto_splits",
+                    "nvfp4kv_decode_launch_count",
                     "nvfp4_paged_decode_attention", "nvfp4_prefix_dequant", "nvfp4kv_check_device_errors",
                     "nvfp4kv_profile_decode", "nvfp4_paged_decode_attention_noalloc",
                     "nvfp4kv_selftest_bounded_wait", "nvfp4kv_calibrate_global_scales", "nvfp4_extend_attention",
@@ -212,6 +214,13 @@ def decode_workspace_bytes(cache: PagedCache, batch: int, num_q_heads: int, num_
 
 def decode_auto_splits(cache: PagedCache, num_q_heads: int) -> int:
     return int(_lib.nvfp4kv_decode_auto_splits(cache.desc, int(num_q_heads)))
+
+
+def decode_launch_count(cache: PagedCache, batch: int, num_q_heads: int, num_splits: int = 0,
+                        shared_len: int = 0) -> int:
+    """Kernel launches of one decode (shared_len = 0) or cascade call of this shape."""
+    return int(_lib.nvfp4kv_decode_launch_count(cache.desc, int(batch), int(num_q_heads), int(num_splits),
+                                                int(shared_len)))
 
 
 def alloc_decode_workspace(cache: PagedCache, batch: int, num_q_heads: int, num_splits: int = 0) -> torch.Tensor:

@@ -215,6 +215,14 @@ int nvfp4kv_decode_auto_splits(const nvfp4kv_cache *cache, int num_q_heads) {
     return decode_auto_grid(*cache, G, nullptr);
 }
 
+int nvfp4kv_decode_launch_count(const nvfp4kv_cache *cache, int batch, int num_q_heads, int num_splits,
+                                int shared_len) {
+    if (check_cache(cache) || batch < 1 || num_q_heads < 1 || num_q_heads % cache->num_kv_heads || num_splits < 0 ||
+        shared_len < 0 || num_q_heads / cache->num_kv_heads > 16)
+        return 0;
+    return shared_len > 0 ? 4 : 3;  // plan, (shared prefix,) decode, reduction
+}
+
 size_t nvfp4kv_decode_workspace_bytes(const nvfp4kv_cache *cache, int batch, int num_q_heads, int num_splits) {
     if (check_cache(cache) || batch < 0 || num_q_heads < 1 || num_q_heads % cache->num_kv_heads || num_splits < 0)
         return 0;
