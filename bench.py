@@ -55,7 +55,7 @@ def parse_args():
     p.add_argument("--num-splits", type=int, default=0)
     p.add_argument("--batch", type=int, default=64,
                    help="sequences of the 32K workload (64 = the benchmark; smaller = a profiling case)")
-    p.add_argument("--comparison", choices=["extend", "agent_decode"], default=None,
+    p.add_argument("--comparison", choices=["extend", "agent_decode", "append", "calibrate"], default=None,
                    help="run only this comparison (its own JSON line; a profiling case) and exit")
     return p.parse_args()
 
@@ -665,6 +665,10 @@ def run_comparison(args):
     torch.cuda.set_device(device)
     if args.comparison == "extend":
         res = time_extend(m, device, args.steps, args.warmup, load_bf16_peak())
+    elif args.comparison == "append":
+        res = time_append(m, device, args.steps, args.warmup)
+    elif args.comparison == "calibrate":
+        res = time_calibrate(m, device, args.steps, args.warmup)
     else:
         res = time_agent_decode(m, device, args.steps, args.warmup)
     print(json.dumps({"comparison": args.comparison, **res}), flush=True)

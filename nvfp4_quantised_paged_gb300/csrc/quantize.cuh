@@ -21,6 +21,34 @@ __device__ __forceinline__ float snap13(float y) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
+__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// (a.x * b, a.y * b), each rounded to nearest, in one instruction
+__device__ __forceinline__ float2 mul2(float2 a, float b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;"
+        : "=l"(d)
+        : "l"((uint64_t)__float_as_uint(a.x) | ((uint64_t)__float_as_uint(a.y) << 32)),
+          "l"((uint64_t)__float_as_uint(b) | ((uint64_t)__float_as_uint(b) << 32)));
+    return make_float2(__uint_as_float((uint32_t)d), __uint_as_float((uint32_t)(d >> 32)));
+}
+
+// Approximate reciprocal (the hardware's, at most one unit in the last place off).
+__device__ __forceinline__ float rcp_approx(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// fl32(1/6).  For every non-negative BF16 amax, E4M3(fl32(amax * kOneSixth))
+// equals E4M3(fl32(amax / 6)) (checked over all of them on the host), so the
+// unit-scale path multiplies where the scale decision is defined by a division.
+constexpr float kOneSixth = 0.16666667163372039794921875f;
+
 template <bool kUnitScale>
 __device__ __forceinline__ void quantize_block16(const uint4 &a, const uint4 &b, float g, uint2 &codes,
                                                  uint32_t &scale_byte) {
@@ -28,10 +56,10 @@ __device__ __forceinline__ void quantize_block16(const uint4 &a, const uint4 &b,
     // amax over BF16 magnitudes: unsigned order of |bf16| bit patterns is numeric order
     uint32_t m = 0;
 #pragma unroll
-    for (int i = 0; i < 8; i++) m = __vmaxu2(m, w[i] & 0x7fff7fffu);
+    for (int i = 0; i < 8; i++) m = max_u16x2(m, w[i] & 0x7fff7fffu);
     const uint32_t amax_bits = (m >> 16) > (m & 0xffffu) ? (m >> 16) : (m & 0xffffu);
     const float amax = __uint_as_float(amax_bits << 16);
-    const float q = kUnitScale ? __fdiv_rn(amax, 6.0f) : __fdiv_rn(amax, __fmul_rn(6.0f, g));
+    const float q = kUnitScale ? __fmul_rn(amax, kOneSixth) : __fdiv_rn(amax, __fmul_rn(6.0f, g));
     const uint32_t s = f32x2_to_e4m3x2(0.0f, q) & 0xffu;
     scale_byte = s;
     const float sd = __half2float(__ushort_as_half((uint16_t)(e4m3x2_to_f16x2(s) & 0xffffu)));
@@ -45,12 +73,11 @@ __device__ __forceinline__ void quantize_block16(const uint4 &a, const uint4 &b,
             packed[i / 4] |= byte << (8 * (i % 4));
         }
     } else if (kUnitScale) {
-        const float r = __frcp_rn(sd);
+        const float r = rcp_approx(sd);
 #pragma unroll
         for (int i = 0; i < 8; i++) {
-            const float lo = snap13(bf16_lo(w[i]) * r);
-            const float hi = snap13(bf16_hi(w[i]) * r);
-            packed[i / 4] |= f32x2_to_e2m1x2(hi, lo) << (8 * (i % 4));
+            const float2 y = mul2(make_float2(bf16_lo(w[i]), bf16_hi(w[i])), r);
+            packed[i / 4] |= f32x2_to_e2m1x2(snap13(y.y), snap13(y.x)) << (8 * (i % 4));
         }
     } else {
         const float d = __fmul_rn(sd, g);

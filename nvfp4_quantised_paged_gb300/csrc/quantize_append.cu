@@ -16,14 +16,18 @@
 //   scale = cvt.rn.satfinite.e4m3 (q)            nearest-even, saturating
 //   y_i   = x_i / (scale g)                      see below
 //   code  = cvt.rn.satfinite.e2m1 (y_i)          nearest-even, saturating
-// For g = 1 the kernel forms y_i as x_i * rcp(scale) and then rounds y_i to 13
-// significant bits.  x_i has at most 8 significant bits and the scale at most
-// 4, so every exact quotient that is not exactly an E2M1 rounding midpoint lies
-// more than 2^-8 (relative) away from every midpoint, far outside the 2^-23
-// error of the reciprocal product; an exact midpoint has at most 3 significant
-// bits and the 13-bit rounding lands on it exactly.  Hence the codes equal
-// those of the exactly rounded quotient (the GPU tests check every BF16 value
-// against every scale).  For g != 1 the kernel divides with IEEE division.
+// For g = 1 the kernel forms q as amax * fl32(1/6): the FP32 results differ
+// from the quotient for some amax, but the E4M3 scale never does (all 32,640
+// finite non-negative BF16 values checked on the host).  It forms y_i as
+// x_i * rcp(scale) with the hardware's approximate reciprocal and then rounds
+// y_i to 13 significant bits.  x_i has at most 8 significant bits and the
+// scale at most 4, so every exact quotient that is not exactly an E2M1
+// rounding midpoint lies more than 2^-8 (relative) away from every midpoint,
+// far outside the ~2^-22 error of the reciprocal product; an exact midpoint
+// has at most 3 significant bits and the 13-bit rounding lands on it exactly.
+// Hence the codes equal those of the exactly rounded quotient (the GPU tests
+// check every BF16 value against every scale).  For g != 1 the kernel divides
+// with IEEE division.
 #include "common.cuh"
 #include "kernels.h"
 #include "quantize.cuh"
@@ -38,6 +42,7 @@ struct AppendArgs {
     int P;
     int log2P;
     int Hkv;
+    int log2Hkv;        // log2(Hkv) when Hkv is a power of two, else -1
     int64_t slab;       // bytes per (page, kv_head)
     const uint4 *k;     // BF16 rows viewed as 16-byte vectors
     const uint4 *v;
@@ -59,7 +64,7 @@ __global__ void __launch_bounds__(256) append_kernel(AppendArgs a) {
     const int blk = (int)(id & 7);
     const int which = (int)((id >> 3) & 1);
     const uint32_t th = id >> 4;
-    const uint32_t t32 = th / (uint32_t)a.Hkv;
+    const uint32_t t32 = a.log2Hkv >= 0 ? th >> a.log2Hkv : th / (uint32_t)a.Hkv;
     const int h = (int)(th - t32 * (uint32_t)a.Hkv);
     const int64_t t = t32;
     // the values and the slot are loaded together (both always in bounds)
@@ -87,6 +92,7 @@ cudaError_t launch_quantize_append(const nvfp4kv_cache &c, const void *k, const 
     a.P = c.page_size;
     a.log2P = __builtin_ctz((unsigned)c.page_size);
     a.Hkv = c.num_kv_heads;
+    a.log2Hkv = (c.num_kv_heads & (c.num_kv_heads - 1)) == 0 ? __builtin_ctz((unsigned)c.num_kv_heads) : -1;
     a.slab = (int64_t)(c.dtype == NVFP4KV_DTYPE_NVFP4 ? 144 : 256) * c.page_size;
     a.k = static_cast<const uint4 *>(k);
     a.v = static_cast<const uint4 *>(v);
