@@ -378,7 +378,8 @@ def extend_flops(prefix_lens, chunk, G, Hkv):
 def time_extend(m, device, steps, warmup, peak_tflops):
     """Path 2 on the agent mix's 8 extend requests: prefix dequant of their cached
     prefixes (NVFP4 pages -> BF16 workspace), then extend attention of each
-    512-token chunk over [prefix || chunk]."""
+    512-token chunk over [prefix || chunk]; and the same in one call with the
+    prefix expanded from the pages inside the kernel (paged_us)."""
     import torch
 
     import workloads
@@ -413,7 +414,11 @@ def time_extend(m, device, steps, warmup, peak_tflops):
     def dequant_only():
         m.prefix_dequant(cache, bt, pl_d, cu_p_d, total, k_ws=kw, v_ws=vw)
 
-    for key, fn in (("extend_us", lambda: run(False)), ("path2_us", lambda: run(True)), ("dequant_us", dequant_only)):
+    def paged():  # path 2 in one call: the prefix expanded from the NVFP4 pages inside the kernel
+        m.extend_attention_paged(cache, q, bt, pl_d, kn, vn, cu_q, L, w.sm_scale, out=out)
+
+    for key, fn in (("extend_us", lambda: run(False)), ("path2_us", lambda: run(True)), ("dequant_us", dequant_only),
+                    ("paged_us", paged)):
         for _ in range(warmup):
             fn()
         s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -429,6 +434,8 @@ def time_extend(m, device, steps, warmup, peak_tflops):
     res["dequant_gb_per_s"] = dq_bytes / res["dequant_us"] / 1e3
     res["dequant_algorithmic_bytes"] = dq_bytes
     flops = extend_flops([int(x) for x in pl], L, w.num_q_heads // w.num_kv_heads, w.num_kv_heads)
+    res.update({"paged_tflops": flops / res["paged_us"] / 1e6, "paged_over_path2_time": res["paged_us"] / res["path2_us"],
+                "workspace_bytes_saved": total * w.num_kv_heads * 2 * 2 * 128})
     res.update({"algorithmic_flops": flops, "extend_tflops": flops / res["extend_us"] / 1e6,
                 "extend_frac_of_bf16_peak": flops / res["extend_us"] / 1e6 / peak_tflops,
                 "bf16_peak_tflops": peak_tflops,

@@ -327,6 +327,30 @@ NVFP4KV_API int nvfp4_extend_attention(const void *q, const void *k_prefix, cons
                                        int64_t total_q_tokens, int num_reqs, int max_q_len, int num_q_heads,
                                        int num_kv_heads, float sm_scale, void *out, cudaStream_t stream);
 
+/*
+ * Extend attention with the prefix read straight from the NVFP4 cache: path 2
+ * of section A2 without the BF16 workspace.  Request r's prefix is tokens
+ * 0 .. prefix_lens[r] - 1 of its pages (row r of block_table); the kernel
+ * expands each 128-token tile of them to BF16 (e2m1 * e4m3 * g, rounded once,
+ * as nvfp4_prefix_dequant writes it) in shared memory and attends as
+ * nvfp4_extend_attention does, so the result equals nvfp4_prefix_dequant
+ * followed by nvfp4_extend_attention on the same data, bit for bit.
+ *
+ *   cache           the NVFP4 pool (an FP8 pool gives NVFP4KV_EUNSUPPORTED);
+ *                   num_kv_heads is the cache's.
+ *   block_table     device int32 [num_reqs][max_pages_per_seq].
+ *   prefix_lens     device int32 [num_reqs], 0 <= prefix_lens[r] <=
+ *                   max_pages_per_seq * P (a larger one is clamped and flagged;
+ *                   a page id outside the pool is flagged and read as zeros).
+ *   q, k_chunk, v_chunk, cu_q_lens, total_q_tokens, max_q_len, out, sm_scale
+ *                   as for nvfp4_extend_attention.
+ */
+NVFP4KV_API int nvfp4_extend_attention_paged(const nvfp4kv_cache *cache, const void *q, const int32_t *block_table,
+                                             int max_pages_per_seq, const int32_t *prefix_lens, const void *k_chunk,
+                                             const void *v_chunk, const int32_t *cu_q_lens, int64_t total_q_tokens,
+                                             int num_reqs, int max_q_len, int num_q_heads, float sm_scale, void *out,
+                                             cudaStream_t stream);
+
 /* Synchronises `stream`, then reads and clears the current device's error
  * word.  Returns NVFP4KV_OK, NVFP4KV_EDEVICE_CHECK (some kernel skipped an
  * out-of-range index since the last check) or NVFP4KV_ECUDA. */

@@ -68,6 +68,7 @@ def _load_library():
         "nvfp4kv_selftest_bounded_wait": (i32, [i32, ctypes.c_uint, P, P]),
         "nvfp4kv_calibrate_global_scales": (i32, [P, P, i64, i32, i64, P, P]),
         "nvfp4_extend_attention": (i32, [P, P, P, P, i64, P, P, P, i64, i32, i32, i32, i32, f32, P, P]),
+        "nvfp4_extend_attention_paged": (i32, [D, P, P, i32, P, P, P, P, i64, i32, i32, i32, f32, P, P]),
         "nvfp4_paged_decode_attention_append": (i32, [D, P, P, i64, P, i32, i32, P, i32, P, f32, P, P, sz, i32, P]),
         "nvfp4kv_cascade_workspace_bytes": (sz, [D, i32, i32, i32, i32]),
         "nvfp4_cascade_decode_attention": (i32, [D, P, i32, i32, P, i32, P, i32, P, f32, P, P, sz, i32, P]),
@@ -89,6 +90,7 @@ EXPORTED_SYMBOLS = ("nvfp4kv_version", "nvfp4kv_status_string", "nvfp4kv_slab_by
                     "nvfp4_paged_decode_attention", "nvfp4_prefix_dequant", "nvfp4kv_check_device_errors",
                     "nvfp4kv_profile_decode", "nvfp4_paged_decode_attention_noalloc",
                     "nvfp4kv_selftest_bounded_wait", "nvfp4kv_calibrate_global_scales", "nvfp4_extend_attention",
+                    "nvfp4_extend_attention_paged",
                     "nvfp4_paged_decode_attention_append", "nvfp4kv_cascade_workspace_bytes",
                     "nvfp4_cascade_decode_attention")
 
@@ -436,6 +438,39 @@ def extend_attention(q: torch.Tensor, k_prefix: torch.Tensor, v_prefix: torch.Te
                                      _ptr(k_chunk), _ptr(v_chunk), _ptr(cu_q_lens), int(q.shape[0]), R,
                                      int(max_q_len), hq, hkv, float(sm_scale), _ptr(out), _stream(stream))
     _check(rc, "nvfp4_extend_attention")
+    return out
+
+
+def extend_attention_paged(cache: PagedCache, q: torch.Tensor, block_table: torch.Tensor, prefix_lens: torch.Tensor,
+                           k_chunk: torch.Tensor, v_chunk: torch.Tensor, cu_q_lens: torch.Tensor, max_q_len: int,
+                           sm_scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
+                           stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """extend_attention with request r's prefix read from the NVFP4 cache: tokens
+    0 .. prefix_lens[r] - 1 of its pages (block_table row r, int32 [R][max_pages]),
+    expanded to BF16 inside the kernel; equals prefix_dequant + extend_attention."""
+    for name, x in (("q", q), ("k_chunk", k_chunk), ("v_chunk", v_chunk)):
+        if not x.is_cuda or x.dtype != torch.bfloat16 or not x.is_contiguous() or x.dim() != 3 or x.shape[2] != HEAD_DIM:
+            raise ValueError("%s must be a contiguous CUDA bfloat16 tensor [rows][heads][128]" % name)
+    _require(block_table, "block_table", torch.int32)
+    _require(prefix_lens, "prefix_lens", torch.int32)
+    _require(cu_q_lens, "cu_q_lens", torch.int32)
+    R = int(cu_q_lens.shape[0]) - 1
+    if int(prefix_lens.shape[0]) != R or int(block_table.shape[0]) != R:
+        raise ValueError("prefix_lens and block_table need one entry / row per request")
+    hq = int(q.shape[1])
+    if k_chunk.shape[1] != cache.num_kv_heads or v_chunk.shape[1] != cache.num_kv_heads:
+        raise ValueError("chunk K/V must have the cache's kv heads")
+    if k_chunk.shape[0] != q.shape[0] or v_chunk.shape[0] != q.shape[0]:
+        raise ValueError("chunk K/V must have one row per query token")
+    if out is None:
+        out = torch.empty_like(q)
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(HEAD_DIM)
+    rc = _lib.nvfp4_extend_attention_paged(cache.desc, _ptr(q), _ptr(block_table), int(block_table.shape[1]),
+                                           _ptr(prefix_lens), _ptr(k_chunk), _ptr(v_chunk), _ptr(cu_q_lens),
+                                           int(q.shape[0]), R, int(max_q_len), hq, float(sm_scale), _ptr(out),
+                                           _stream(stream))
+    _check(rc, "nvfp4_extend_attention_paged")
     return out
 
 

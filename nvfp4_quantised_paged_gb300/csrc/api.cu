@@ -198,6 +198,35 @@ int nvfp4_extend_attention(const void *q, const void *k_prefix, const void *v_pr
                                    out, err, stream));
 }
 
+int nvfp4_extend_attention_paged(const nvfp4kv_cache *cache, const void *q, const int32_t *block_table,
+                                 int max_pages_per_seq, const int32_t *prefix_lens, const void *k_chunk,
+                                 const void *v_chunk, const int32_t *cu_q_lens, int64_t total_q_tokens, int num_reqs,
+                                 int max_q_len, int num_q_heads, float sm_scale, void *out, cudaStream_t stream) {
+    int rc = check_cache(cache);
+    if (rc) return rc;
+    if (cache->dtype != NVFP4KV_DTYPE_NVFP4) return NVFP4KV_EUNSUPPORTED;
+    if (num_reqs < 0 || max_q_len < 0 || num_q_heads < 1 || num_q_heads % cache->num_kv_heads ||
+        total_q_tokens < 0 || max_pages_per_seq < 1)
+        return NVFP4KV_EINVAL;
+    if (total_q_tokens >= ((int64_t)1 << 31)) return NVFP4KV_EUNSUPPORTED;
+    if (!isfinite(sm_scale)) return NVFP4KV_EINVAL;
+    if (num_reqs == 0 || max_q_len == 0) return NVFP4KV_OK;
+    if (!q || !block_table || !prefix_lens || !k_chunk || !v_chunk || !cu_q_lens || !out) return NVFP4KV_EINVAL;
+    if (!aligned(q, 16) || !aligned(k_chunk, 16) || !aligned(v_chunk, 16) || !aligned(out, 16) ||
+        !aligned(block_table, 4) || !aligned(prefix_lens, 4) || !aligned(cu_q_lens, 4))
+        return NVFP4KV_EINVAL;
+    const int64_t G = num_q_heads / cache->num_kv_heads;
+    if ((int64_t)max_q_len * G >= ((int64_t)1 << 31) || cache->num_kv_heads > 65535 || num_reqs > 65535 ||
+        (int64_t)max_pages_per_seq * cache->page_size >= ((int64_t)1 << 31))
+        return NVFP4KV_EUNSUPPORTED;
+    cudaError_t e;
+    unsigned *err = error_word(&e);
+    if (!err) return NVFP4KV_ECUDA;
+    return from_cuda(launch_extend_paged(*cache, q, block_table, max_pages_per_seq, prefix_lens, k_chunk, v_chunk,
+                                         cu_q_lens, total_q_tokens, num_reqs, max_q_len, num_q_heads, sm_scale, out,
+                                         err, stream));
+}
+
 int nvfp4kv_calibrate_global_scales(const void *k, const void *v, int64_t num_tokens, int num_kv_heads,
                                     int64_t token_stride, float *scales, cudaStream_t stream) {
     if (num_tokens < 0 || num_kv_heads < 1 || !scales || !aligned(scales, 8)) return NVFP4KV_EINVAL;

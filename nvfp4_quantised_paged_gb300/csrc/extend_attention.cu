@@ -42,6 +42,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "quantize.cuh"
 #include "tcgen05.cuh"
 
 namespace nvfp4kv {
@@ -53,6 +54,8 @@ constexpr int kQRows = 128;                    // rows per query tile (one TMEM 
 constexpr int kCtaRows = kWGs * kQRows;
 constexpr int kSoftThreads = kWGs * kQRows;
 constexpr int kEThreads = kSoftThreads + 32;   // + the load / MMA warp
+constexpr int kDqThreads = 96;                 // paged prefix: three warps expanding NVFP4 tiles
+constexpr int kEThreadsPaged = kEThreads + kDqThreads;
 constexpr int kKeys = 128;                     // keys per K/V tile
 constexpr int kQBytes = kQRows * 256;          // a query tile: 2 column blocks of [128][64] BF16
 constexpr int kKVBlock = kKeys * 128;          // one column block of a K or V tile (one TMA box)
@@ -61,11 +64,12 @@ constexpr int kOffQ = 0;                                   // Q0 | Q1
 constexpr int kOffK = kWGs * kQBytes;                      // K slots [2]
 constexpr int kOffV = kOffK + 2 * kKVTile;                 // V slots [2]
 constexpr int kOffBar = kOffV + 2 * kKVTile;
-// mbarriers: k_full[2] v_full[2] s_done[2] p_full[2] pv_done[2] drain
-constexpr int kNumBars = 11;
+// mbarriers: k_full[2] v_full[2] s_done[2] p_full[2] pv_done[2] drain, and for a
+// paged prefix k_go[2] v_go[2] (tile may be expanded) k_dq[2] v_dq[2] (expanded)
+constexpr int kNumBars = 19;
 constexpr int kOffTmem = kOffBar + kNumBars * 8;
 constexpr int kOffAbort = kOffTmem + 4;
-constexpr int kOffOrder = kOffBar + 128;       // int[256]: requests by decreasing prefix length
+constexpr int kOffOrder = kOffBar + 256;       // int[256]: requests by decreasing prefix length
 constexpr int kOrderMax = 256;
 constexpr int kESmem = kOffOrder + 4 * kOrderMax;
 // TMEM columns: S_w at 128w (FP32; P_w as BF16 pairs over its first 64 columns), O_w at 256 + 128w
@@ -82,6 +86,13 @@ struct ExtendArgs {
     float score_log2;                  // sm_scale * log2(e)
     uint16_t *out;                     // BF16 [total_q][Hq][128]
     unsigned *err;
+    // paged prefix: request r's prefix is tokens 0 .. prefix_lens[r] - 1 of its
+    // pages in the NVFP4 pool (block_table row r), not workspace rows
+    const uint8_t *pool;
+    int64_t num_pages, slab;
+    int P, log2P, max_pages;
+    const int32_t *block_table, *prefix_lens;
+    float gk, gv;
 };
 
 // K/V tensors [rows][Hkv][128] BF16 as 3-D TMA maps with 64 x 1 x 128 boxes, 128-byte swizzle.
@@ -103,6 +114,16 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+
+// Bounded wait on an mbarrier phase without sleeping between polls (these
+// waits are on the critical path); gives up when another warp has aborted.
+__device__ __forceinline__ bool spin_wait(uint64_t *bar, uint32_t parity, const volatile int *abort_flag) {
+    for (uint32_t n = 0; n < kWaitLimitE; n++) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+    }
+    return false;
+}
 
 __device__ __forceinline__ float max3(float a, float b, float c) {
     float d;
@@ -130,11 +151,13 @@ __device__ __forceinline__ void add_bf16x2(float &s0, float &s1, uint32_t w) {
         : "r"(w), "h"(one));
 }
 
-__global__ void __launch_bounds__(kEThreads, 1) extend_kernel(const __grid_constant__ ExtendMaps maps, ExtendArgs a) {
+template <bool kPaged>
+__global__ void __launch_bounds__(kPaged ? kEThreadsPaged : kEThreads, 1)
+    extend_kernel(const __grid_constant__ ExtendMaps maps, ExtendArgs a) {
     extern __shared__ __align__(1024) uint8_t smem[];
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBar);
     uint64_t *k_full = bars, *v_full = bars + 2, *s_done = bars + 4, *p_full = bars + 6, *pv_done = bars + 8;
-    uint64_t *drain = bars + 10;
+    uint64_t *drain = bars + 10, *k_go = bars + 11, *v_go = bars + 13, *k_dq = bars + 15, *v_dq = bars + 17;
     uint32_t &tmem_base = *reinterpret_cast<uint32_t *>(smem + kOffTmem);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffAbort);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -145,11 +168,12 @@ __global__ void __launch_bounds__(kEThreads, 1) extend_kernel(const __grid_const
     if (gridDim.z <= kOrderMax) {
         int *order = reinterpret_cast<int *>(smem + kOffOrder);
         const int nr = (int)gridDim.z;
+        auto prefix_len = [&](int c) { return kPaged ? a.prefix_lens[c] : a.cu_prefix[c + 1] - a.cu_prefix[c]; };
         if (tid < nr) {
-            const int nj = a.cu_prefix[tid + 1] - a.cu_prefix[tid];
+            const int nj = prefix_len(tid);
             int rank = 0;
             for (int c = 0; c < nr; c++) {
-                const int nc = a.cu_prefix[c + 1] - a.cu_prefix[c];
+                const int nc = prefix_len(c);
                 rank += nc > nj || (nc == nj && c < tid);
             }
             order[rank] = tid;
@@ -158,12 +182,16 @@ __global__ void __launch_bounds__(kEThreads, 1) extend_kernel(const __grid_const
         r = order[blockIdx.z];
     }
     const int kv = blockIdx.y;
-    const int q0 = a.cu_q[r], p0 = a.cu_prefix[r];
+    const int q0 = a.cu_q[r], p0 = kPaged ? 0 : a.cu_prefix[r];
     int L = a.cu_q[r + 1] - q0;
-    const int np = a.cu_prefix[r + 1] - p0;
+    int np = kPaged ? a.prefix_lens[r] : a.cu_prefix[r + 1] - p0;
     if (L < 0 || np < 0) {
         if (tid == 0 && blockIdx.x == 0 && kv == 0) flag_error(a.err, kErrCuPrefix);
         return;
+    }
+    if (kPaged && (int64_t)np > (int64_t)a.max_pages * a.P) {
+        if (tid == 0 && blockIdx.x == 0 && kv == 0) flag_error(a.err, kErrSeqLen);
+        np = a.max_pages * a.P;
     }
     if (L > a.max_q_len) {
         if (tid == 0 && blockIdx.x == 0 && kv == 0) flag_error(a.err, kErrSeqLen);
@@ -198,7 +226,13 @@ __global__ void __launch_bounds__(kEThreads, 1) extend_kernel(const __grid_const
     // 64..127) of 128 rows; rows past the tensor are zero-filled, rows of a
     // neighbouring request are masked by the softmax
     auto tile_row = [&](int j) { return j < nt_pre ? p0 + j * kKeys : q0 + (j - nt_pre) * kKeys; };
+    // (paged prefix: the tile is expanded by the dequantising warps instead,
+    // told to start by its go barrier; they complete the same full barrier)
     auto load_k = [&](int j, int s) {
+        if (kPaged && j < nt_pre) {
+            mbar_arrive(&k_go[s]);
+            return;
+        }
         const CUtensorMap *m = j < nt_pre ? &maps.k_pre : &maps.k_new;
         const uint32_t dst = sbase + kOffK + s * kKVTile;
         mbar_arrive_expect_tx(&k_full[s], kKVTile);
@@ -206,6 +240,10 @@ __global__ void __launch_bounds__(kEThreads, 1) extend_kernel(const __grid_const
         tma_load_3d(dst + kKVBlock, m, 64, kv, tile_row(j), &k_full[s]);
     };
     auto load_v = [&](int j, int s) {
+        if (kPaged && j < nt_pre) {
+            mbar_arrive(&v_go[s]);
+            return;
+        }
         const CUtensorMap *m = j < nt_pre ? &maps.v_pre : &maps.v_new;
         const uint32_t dst = sbase + kOffV + s * kKVTile;
         mbar_arrive_expect_tx(&v_full[s], kKVTile);
@@ -215,7 +253,7 @@ __global__ void __launch_bounds__(kEThreads, 1) extend_kernel(const __grid_const
 
     if (warp == 0) tc_alloc(&tmem_base, kTmemCols);
     if (tid == kSoftThreads) {
-        for (int j = 0; j < kNumBars; j++) mbar_init(&bars[j], (j == 6 || j == 7) ? kQRows : 1);
+        for (int j = 0; j < kNumBars; j++) mbar_init(&bars[j], (j == 6 || j == 7) ? kQRows : j >= 15 ? kDqThreads : 1);
         *abort_flag = 0;
         fence_mbar_init();
         for (int j = 0; j < 2 && j < nt; j++) {
@@ -261,6 +299,10 @@ __global__ void __launch_bounds__(kEThreads, 1) extend_kernel(const __grid_const
             //   K(t) into slot t % 2 once both S(t - 2) are done (their P V issued);
             //   V(t) into slot t % 2 once both P(t - 2) V(t - 2) are complete.
             // Each barrier is polled only where it cannot be two phases ahead.
+            // Phase of the barrier that completes tile t in slot t % 2: tile t is
+            // the (t / 2)-th of its slot; with a paged prefix, chunk tiles count
+            // from the first chunk tile (prefix tiles complete k_dq / v_dq instead).
+            auto kv_phase = [&](int t) { return (uint32_t)((((kPaged && t >= nt_pre) ? t - nt_pre : t) >> 1) & 1); };
             int tw[kWGs] = {0, 0};                 // next tile of query tile w
             bool at_pv[kWGs] = {false, false};     // its next product is P V (else S)
             int pv_seen[kWGs] = {0, 0};            // its P V of tiles < pv_seen are known complete
@@ -279,13 +321,15 @@ __global__ void __launch_bounds__(kEThreads, 1) extend_kernel(const __grid_const
                             if (!mbar_test_wait(&pv_done[w], (uint32_t)((t - 1) & 1))) continue;
                             pv_seen[w] = t;
                         }
-                        if (!mbar_test_wait(&k_full[t & 1], (uint32_t)((t >> 1) & 1))) continue;
+                        uint64_t *kb = kPaged && t < nt_pre ? &k_dq[t & 1] : &k_full[t & 1];
+                        if (!mbar_test_wait(kb, kv_phase(t))) continue;
                         tc_fence_after();
                         mma_s(w, t & 1);
                         at_pv[w] = true;
                     } else {
                         if (!mbar_test_wait(&p_full[w], (uint32_t)(t & 1))) continue;
-                        if (!mbar_test_wait(&v_full[t & 1], (uint32_t)((t >> 1) & 1))) continue;
+                        uint64_t *vb = kPaged && t < nt_pre ? &v_dq[t & 1] : &v_full[t & 1];
+                        if (!mbar_test_wait(vb, kv_phase(t))) continue;
                         tc_fence_after();
                         mma_pv(w, t, t & 1);
                         at_pv[w] = false;
@@ -320,15 +364,78 @@ __global__ void __launch_bounds__(kEThreads, 1) extend_kernel(const __grid_const
                 *abort_flag = 1;
                 flag_error(a.err, kErrTimeout);
                 // no copy or MMA may still be running when the CTA frees its memory
-                for (int t = max(0, k_next - 2); t < k_next; t++)
-                    mbar_wait_bounded(&k_full[t & 1], (uint32_t)((t >> 1) & 1), kWaitLimitE, nullptr);
-                for (int t = max(0, v_next - 2); t < v_next; t++)
-                    mbar_wait_bounded(&v_full[t & 1], (uint32_t)((t >> 1) & 1), kWaitLimitE, nullptr);
+                for (int t = max(kPaged ? nt_pre : 0, k_next - 2); t < k_next; t++)  // tensor copies only
+                    mbar_wait_bounded(&k_full[t & 1], kv_phase(t), kWaitLimitE, nullptr);
+                for (int t = max(kPaged ? nt_pre : 0, v_next - 2); t < v_next; t++)
+                    mbar_wait_bounded(&v_full[t & 1], kv_phase(t), kWaitLimitE, nullptr);
                 tc_commit(drain);
                 mbar_wait_bounded(drain, 0, kWaitLimitE, nullptr);
             }
         }
         __syncwarp();
+    } else if (kPaged && warp > kSoftThreads / 32) {
+        // ---------------- paged prefix: expand tile j's K (then V) from the NVFP4
+        // pages into the BF16 operand layout of the slot, once it may be written
+        const int dt = tid - kEThreads;  // 0 .. kDqThreads - 1
+        const int32_t *bt = a.block_table + (int64_t)r * a.max_pages;
+        constexpr int kBlocks = kKeys * 8;  // 16-value blocks of one K (or V) tile
+        constexpr int kPer = (kBlocks + kDqThreads - 1) / kDqThreads;
+        // item n = K (n even) or V (n odd) of prefix tile n / 2; its page data is
+        // loaded one item ahead (the loads need no free slot), zeros past the prefix
+        struct Raw {
+            uint2 codes[kPer];
+            uint32_t sb[kPer];
+        };
+        auto fetch = [&](int n, Raw &raw) {
+            const int j = n >> 1, which = n & 1;
+#pragma unroll
+            for (int i = 0; i < kPer; i++) {
+                const int b = dt + i * kDqThreads, key = b >> 3, blk = b & 7, tok = j * kKeys + key;
+                raw.codes[i] = make_uint2(0u, 0u);
+                raw.sb[i] = 0u;
+                if (b < kBlocks && tok < np) {
+                    const int32_t pg = __ldg(bt + (tok >> a.log2P));
+                    if (pg >= 0 && pg < a.num_pages) {
+                        const uint8_t *grp =
+                            a.pool + ((int64_t)pg * a.Hkv + kv) * a.slab + ((tok & (a.P - 1)) >> 4) * 2304;
+                        const int rr = tok & 15;
+                        raw.codes[i] = __ldg(reinterpret_cast<const uint2 *>(grp + (which ? 1152 : 0) + rr * 64 + blk * 8));
+                        raw.sb[i] = __ldg(grp + (which ? 2176 + blk * 16 + rr : 1024 + rr * 8 + blk));
+                    } else if (blk == 0) {
+                        flag_error(a.err, kErrPage);
+                    }
+                }
+            }
+        };
+        const int items = 2 * nt_pre;
+        Raw cur, nxt;
+        if (items > 0) fetch(0, cur);
+        bool ok = true;
+        for (int n = 0; n < items; n++) {
+            const int j = n >> 1, which = n & 1, s = j & 1;
+            if (n + 1 < items) fetch(n + 1, nxt);
+            ok = __all_sync(0xffffffffu, spin_wait(which ? &v_go[s] : &k_go[s], (uint32_t)((j >> 1) & 1), abort_flag));
+            if (!ok) break;
+            uint8_t *tile = smem + (which ? kOffV : kOffK) + s * kKVTile;
+#pragma unroll
+            for (int i = 0; i < kPer; i++) {
+                const int b = dt + i * kDqThreads;
+                if (b >= kBlocks) continue;
+                const int key = b >> 3, blk = b & 7;
+                uint32_t o[8];
+                nvfp4_block_to_bf16(cur.codes[i], cur.sb[i], which ? a.gv : a.gk, o);
+                uint8_t *cb = tile + (blk >> 2) * kKVBlock;  // column block of head_dim 64 (blk / 4) ..
+                *reinterpret_cast<uint4 *>(cb + sw128_off(key, (blk & 3) * 2)) = make_uint4(o[0], o[1], o[2], o[3]);
+                *reinterpret_cast<uint4 *>(cb + sw128_off(key, (blk & 3) * 2 + 1)) = make_uint4(o[4], o[5], o[6], o[7]);
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the tile for the tensor core
+            mbar_arrive(which ? &v_dq[s] : &k_dq[s]);
+            cur = nxt;
+        }
+        if (!ok) {
+            *abort_flag = 1;
+            if (lane == 0) flag_error(a.err, kErrTimeout);
+        }
     } else if ((tid >> 7) < nwg) {
         // ---------------- softmax of this thread's query row
         const int w = tid >> 7;
@@ -508,30 +615,32 @@ bool make_kv_map(CUtensorMap *map, const void *base, int64_t rows, int Hkv) {
 
 }  // namespace
 
-cudaError_t launch_extend(const void *q, const void *k_prefix, const void *v_prefix, const int32_t *cu_prefix,
-                          int64_t total_prefix, const void *k_chunk, const void *v_chunk, const int32_t *cu_q,
-                          int64_t total_q, int num_reqs, int max_q_len, int num_q_heads, int num_kv_heads,
-                          float sm_scale, void *out, unsigned *err, cudaStream_t stream) {
+namespace {
+
+template <bool kPaged>
+cudaError_t launch_extend_kernel(const ExtendMaps &maps, const ExtendArgs &a, int num_reqs, int max_q_len,
+                                 int num_kv_heads, cudaStream_t stream) {
     static bool attr_set[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!attr_set[dev]) {
-        e = cudaFuncSetAttribute(reinterpret_cast<const void *>(&extend_kernel),
+        e = cudaFuncSetAttribute(reinterpret_cast<const void *>(&extend_kernel<kPaged>),
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, kESmem);
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
-    ExtendMaps maps;
-    if (!make_kv_map(&maps.k_pre, k_prefix, total_prefix, num_kv_heads) ||
-        !make_kv_map(&maps.v_pre, v_prefix, total_prefix, num_kv_heads) ||
-        !make_kv_map(&maps.k_new, k_chunk, total_q, num_kv_heads) ||
-        !make_kv_map(&maps.v_new, v_chunk, total_q, num_kv_heads))
-        return cudaErrorInvalidValue;
-    ExtendArgs a;
+    const int64_t qtiles = ceil_div64((int64_t)max_q_len * a.G, kCtaRows);
+    dim3 grid((unsigned)qtiles, (unsigned)num_kv_heads, (unsigned)num_reqs);
+    extend_kernel<kPaged><<<grid, kPaged ? kEThreadsPaged : kEThreads, kESmem, stream>>>(maps, a);
+    return cudaGetLastError();
+}
+
+ExtendArgs common_args(const void *q, const int32_t *cu_q, int max_q_len, int num_q_heads, int num_kv_heads,
+                       float sm_scale, void *out, unsigned *err) {
+    ExtendArgs a = {};
     a.q = static_cast<const uint16_t *>(q);
-    a.cu_prefix = cu_prefix;
     a.cu_q = cu_q;
     a.Hq = num_q_heads;
     a.Hkv = num_kv_heads;
@@ -540,10 +649,48 @@ cudaError_t launch_extend(const void *q, const void *k_prefix, const void *v_pre
     a.score_log2 = (float)((double)sm_scale * 1.4426950408889634);
     a.out = static_cast<uint16_t *>(out);
     a.err = err;
-    const int64_t qtiles = ceil_div64((int64_t)max_q_len * a.G, kCtaRows);
-    dim3 grid((unsigned)qtiles, (unsigned)num_kv_heads, (unsigned)num_reqs);
-    extend_kernel<<<grid, kEThreads, kESmem, stream>>>(maps, a);
-    return cudaGetLastError();
+    return a;
+}
+
+}  // namespace
+
+cudaError_t launch_extend(const void *q, const void *k_prefix, const void *v_prefix, const int32_t *cu_prefix,
+                          int64_t total_prefix, const void *k_chunk, const void *v_chunk, const int32_t *cu_q,
+                          int64_t total_q, int num_reqs, int max_q_len, int num_q_heads, int num_kv_heads,
+                          float sm_scale, void *out, unsigned *err, cudaStream_t stream) {
+    ExtendMaps maps;
+    if (!make_kv_map(&maps.k_pre, k_prefix, total_prefix, num_kv_heads) ||
+        !make_kv_map(&maps.v_pre, v_prefix, total_prefix, num_kv_heads) ||
+        !make_kv_map(&maps.k_new, k_chunk, total_q, num_kv_heads) ||
+        !make_kv_map(&maps.v_new, v_chunk, total_q, num_kv_heads))
+        return cudaErrorInvalidValue;
+    ExtendArgs a = common_args(q, cu_q, max_q_len, num_q_heads, num_kv_heads, sm_scale, out, err);
+    a.cu_prefix = cu_prefix;
+    return launch_extend_kernel<false>(maps, a, num_reqs, max_q_len, num_kv_heads, stream);
+}
+
+cudaError_t launch_extend_paged(const nvfp4kv_cache &c, const void *q, const int32_t *block_table, int max_pages,
+                                const int32_t *prefix_lens, const void *k_chunk, const void *v_chunk,
+                                const int32_t *cu_q, int64_t total_q, int num_reqs, int max_q_len, int num_q_heads,
+                                float sm_scale, void *out, unsigned *err, cudaStream_t stream) {
+    ExtendMaps maps;  // the prefix maps are never used: they alias the chunk
+    if (!make_kv_map(&maps.k_new, k_chunk, total_q, c.num_kv_heads) ||
+        !make_kv_map(&maps.v_new, v_chunk, total_q, c.num_kv_heads))
+        return cudaErrorInvalidValue;
+    maps.k_pre = maps.k_new;
+    maps.v_pre = maps.v_new;
+    ExtendArgs a = common_args(q, cu_q, max_q_len, num_q_heads, c.num_kv_heads, sm_scale, out, err);
+    a.pool = static_cast<const uint8_t *>(c.pool);
+    a.num_pages = c.num_pages;
+    a.slab = (int64_t)144 * c.page_size;
+    a.P = c.page_size;
+    a.log2P = __builtin_ctz((unsigned)c.page_size);
+    a.max_pages = max_pages;
+    a.block_table = block_table;
+    a.prefix_lens = prefix_lens;
+    a.gk = c.k_global_scale;
+    a.gv = c.v_global_scale;
+    return launch_extend_kernel<true>(maps, a, num_reqs, max_q_len, c.num_kv_heads, stream);
 }
 
 }  // namespace nvfp4kv

@@ -52,6 +52,13 @@ cudaError_t launch_extend(const void *q, const void *k_prefix, const void *v_pre
                           int64_t total_q, int num_reqs, int max_q_len, int num_q_heads, int num_kv_heads,
                           float sm_scale, void *out, unsigned *err, cudaStream_t stream);
 
+// The same with request r's prefix read from the NVFP4 pool through row r of
+// the block table (prefix_lens[r] tokens) and expanded to BF16 in the kernel.
+cudaError_t launch_extend_paged(const nvfp4kv_cache &c, const void *q, const int32_t *block_table, int max_pages,
+                                const int32_t *prefix_lens, const void *k_chunk, const void *v_chunk,
+                                const int32_t *cu_q, int64_t total_q, int num_reqs, int max_q_len, int num_q_heads,
+                                float sm_scale, void *out, unsigned *err, cudaStream_t stream);
+
 // g_K, g_V = amax / (6 * 448) of K and V (1.0 for an all-zero tensor) into scales[0..1].
 cudaError_t launch_calibrate(const void *k, const void *v, int64_t num_tokens, int num_kv_heads, int64_t token_stride,
                              float *scales, cudaStream_t stream);

@@ -12,6 +12,7 @@
 // (per token and KV head 144 B in, 512 B out).
 #include "common.cuh"
 #include "kernels.h"
+#include "quantize.cuh"
 
 namespace nvfp4kv {
 
@@ -37,20 +38,6 @@ struct PrefixArgs {
     unsigned *err;
 };
 
-__device__ __forceinline__ float f16_lo(uint32_t x) { return __half2float(__ushort_as_half((uint16_t)(x & 0xffffu))); }
-__device__ __forceinline__ float f16_hi(uint32_t x) { return __half2float(__ushort_as_half((uint16_t)(x >> 16))); }
-
-__device__ __forceinline__ uint32_t f32x2_to_bf16x2(float hi, float lo) {
-    uint32_t r;
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-    return r;
-}
-
-// f16x2 holding exact values -> bf16x2 of (value * g), one rounding to BF16
-// after the FP32 product (exact when g = 1).
-__device__ __forceinline__ uint32_t f16x2_to_bf16x2_scaled(uint32_t x, float g) {
-    return f32x2_to_bf16x2(__fmul_rn(f16_hi(x), g), __fmul_rn(f16_lo(x), g));
-}
 
 __global__ void __launch_bounds__(256) prefix_dequant_kernel(PrefixArgs a) {
     // the host guarantees total * Hkv * 16 < 2^31
@@ -93,12 +80,7 @@ __global__ void __launch_bounds__(256) prefix_dequant_kernel(PrefixArgs a) {
         const uint8_t *grp = slab + (rp >> 4) * 2304;
         const uint2 codes = __ldg(reinterpret_cast<const uint2 *>(grp + (which ? 1152 : 0) + rr * 64 + blk * 8));
         const uint32_t sbyte = __ldg(grp + (which ? 2176 + blk * 16 + rr : 1024 + rr * 8 + blk));
-        const uint32_t s2 = e4m3x2_to_f16x2(sbyte | (sbyte << 8));  // {s, s}
-        uint32_t f[8];
-        e2m1x8_to_f16x2x4(codes.x, f[0], f[1], f[2], f[3]);
-        e2m1x8_to_f16x2x4(codes.y, f[4], f[5], f[6], f[7]);
-#pragma unroll
-        for (int i = 0; i < 8; i++) o[i] = f16x2_to_bf16x2_scaled(hmul2(f[i], s2), g);
+        nvfp4_block_to_bf16(codes, sbyte, g, o);
     } else {
         const uint4 c = __ldg(
             reinterpret_cast<const uint4 *>(slab + (rp >> 4) * 4096 + (which ? 2048 : 0) + rr * 128 + blk * 16));

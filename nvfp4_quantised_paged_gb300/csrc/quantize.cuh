@@ -91,6 +91,33 @@ __device__ __forceinline__ void quantize_block16(const uint4 &a, const uint4 &b,
     codes = make_uint2(packed[0], packed[1]);
 }
 
+__device__ __forceinline__ float f16_lo(uint32_t x) { return __half2float(__ushort_as_half((uint16_t)(x & 0xffffu))); }
+__device__ __forceinline__ float f16_hi(uint32_t x) { return __half2float(__ushort_as_half((uint16_t)(x >> 16))); }
+
+__device__ __forceinline__ uint32_t f32x2_to_bf16x2(float hi, float lo) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// f16x2 holding exact values -> bf16x2 of (value * g), one rounding to BF16
+// after the FP32 product (exact when g = 1).
+__device__ __forceinline__ uint32_t f16x2_to_bf16x2_scaled(uint32_t x, float g) {
+    return f32x2_to_bf16x2(__fmul_rn(f16_hi(x), g), __fmul_rn(f16_lo(x), g));
+}
+
+// One NVFP4 16-value block (8 code bytes, one E4M3 scale byte) -> 8 BF16 pairs
+// of e2m1 * e4m3 * g, rounded to BF16 once (exact for g = 1): the prefix
+// dequant kernel and the paged extend kernel both expand blocks this way.
+__device__ __forceinline__ void nvfp4_block_to_bf16(uint2 codes, uint32_t sbyte, float g, uint32_t (&o)[8]) {
+    const uint32_t s2 = e4m3x2_to_f16x2(sbyte | (sbyte << 8));  // {s, s}
+    uint32_t f[8];
+    e2m1x8_to_f16x2x4(codes.x, f[0], f[1], f[2], f[3]);
+    e2m1x8_to_f16x2x4(codes.y, f[4], f[5], f[6], f[7]);
+#pragma unroll
+    for (int i = 0; i < 8; i++) o[i] = f16x2_to_bf16x2_scaled(hmul2(f[i], s2), g);
+}
+
 // Quantise block `blk` (0..7) of K (which = 0) or V (which = 1) of one
 // head_dim row -- the 16 BF16 values at src[0..1] -- and store it at row `r`
 // of the (page, h) slab.  NVFP4 slabs are 16-token groups of 2304 bytes

@@ -1,6 +1,7 @@
 """Extend attention (section A2, path 2) on the GPU against the fp64 oracle:
 ragged prefixes and chunks across the 128-key tile and 256-row CTA
-boundaries, GQA groups 1-8, query tiles left empty, empty
+boundaries, GQA groups 1-8, query tiles left empty, the prefix read from the
+NVFP4 pages inside the kernel (bit-identical to the workspace path), empty
 prefixes and chunks, and the whole path -- prefix dequantised from the NVFP4
 cache by prefix_dequant, then attended together with the chunk."""
 
@@ -90,3 +91,67 @@ def test_path2_prefix_dequant_then_extend(m):
     assert np.array_equal(bits(kw), rk) and np.array_equal(bits(vw), rv)
     ref = oracle.extend_attention(bits(q), rk, rv, cu_p.numpy(), bits(kn), bits(vn), cu_q.numpy(), SM)
     check_attention(out, ref, "path 2")
+
+
+def _paged_case(m, lens, chunk, Hq, Hkv, P, seed, gk=1.0, gv=1.0):
+    w = workloads.make_decode("paged extend", seed, lens, Hq, Hkv, P, recipe=workloads.ValueRecipe(outlier_p=0.002))
+    cache, pool = fill_both(w, m, gk=gk, gv=gv)
+    pl = w.seq_lens
+    cu_p = torch.zeros(w.batch + 1, dtype=torch.int32)
+    cu_p[1:] = torch.cumsum(pl, 0)
+    cu_q = torch.tensor(np.concatenate([[0], np.cumsum(chunk)]), dtype=torch.int32)
+    TQ = int(cu_q[-1])
+    q = _rand((TQ, Hq, 128), seed + 1)
+    kn, vn = _rand((TQ, Hkv, 128), seed + 2), _rand((TQ, Hkv, 128), seed + 3)
+    L = max(chunk)
+    bt = w.block_table.cuda()
+    paged = m.extend_attention_paged(cache, q, bt, pl.cuda(), kn, vn, cu_q.cuda(), L, SM)
+    kw, vw = m.prefix_dequant(cache, bt, pl.cuda(), cu_p.cuda(), int(cu_p[-1]))
+    two = m.extend_attention(q, kw, vw, cu_p.cuda(), kn, vn, cu_q.cuda(), L, SM)
+    torch.cuda.synchronize()
+    assert m.check_device_errors() == 0
+    return paged, two, (w, pool, pl, cu_p, cu_q, q, kn, vn)
+
+
+@pytest.mark.parametrize("lens,chunk,Hq,Hkv,P", [
+    ([700, 64, 1500, 100], [50, 512, 1, 130], 32, 8, 64),
+    ([0, 1, 127, 129, 300], [17, 64, 255, 5, 1], 16, 2, 16),
+    ([1000, 257], [96, 200], 40, 8, 128),
+    ([63, 2048], [300, 7], 8, 1, 32),
+])
+def test_paged_extend_equals_dequant_then_extend(m, lens, chunk, Hq, Hkv, P):
+    """The prefix expanded inside the kernel gives the same BF16 operands, in the
+    same order, as the workspace path: the outputs are identical."""
+    paged, two, _ = _paged_case(m, lens, chunk, Hq, Hkv, P, 70 + P)
+    assert torch.equal(paged, two)
+
+
+def test_paged_extend_with_tensor_scales_matches_oracle(m):
+    paged, two, (w, pool, pl, cu_p, cu_q, q, kn, vn) = _paged_case(m, [300, 130], [64, 129], 32, 8, 64, 91,
+                                                                  gk=0.37, gv=2.5)
+    assert torch.equal(paged, two)
+    rk, rv = oracle.prefix_dequant(pool, w.block_table.numpy(), pl.numpy(), cu_p.numpy())
+    ref = oracle.extend_attention(bits(q), rk, rv, cu_p.numpy(), bits(kn), bits(vn), cu_q.numpy(), SM)
+    check_attention(paged, ref, "paged extend g != 1")
+
+
+def test_paged_extend_bad_page_is_flagged(m):
+    w = workloads.make_decode("paged bad page", 93, [200], 8, 2, 64)
+    cache, _ = fill_both(w, m)
+    bt = w.block_table.clone()
+    bt[0, 1] = -1
+    cu_q = torch.tensor([0, 16], dtype=torch.int32, device="cuda")
+    q, kn, vn = _rand((16, 8, 128), 94), _rand((16, 2, 128), 95), _rand((16, 2, 128), 96)
+    out = m.extend_attention_paged(cache, q, bt.cuda(), w.seq_lens.cuda(), kn, vn, cu_q, 16, SM)
+    torch.cuda.synchronize()
+    assert m.check_device_errors() == -4
+    assert torch.isfinite(out.float()).all()  # the missing page reads as zeros
+
+
+def test_paged_extend_needs_an_nvfp4_pool(m):
+    cache = m.PagedCache(4, 64, 2, dtype=m.DTYPE_FP8_E4M3)
+    cu_q = torch.tensor([0, 16], dtype=torch.int32, device="cuda")
+    q, kn, vn = _rand((16, 8, 128), 97), _rand((16, 2, 128), 98), _rand((16, 2, 128), 99)
+    with pytest.raises(m.NVFP4KVError):
+        m.extend_attention_paged(cache, q, torch.zeros((1, 4), dtype=torch.int32, device="cuda"),
+                                 torch.tensor([64], dtype=torch.int32, device="cuda"), kn, vn, cu_q, 16, SM)
