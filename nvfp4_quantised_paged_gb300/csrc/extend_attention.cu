@@ -66,12 +66,23 @@ constexpr int kOffV = kOffK + 2 * kKVTile;                 // V slots [2]
 constexpr int kOffBar = kOffV + 2 * kKVTile;
 // mbarriers: k_full[2] v_full[2] s_done[2] p_full[2] pv_done[2] drain, and for a
 // paged prefix k_go[2] v_go[2] (tile may be expanded) k_dq[2] v_dq[2] (expanded)
-constexpr int kNumBars = 19;
+// rawk_full rawv_full[2] (raw halves landed) rawk_free rawv_free[2] (read)
+constexpr int kNumBars = 25;
 constexpr int kOffTmem = kOffBar + kNumBars * 8;
 constexpr int kOffAbort = kOffTmem + 4;
 constexpr int kOffOrder = kOffBar + 256;       // int[256]: requests by decreasing prefix length
 constexpr int kOrderMax = 256;
 constexpr int kESmem = kOffOrder + 4 * kOrderMax;
+// paged prefix: raw stages of a tile's NVFP4 groups, the K halves (codes and
+// scales, 1,152 B of each 2,304-B group) single, the V halves double-buffered
+// (V is needed a softmax later than K, so its copies get the longer lead)
+constexpr int kGroupBytes = 2304, kHalfGroup = 1152;
+constexpr int kRawHalf = 8 * kHalfGroup;       // one tile's K (or V) halves
+constexpr int kOffRawK = kESmem;
+constexpr int kOffRawV = kOffRawK + kRawHalf;  // [2]
+constexpr int kESmemPaged = kOffRawV + 2 * kRawHalf;
+static_assert(kOffRawK % 16 == 0 && kRawHalf % 16 == 0, "bulk copies need 16-byte aligned destinations");
+static_assert(kESmemPaged <= 227 * 1024, "paged extend exceeds the shared memory of a CTA");
 // TMEM columns: S_w at 128w (FP32; P_w as BF16 pairs over its first 64 columns), O_w at 256 + 128w
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 256;
@@ -158,6 +169,7 @@ __global__ void __launch_bounds__(kPaged ? kEThreadsPaged : kEThreads, 1)
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBar);
     uint64_t *k_full = bars, *v_full = bars + 2, *s_done = bars + 4, *p_full = bars + 6, *pv_done = bars + 8;
     uint64_t *drain = bars + 10, *k_go = bars + 11, *v_go = bars + 13, *k_dq = bars + 15, *v_dq = bars + 17;
+    uint64_t *rawk_full = bars + 19, *rawv_full = bars + 20, *rawk_free = bars + 22, *rawv_free = bars + 23;
     uint32_t &tmem_base = *reinterpret_cast<uint32_t *>(smem + kOffTmem);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffAbort);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -253,7 +265,8 @@ __global__ void __launch_bounds__(kPaged ? kEThreadsPaged : kEThreads, 1)
 
     if (warp == 0) tc_alloc(&tmem_base, kTmemCols);
     if (tid == kSoftThreads) {
-        for (int j = 0; j < kNumBars; j++) mbar_init(&bars[j], (j == 6 || j == 7) ? kQRows : j >= 15 ? kDqThreads : 1);
+        for (int j = 0; j < kNumBars; j++)
+            mbar_init(&bars[j], (j == 6 || j == 7) ? kQRows : ((j >= 15 && j < 19) || j >= 22) ? kDqThreads : 1);
         *abort_flag = 0;
         fence_mbar_init();
         for (int j = 0; j < 2 && j < nt; j++) {
@@ -380,57 +393,101 @@ __global__ void __launch_bounds__(kPaged ? kEThreadsPaged : kEThreads, 1)
         const int32_t *bt = a.block_table + (int64_t)r * a.max_pages;
         constexpr int kBlocks = kKeys * 8;  // 16-value blocks of one K (or V) tile
         constexpr int kPer = (kBlocks + kDqThreads - 1) / kDqThreads;
-        // item n = K (n even) or V (n odd) of prefix tile n / 2; its page data is
-        // loaded one item ahead (the loads need no free slot), zeros past the prefix
-        struct Raw {
-            uint2 codes[kPer];
-            uint32_t sb[kPer];
+        // Tile j's eight 16-token groups are bulk-copied in halves (K codes and
+        // scales, V codes and scales: 1,152 B each) into raw stages by lanes 0..7
+        // of the first dequantising warp as soon as a stage is free: the K halves
+        // one tile ahead, the V halves two.  Groups past the prefix are not copied
+        // (those keys are written as zeros); a group of an invalid page is
+        // zero-filled and flagged.
+        auto issue_raw = [&](int j, int which, uint8_t *dst, uint64_t *bar) {  // the first dequantising warp
+            const int g = lane, tok = j * kKeys + 16 * g;
+            int32_t pg = -1;
+            if (g < 8 && tok < np) {
+                pg = __ldg(bt + (tok >> a.log2P));
+                if (pg < 0 || pg >= a.num_pages) {
+                    flag_error(a.err, kErrPage);
+                    uint4 *z = reinterpret_cast<uint4 *>(dst + g * kHalfGroup);
+                    for (int i = 0; i < kHalfGroup / 16; i++) z[i] = make_uint4(0u, 0u, 0u, 0u);
+                    pg = -1;
+                }
+            }
+            const unsigned copies = __popc(__ballot_sync(0xffffffffu, pg >= 0));
+            __syncwarp();
+            if (lane == 0) mbar_arrive_expect_tx(bar, copies * kHalfGroup);
+            __syncwarp();
+            if (pg >= 0)
+                bulk_g2s(dst + g * kHalfGroup,
+                         a.pool + ((int64_t)pg * a.Hkv + kv) * a.slab + ((tok & (a.P - 1)) >> 4) * kGroupBytes +
+                             which * kHalfGroup,
+                         kHalfGroup, bar);
         };
-        auto fetch = [&](int n, Raw &raw) {
-            const int j = n >> 1, which = n & 1;
+        uint8_t *rawk = smem + kOffRawK, *rawv = smem + kOffRawV;
+        const bool issuer = warp == kEThreads / 32;
+        // tiles whose halves were requested / seen landed (for the drain after an abort)
+        int k_req = 0, k_seen = 0, v_req = 0, v_seen = 0;
+        if (issuer) {
+            for (int j = 0; j < 2 && j < nt_pre; j++) issue_raw(j, 1, rawv + j * kRawHalf, &rawv_full[j]);
+            v_req = nt_pre < 2 ? nt_pre : 2;
+            if (nt_pre > 0) {
+                issue_raw(0, 0, rawk, rawk_full);
+                k_req = 1;
+            }
+        }
+        bool ok = true;
+        for (int j = 0; ok && j < nt_pre; j++) {
+            const int s = j & 1;
+            for (int which = 0; which < 2; which++) {
+                uint64_t *landed = which ? &rawv_full[s] : rawk_full;
+                const uint32_t lph = (uint32_t)((which ? j >> 1 : j) & 1);
+                ok = __all_sync(0xffffffffu, spin_wait(landed, lph, abort_flag));
+                if (!ok) break;
+                if (which) v_seen = j + 1;
+                else k_seen = j + 1;
+                ok = __all_sync(0xffffffffu,
+                                spin_wait(which ? &v_go[s] : &k_go[s], (uint32_t)((j >> 1) & 1), abort_flag));
+                if (!ok) break;
+                const uint8_t *src = which ? rawv + s * kRawHalf : rawk;
+                uint8_t *tile = smem + (which ? kOffV : kOffK) + s * kKVTile;
 #pragma unroll
-            for (int i = 0; i < kPer; i++) {
-                const int b = dt + i * kDqThreads, key = b >> 3, blk = b & 7, tok = j * kKeys + key;
-                raw.codes[i] = make_uint2(0u, 0u);
-                raw.sb[i] = 0u;
-                if (b < kBlocks && tok < np) {
-                    const int32_t pg = __ldg(bt + (tok >> a.log2P));
-                    if (pg >= 0 && pg < a.num_pages) {
-                        const uint8_t *grp =
-                            a.pool + ((int64_t)pg * a.Hkv + kv) * a.slab + ((tok & (a.P - 1)) >> 4) * 2304;
-                        const int rr = tok & 15;
-                        raw.codes[i] = __ldg(reinterpret_cast<const uint2 *>(grp + (which ? 1152 : 0) + rr * 64 + blk * 8));
-                        raw.sb[i] = __ldg(grp + (which ? 2176 + blk * 16 + rr : 1024 + rr * 8 + blk));
-                    } else if (blk == 0) {
-                        flag_error(a.err, kErrPage);
+                for (int i = 0; i < kPer; i++) {
+                    const int b = dt + i * kDqThreads;
+                    if (b >= kBlocks) continue;
+                    const int key = b >> 3, blk = b & 7, tok = j * kKeys + key;
+                    uint32_t o[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+                    if (tok < np) {
+                        const uint8_t *grp = src + (key >> 4) * kHalfGroup;  // codes [16][64] then scales
+                        const int rr = key & 15;
+                        const uint2 codes = *reinterpret_cast<const uint2 *>(grp + rr * 64 + blk * 8);
+                        const uint32_t sb = grp[1024 + (which ? blk * 16 + rr : rr * 8 + blk)];
+                        nvfp4_block_to_bf16(codes, sb, which ? a.gv : a.gk, o);
+                    }
+                    uint8_t *cb = tile + (blk >> 2) * kKVBlock;  // column block of head_dim 64 (blk / 4) ..
+                    *reinterpret_cast<uint4 *>(cb + sw128_off(key, (blk & 3) * 2)) = make_uint4(o[0], o[1], o[2], o[3]);
+                    *reinterpret_cast<uint4 *>(cb + sw128_off(key, (blk & 3) * 2 + 1)) =
+                        make_uint4(o[4], o[5], o[6], o[7]);
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the tile for the tensor core
+                mbar_arrive(which ? &v_dq[s] : &k_dq[s]);
+                // the raw half is read: the tile after next (K) or the next (V) may land in it
+                mbar_arrive(which ? &rawv_free[s] : rawk_free);
+                const int jn = which ? j + 2 : j + 1;
+                if (issuer && jn < nt_pre) {
+                    ok = __all_sync(0xffffffffu, spin_wait(which ? &rawv_free[s] : rawk_free, lph, abort_flag));
+                    if (!ok) break;
+                    if (which) {
+                        issue_raw(jn, 1, rawv + s * kRawHalf, &rawv_full[s]);
+                        v_req = jn + 1;
+                    } else {
+                        issue_raw(jn, 0, rawk, rawk_full);
+                        k_req = jn + 1;
                     }
                 }
             }
-        };
-        const int items = 2 * nt_pre;
-        Raw cur, nxt;
-        if (items > 0) fetch(0, cur);
-        bool ok = true;
-        for (int n = 0; n < items; n++) {
-            const int j = n >> 1, which = n & 1, s = j & 1;
-            if (n + 1 < items) fetch(n + 1, nxt);
-            ok = __all_sync(0xffffffffu, spin_wait(which ? &v_go[s] : &k_go[s], (uint32_t)((j >> 1) & 1), abort_flag));
-            if (!ok) break;
-            uint8_t *tile = smem + (which ? kOffV : kOffK) + s * kKVTile;
-#pragma unroll
-            for (int i = 0; i < kPer; i++) {
-                const int b = dt + i * kDqThreads;
-                if (b >= kBlocks) continue;
-                const int key = b >> 3, blk = b & 7;
-                uint32_t o[8];
-                nvfp4_block_to_bf16(cur.codes[i], cur.sb[i], which ? a.gv : a.gk, o);
-                uint8_t *cb = tile + (blk >> 2) * kKVBlock;  // column block of head_dim 64 (blk / 4) ..
-                *reinterpret_cast<uint4 *>(cb + sw128_off(key, (blk & 3) * 2)) = make_uint4(o[0], o[1], o[2], o[3]);
-                *reinterpret_cast<uint4 *>(cb + sw128_off(key, (blk & 3) * 2 + 1)) = make_uint4(o[4], o[5], o[6], o[7]);
-            }
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the tile for the tensor core
-            mbar_arrive(which ? &v_dq[s] : &k_dq[s]);
-            cur = nxt;
+        }
+        if (issuer) {  // no copy may still be writing when the CTA frees its memory
+            for (int j = k_seen; j < k_req; j++) mbar_wait_bounded(rawk_full, (uint32_t)(j & 1), kWaitLimitE, nullptr);
+            for (int j = v_seen; j < v_req; j++)
+                mbar_wait_bounded(&rawv_full[j & 1], (uint32_t)((j >> 1) & 1), kWaitLimitE, nullptr);
         }
         if (!ok) {
             *abort_flag = 1;
@@ -627,13 +684,13 @@ cudaError_t launch_extend_kernel(const ExtendMaps &maps, const ExtendArgs &a, in
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!attr_set[dev]) {
         e = cudaFuncSetAttribute(reinterpret_cast<const void *>(&extend_kernel<kPaged>),
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kESmem);
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kPaged ? kESmemPaged : kESmem);
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
     const int64_t qtiles = ceil_div64((int64_t)max_q_len * a.G, kCtaRows);
     dim3 grid((unsigned)qtiles, (unsigned)num_kv_heads, (unsigned)num_reqs);
-    extend_kernel<kPaged><<<grid, kPaged ? kEThreadsPaged : kEThreads, kESmem, stream>>>(maps, a);
+    extend_kernel<kPaged><<<grid, kPaged ? kEThreadsPaged : kEThreads, kPaged ? kESmemPaged : kESmem, stream>>>(maps, a);
     return cudaGetLastError();
 }
 
