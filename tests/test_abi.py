@@ -121,3 +121,30 @@ def test_status_strings(m):
     for s in (0, -1, -2, -3, -4):
         assert lib.nvfp4kv_status_string(s)
     assert lib.nvfp4kv_version() >= 100
+
+
+def test_paged_extend_and_launch_count_arguments(m):
+    lib = m.library()
+    d = ctypes.byref(_desc(m))
+    f8 = ctypes.byref(_desc(m, dtype=1))
+    P = ctypes.c_void_p
+    # paged extend: (cache, q, block_table, max_pages, prefix_lens, k_chunk, v_chunk, cu_q, total_q, num_reqs,
+    # max_q_len, num_q_heads, sm_scale, out, stream)
+    args = [P(4096), P(4096), 4, P(4096), P(4096), P(4096), P(4096), 16, 1, 16, 8, 0.1, P(4096), None]
+    ok_args = list(args)
+    assert lib.nvfp4_extend_attention_paged(f8, *ok_args) == -2  # an NVFP4 pool only
+    bad = list(args); bad[10] = 3                                # heads not a multiple of kv heads
+    assert lib.nvfp4_extend_attention_paged(d, *bad) == -1
+    bad = list(args); bad[2] = 0                                 # no pages per request
+    assert lib.nvfp4_extend_attention_paged(d, *bad) == -1
+    bad = list(args); bad[0] = P(4098)                           # misaligned q
+    assert lib.nvfp4_extend_attention_paged(d, *bad) == -1
+    bad = list(args); bad[11] = float("nan")
+    assert lib.nvfp4_extend_attention_paged(d, *bad) == -1
+    bad = list(args); bad[8] = 0                                 # no requests: nothing to do
+    assert lib.nvfp4_extend_attention_paged(d, *bad) == 0
+    # launch count: plan + decode + reduction, plus the shared-prefix kernel for a cascade call
+    assert lib.nvfp4kv_decode_launch_count(d, 4, 8, 0, 0) == 3
+    assert lib.nvfp4kv_decode_launch_count(d, 4, 8, 0, 128) == 4
+    assert lib.nvfp4kv_decode_launch_count(d, 0, 8, 0, 0) == 0
+    assert lib.nvfp4kv_decode_launch_count(d, 4, 3, 0, 0) == 0
