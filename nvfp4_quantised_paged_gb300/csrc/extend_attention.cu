@@ -17,8 +17,8 @@
 //
 // One CTA = 256 query rows of one (request, kv head), row = chunk token * G +
 // query head of the group, so the G heads that share a KV head share every
-// K/V tile; one CTA per SM (192 KB of shared memory, all 512 TMEM columns).
-// Nine warps:
+// K/V tile; one CTA per SM (193 KB of shared memory, 211 KB with the paged
+// prefix; all 512 TMEM columns).  Nine warps (twelve with the paged prefix):
 //   * warpgroup w (warps 4w .. 4w + 3, w = 0, 1), one thread per row of query
 //     tile w = one TMEM lane, runs the softmax of that tile: wait for S_w(j)
 //     (128 scores per row, FP32 in TMEM columns 128w ..), load it, mask edge
@@ -36,7 +36,15 @@
 //     while warpgroup 0 works on tile j + 1 the tensor core runs the products
 //     of query tile 1, and the other way round.
 // K and V have two-slot rings each; K(j + 2) is requested once S1(j) is done,
-// V(j + 1) once O1 += P1(j - 1) V(j - 1) is done.  Every wait is bounded; a
+// V(j + 1) once O1 += P1(j - 1) V(j - 1) is done.  The MMA thread issues
+// whatever is ready for either query tile, polling the barriers.
+//
+// Two instantiations: the prefix as BF16 workspace rows loaded by TMA
+// (extend_kernel<false>), or read from the NVFP4 pages of the cache
+// (extend_kernel<true>): three more warps then bulk-copy each prefix tile's
+// NVFP4 groups into raw shared-memory stages and expand them into the K / V
+// slots in BF16 (as the prefix dequant kernel would), so the result is the
+// same bit for bit and no workspace is written.  Every wait is bounded; a
 // timeout is recorded in the device error word and ends every warp's loop.
 #include <cuda.h>
 
