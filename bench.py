@@ -55,7 +55,7 @@ def parse_args():
     p.add_argument("--num-splits", type=int, default=0)
     p.add_argument("--batch", type=int, default=64,
                    help="sequences of the 32K workload (64 = the benchmark; smaller = a profiling case)")
-    p.add_argument("--comparison", choices=["extend", "agent_decode", "append", "calibrate"], default=None,
+    p.add_argument("--comparison", choices=["extend", "agent_decode", "agent_step", "append", "calibrate"], default=None,
                    help="run only this comparison (its own JSON line; a profiling case) and exit")
     return p.parse_args()
 
@@ -227,11 +227,26 @@ def oracle_decode_sample(w, nseq, seed_device="cpu"):
     sl = w.seq_lens[:nseq].numpy()
     cores = os.cpu_count() or 1
 
-    def run():
-        return oracle.decode_attention(pool, q, bt.numpy(), sl, w.sm_scale, nthreads=cores)
+    def run(nthreads=cores):
+        return oracle.decode_attention(pool, q, bt.numpy(), sl, w.sm_scale, nthreads=nthreads)
 
     nbytes = decode_bytes(nseq, int(w.seq_lens[0]), w.num_q_heads, w.num_kv_heads, w.max_pages, 144)
     return run, nbytes, cores
+
+
+def cpu_model():
+    """The host CPU as /proc/cpuinfo names it (x86 'model name', Arm implementer / part)."""
+    try:
+        info = open("/proc/cpuinfo").read()
+    except OSError:
+        return "unknown"
+    for key in ("model name", "Model"):
+        for ln in info.splitlines():
+            if ln.startswith(key):
+                return ln.split(":", 1)[1].strip()
+    impl = [ln.split(":", 1)[1].strip() for ln in info.splitlines() if ln.startswith("CPU implementer")]
+    part = [ln.split(":", 1)[1].strip() for ln in info.splitlines() if ln.startswith("CPU part")]
+    return "Arm implementer %s part %s" % (impl[0] if impl else "?", part[0] if part else "?")
 
 
 def cpu_baseline(w, seed_device):
@@ -247,11 +262,23 @@ def cpu_baseline(w, seed_device):
         if time.perf_counter() - t0 > 10.0:
             break
     dt = (time.perf_counter() - t0) / reps
+    # one thread on one sequence (all its kv heads), a few seconds of work
+    run1, nbytes1, _ = oracle_decode_sample(w, 1, seed_device)
+    t1 = time.perf_counter()
+    reps1 = 0
+    while True:
+        run1(nthreads=1)
+        reps1 += 1
+        if time.perf_counter() - t1 > 3.0:
+            break
+    dt1 = (time.perf_counter() - t1) / reps1
     return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
             "sample": "%d of %d sequences (%d (seq, kv_head) units of %d tokens), fp64 decode over the oracle's "
                       "own NVFP4 pool, %d repetitions" % (nseq, w.batch, nseq * w.num_kv_heads,
                                                           int(w.seq_lens[0]), reps),
-            "ms_per_sample": dt * 1e3}
+            "ms_per_sample": dt * 1e3, "cpu_model": cpu_model(),
+            "single_thread": {"value": nbytes1 / dt1 / 1e9, "unit": "GB/s", "ms_per_sample": dt1 * 1e3,
+                              "sample": "1 sequence x %d kv heads, %d repetitions" % (w.num_kv_heads, reps1)}}
 
 
 def run_reference(args):
@@ -509,6 +536,67 @@ def time_agent_decode(m, device, steps, warmup):
     return res
 
 
+def time_agent_step(m, device, steps, warmup):
+    """One step of the whole agent mix: cascade decode of the 128 sequences, then
+    path 2 of the 8 extends (prefix dequant, extend attention, quantise-append of
+    their chunks)."""
+    import torch
+
+    import workloads
+    mix = workloads.agent_mix()
+    w = mix.decode
+    P = w.page_size
+    cache = m.PagedCache(w.num_pages, P, w.num_kv_heads, device=device)
+    fill_cache(m, w, cache, device)  # decode rows, and the extend rows' prefixes
+    dec, rows = list(range(mix.num_decode)), mix.extend_rows()
+    q = w.q(device)[dec].contiguous()
+    bt_d, sl_d = w.block_table[dec].contiguous().to(device), w.seq_lens[dec].contiguous().to(device)
+    shared = w.shared_prefix_tokens
+    sp = w.block_table[0, :shared // P].contiguous().to(device)
+    ws = torch.empty(max(m.cascade_workspace_bytes(cache, len(dec), w.num_q_heads, shared), 256), dtype=torch.uint8,
+                     device=device)
+    pl = w.seq_lens[rows].contiguous()
+    cu_p = torch.zeros(len(rows) + 1, dtype=torch.int32)
+    cu_p[1:] = torch.cumsum(pl, 0)
+    total = int(cu_p[-1])
+    bt_e, pl_d, cu_p_d = w.block_table[rows].contiguous().to(device), pl.to(device), cu_p.to(device)
+    L = mix.chunk_tokens
+    qc = torch.cat([mix.chunk_q(r, device) for r in range(len(rows))])
+    kn = torch.cat([mix.chunk_kv(r, device)[0] for r in range(len(rows))])
+    vn = torch.cat([mix.chunk_kv(r, device)[1] for r in range(len(rows))])
+    cu_q = torch.arange(0, L * (len(rows) + 1), L, dtype=torch.int32, device=device)
+    slots_c = torch.cat([mix.chunk_slots(r) for r in range(len(rows))]).to(device)
+    kw, vw = m.prefix_dequant(cache, bt_e, pl_d, cu_p_d, total)
+    out_d, out_e = torch.empty_like(q), torch.empty_like(qc)
+
+    def step():
+        m.cascade_decode_attention(cache, q, sp, shared, bt_d, sl_d, w.sm_scale, out=out_d, workspace=ws)
+        m.prefix_dequant(cache, bt_e, pl_d, cu_p_d, total, k_ws=kw, v_ws=vw)
+        m.extend_attention(qc, kw, vw, cu_p_d, kn, vn, cu_q, L, w.sm_scale, out=out_e)
+        m.quantize_append(cache, kn, vn, slots_c)
+
+    for _ in range(warmup):
+        step()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    s.record()
+    for _ in range(steps):
+        step()
+    e.record()
+    torch.cuda.synchronize()
+    assert m.check_device_errors() == 0
+    us = s.elapsed_time(e) / steps * 1e3
+    Hkv = w.num_kv_heads
+    unique = (int(sl_d.sum()) - (len(dec) - 1) * shared) * Hkv * 144   # decode: the shared pages counted once
+    extend_bytes = total * Hkv * (144 + 4 * 128) + len(rows) * L * Hkv * (512 + 144)
+    flops = extend_flops([int(x) for x in pl], L, w.num_q_heads // Hkv, Hkv)
+    del cache
+    torch.cuda.empty_cache()
+    return {"workload": "agent mix step: cascade decode of 128 sequences + path 2 of 8 extends of 512 tokens",
+            "us_per_step": us, "unique_bytes_per_step": unique + extend_bytes,
+            "unique_gb_per_s": (unique + extend_bytes) / us / 1e3, "extend_flops_per_step": flops}
+
+
 def run_ours(args):
     import torch
 
@@ -578,7 +666,9 @@ def run_ours(args):
     sampler.stop()
     assert m.check_device_errors() == 0
     ms_step = max_over_ranks(dist, ev0.elapsed_time(ev1) / K)
-    dec_us = max_over_ranks(dist, sum(b.elapsed_time(a) for b, a in zip(before, after)) / n_prof * 1e3)
+    dec_samples = sorted(b.elapsed_time(a) * 1e3 for b, a in zip(before, after))
+    dec_us = max_over_ranks(dist, sum(dec_samples) / n_prof)
+    dec_median_us = max_over_ranks(dist, dec_samples[len(dec_samples) // 2])
 
     dbytes = decode_bytes(B, S, Hq, Hkv, w.max_pages, 144)
     abytes = append_bytes(B, Hkv, 144)
@@ -646,7 +736,7 @@ def run_ours(args):
         "gpu_launches": m.decode_launch_count(cache, B, Hq, args.num_splits) * K,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic, "peak_kind": peak_kind,
-                     "kernel": "decode_kernel<nvfp4>", "us_per_launch": dec_us,
+                     "kernel": "decode_kernel<nvfp4>", "us_per_launch": dec_us, "median_us_per_launch": dec_median_us,
                      "timed_launches": n_prof, "algorithmic_bytes_per_launch": dbytes},
         "clocks": sampler.summary(t_wall0, t_wall1),
     }
@@ -672,6 +762,7 @@ def run_ours(args):
         comp["calibrate_65k"] = time_calibrate(m, device, 50, 5)
         comp["extend_agent_mix"] = time_extend(m, device, 10, 2, load_bf16_peak())
         comp["decode_agent_mix"] = time_agent_decode(m, device, 20, 3)
+        comp["agent_mix_step"] = time_agent_step(m, device, 10, 2)
         line["comparisons"] = comp
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -693,6 +784,8 @@ def run_comparison(args):
         res = time_append(m, device, args.steps, args.warmup)
     elif args.comparison == "calibrate":
         res = time_calibrate(m, device, args.steps, args.warmup)
+    elif args.comparison == "agent_step":
+        res = time_agent_step(m, device, args.steps, args.warmup)
     else:
         res = time_agent_decode(m, device, args.steps, args.warmup)
     print(json.dumps({"comparison": args.comparison, **res}), flush=True)
