@@ -640,7 +640,6 @@ __global__ void __launch_bounds__(kThreads, DTYPE == NVFP4KV_DTYPE_NVFP4 && NT =
     using S = Smem<DTYPE>;
     extern __shared__ __align__(128) uint8_t smem[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    pdl_launch_dependents();  // the reduction may be scheduled once every CTA runs
     // chunk_prefix comes from the plan kernel.  Behind the shared-prefix
     // kernel, this grid starts only once every CTA of that kernel has waited
     // for the plan to complete (and flush) and then triggered, so the plan's
@@ -648,6 +647,9 @@ __global__ void __launch_bounds__(kThreads, DTYPE == NVFP4KV_DTYPE_NVFP4 && NT =
     // the decode then runs beside the shared-prefix kernel, and its own
     // completion, which the reduction waits for, implies that kernel's.
     if (!a.after_shared) pdl_wait();
+    // The reduction may be scheduled once every CTA is past this point, so
+    // with the plan complete: it reads chunk_prefix before its own wait.
+    pdl_launch_dependents();
 
     const int64_t U = (int64_t)a.Hkv * a.chunk_prefix[a.B];
     const int64_t c = blockIdx.x;
@@ -898,40 +900,73 @@ constexpr int kReduceWarps = 8;
 
 __device__ __forceinline__ float lse_factor(float m, float mx) { return m == kNegInf ? 0.f : ex2(m - mx); }
 
+// n / d for n >= 0, d > 0; in 32 bits when both fit, the usual case.
+__device__ __forceinline__ int64_t udiv64(int64_t n, int64_t d) {
+    if ((((uint64_t)n | (uint64_t)d) >> 32) == 0) return (int64_t)((uint32_t)n / (uint32_t)d);
+    return n / d;
+}
+
 __global__ void __launch_bounds__(32 * kReduceWarps) reduce_kernel(ReduceArgs a, int wpr) {
     __shared__ float4 s_acc[kReduceWarps][32];
     __shared__ float s_m[kReduceWarps], s_l[kReduceWarps];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    pdl_wait();  // partials come from the decode kernel
     const int64_t row = (int64_t)blockIdx.x * (kReduceWarps / wpr) + warp / wpr;
     const int sub = warp % wpr;  // this warp's share of the row's partials
     const bool live = row < (int64_t)a.B * a.Hq;
+    // Where the row's pair p = b * Hkv + kv lies, found before the wait: the
+    // decode kernel lets this grid launch only once the plan that wrote
+    // chunk_prefix is complete, so the arithmetic overlaps the decode's last
+    // CTAs (loads through L2: the values come from an earlier grid).  The
+    // pair's units [off, off + nch) of the flat order are covered by CTAs
+    // c0 .. c1, CTA c owning units [c U / grid, (c + 1) U / grid); lo0 .. hi0
+    // are the pair's units within CTA c0's range, 0 .. hi1 within CTA c1's.
+    int b = 0, kv = 0, hh = 0;
+    int64_t p = 0, U = 0, nch = 0, off = 0, c0 = 0, c1 = -1, lo0 = 0, hi0 = 0, hi1 = 0;
+    if (live) {
+        b = (int)(row / a.Hq);
+        const int h = (int)(row % a.Hq);
+        kv = h / a.G;
+        hh = h % a.G;
+        p = (int64_t)b * a.Hkv + kv;
+        const long long *cp = reinterpret_cast<const long long *>(a.chunk_prefix);
+        const int64_t pb = __ldcg(cp + b);
+        nch = __ldcg(cp + b + 1) - pb;
+        U = (int64_t)a.Hkv * __ldcg(cp + a.B);
+        if (nch > 0) {
+            off = (int64_t)a.Hkv * pb + (int64_t)kv * nch;
+            c0 = udiv64((off + 1) * a.grid - 1, U);
+            c1 = udiv64((off + nch) * a.grid - 1, U);
+            const int64_t a0 = udiv64(c0 * U, a.grid), e0 = udiv64((c0 + 1) * U, a.grid);
+            lo0 = off - a0;
+            hi0 = (off + nch < e0 ? off + nch : e0) - a0;
+            hi1 = off + nch - udiv64(c1 * U, a.grid);
+        }
+    }
+    // With every CTA's range at least two units long, a CTA strictly between
+    // c0 and c1 holds two or more of the pair's units, so both of its warps
+    // left a partial; otherwise each candidate CTA's range is recomputed.
+    const bool dense = U >= 2 * (int64_t)a.grid;
+    pdl_wait();  // partials come from the decode kernel
     float m_w = kNegInf, l_w = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    int64_t nch = 0;
     if (live) {
-        const int b = (int)(row / a.Hq), h = (int)(row % a.Hq);
-        const int kv = h / a.G, hh = h % a.G;
-        nch = a.chunk_prefix[b + 1] - a.chunk_prefix[b];
-        const int64_t p = (int64_t)b * a.Hkv + kv;
         const int64_t ncasc = a.casc_ml ? a.casc_splits : 0;
-        int64_t c0 = 0, c1 = -1, off = 0;
-        const int64_t U = (int64_t)a.Hkv * a.chunk_prefix[a.B];
-        if (nch > 0) {
-            off = (int64_t)a.Hkv * a.chunk_prefix[b] + (int64_t)kv * nch;
-            c0 = ((off + 1) * a.grid - 1) / U;
-            c1 = ((off + nch) * a.grid - 1) / U;
-        }
         // Candidate partials: first the ncasc shared-prefix partials of the pair,
         // then (CTA cc, warp w) for cc in [c0, c1].  Warp w of CTA cc left one iff
         // the CTA's units of this pair include one with index (within the CTA's
         // range) = w mod kWarps; an empty CTA (possible when grid > U) left none.
-        auto has_partial = [&](int64_t cc, int w) {
-            const int64_t cu0 = cc * U / a.grid, cu1 = (cc + 1) * U / a.grid;
-            const int64_t lo = (off > cu0 ? off : cu0) - cu0;
-            const int64_t hi = (off + nch < cu1 ? off + nch : cu1) - cu0;
+        auto left_one = [](int64_t lo, int64_t hi, int w) {
             if (hi <= lo) return false;
             return hi - lo > (int64_t)((w - lo % kWarps + kWarps) % kWarps);
+        };
+        auto has_partial = [&](int64_t cc, int w) {
+            if (dense) {
+                if (cc == c0) return left_one(lo0, hi0, w);
+                if (cc == c1) return left_one(0, hi1, w);
+                return true;
+            }
+            const int64_t cu0 = udiv64(cc * U, a.grid), cu1 = udiv64((cc + 1) * U, a.grid);
+            return left_one((off > cu0 ? off : cu0) - cu0, (off + nch < cu1 ? off + nch : cu1) - cu0, w);
         };
         const int64_t ncand = ncasc + (c1 - c0 + 1) * kWarps;
         for (int64_t base = sub; base < ncand; base += 4 * wpr) {
@@ -1169,7 +1204,7 @@ cudaError_t launch_decode(const nvfp4kv_cache &c, const void *q, int batch, int 
     // warps per output row from the average number of partials per pair
     const int64_t pairs = (int64_t)batch * c.num_kv_heads;
     const int64_t avg_parts = (grid + 2 * pairs - 1) / pairs * kWarps + csplits;
-    int wpr = avg_parts <= 4 ? 1 : avg_parts <= 8 ? 2 : avg_parts <= 16 ? 4 : 8;
+    int wpr = avg_parts <= 8 ? 1 : avg_parts <= 16 ? 2 : avg_parts <= 32 ? 4 : 8;
     const int64_t rows_per_cta = kReduceWarps / wpr;
     void *rargs[] = {&r, &wpr};
     return launch_pdl(reinterpret_cast<const void *>(&reduce_kernel), (unsigned)ceil_div64(rows, rows_per_cta),
