@@ -153,9 +153,15 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(rows), "note": note}
 
 
-def decode_kernel_traffic():
+def decode_kernel_traffic(batch, num_splits):
     """DRAM bytes per decode-kernel launch from the committed ncu summary, if it
-    was taken on the current kernel source (else None)."""
+    was taken on the current kernel source and covers this batch of the 32K
+    workload with the automatic split (else None)."""
+    if num_splits:
+        return None
+    key = {64: "dram_bytes_per_launch_full_size", 8: "dram_bytes_per_launch_batch8"}.get(batch)
+    if key is None:
+        return None
     src = os.path.join(ROOT, "nvfp4_quantised_paged_gb300", "csrc", "decode_attention.cu")
     summ = os.path.join(ROOT, "profiles", "decode_kernel_dram.txt")
     try:
@@ -166,7 +172,7 @@ def decode_kernel_traffic():
                 k, v = line.split(":", 1)
                 kv[k.strip()] = v.strip()
         if kv.get("kernel_source_sha256_16") == h:
-            return float(kv["dram_bytes_per_launch_full_size"])
+            return float(kv[key])
     except Exception:
         pass
     return None
@@ -772,7 +778,7 @@ def run_ours(args):
 
     peak, peak_kind = peak_hbm()
     achieved = dbytes / (dec_us * 1e-6) / 1e9
-    traffic = decode_kernel_traffic()
+    traffic = decode_kernel_traffic(B, args.num_splits)
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
