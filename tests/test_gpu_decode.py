@@ -40,7 +40,11 @@ def test_decode_page_sizes_and_groups(m, P, Hq, Hkv):
     assert not out[6].float().abs().sum().item()   # empty sequence -> zeros
 
 
-@pytest.mark.parametrize("splits", [1, 3, 7, 64, 500])
+# The workload has 63 + 40 + 1 + 1 = 105 chunks of 64 tokens per kv head, so
+# U = 210 units: 104 and 105 splits give every CTA >= 2 units (the reduction
+# takes interior CTAs' partials without recomputing their ranges), 106 gives
+# some CTAs one unit, 210 exactly one each, 211 and 500 leave CTAs empty.
+@pytest.mark.parametrize("splits", [1, 3, 7, 64, 104, 105, 106, 210, 211, 500])
 def test_split_count_does_not_change_the_result_beyond_tolerance(m, splits):
     w = workloads.make_decode("s", 5, [4000, 2500, 31, 1], 16, 2, 64)
     cache, pool = fill_both(w, m)
