@@ -12,6 +12,8 @@
 // (bit patterns compared as integers; Inf and NaN ignored) accumulated by
 // atomicMax into the two output words, then one thread turning each maximum
 // into g in place (IEEE division; 1.0 when the maximum is 0).
+#include <mutex>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -35,7 +37,8 @@ __device__ __forceinline__ uint32_t amax8(uint4 w) {
     return m;
 }
 
-__global__ void __launch_bounds__(256) amax_kernel(const uint4 *k, const uint4 *v, int64_t num_tokens,
+// Eight CTAs per SM (32 registers): the grid below is one wave of resident CTAs.
+__global__ void __launch_bounds__(256, 8) amax_kernel(const uint4 *k, const uint4 *v, int64_t num_tokens,
                                                    int64_t stride16, int row16, unsigned *out) {
     pdl_launch_dependents();
     const int64_t n = num_tokens * row16;
@@ -96,6 +99,28 @@ __global__ void finalize_kernel(unsigned *words) {
     }
 }
 
+constexpr int kMaxDevices = 64;
+std::mutex g_wave_mu;
+int64_t g_wave[kMaxDevices];  // resident amax CTAs per device (SMs x CTAs per SM), 0 until known
+
+// One wave of resident amax CTAs, so that the grid-stride loop has no tail
+// wave; looked up once per device (the occupancy query costs host time).
+cudaError_t amax_wave(int64_t *wave) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_wave_mu);
+    if (!g_wave[dev]) {
+        int sms = 0, per_sm = 0;
+        if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+        if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, amax_kernel, 256, 0)) != cudaSuccess) return e;
+        g_wave[dev] = (int64_t)sms * (per_sm > 0 ? per_sm : 1);
+    }
+    *wave = g_wave[dev];
+    return cudaSuccess;
+}
+
 }  // namespace
 
 cudaError_t launch_calibrate(const void *k, const void *v, int64_t num_tokens, int num_kv_heads, int64_t token_stride,
@@ -105,11 +130,10 @@ cudaError_t launch_calibrate(const void *k, const void *v, int64_t num_tokens, i
     if (e != cudaSuccess) return e;
     const int row16 = num_kv_heads * (kHeadDim / 8);
     const int64_t n = num_tokens * row16;
-    int dev = 0, sms = 0;
-    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    int64_t wave = 0;
+    if ((e = amax_wave(&wave)) != cudaSuccess) return e;
     const int64_t want = ceil_div64(n, 256);
-    const unsigned grid = (unsigned)(want < (int64_t)sms * 8 ? (want > 0 ? want : 1) : (int64_t)sms * 8);
+    const unsigned grid = (unsigned)(want < wave ? (want > 0 ? want : 1) : wave);
     amax_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint4 *>(k), static_cast<const uint4 *>(v), num_tokens,
                                           token_stride / 8, row16, words);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
