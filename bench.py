@@ -287,6 +287,15 @@ def cpu_baseline(w, seed_device):
                               "sample": "1 sequence x %d kv heads, %d repetitions" % (w.num_kv_heads, reps1)}}
 
 
+def workload_config(w, world):
+    """The workload keys both arms report under "config"."""
+    return {"workload": w.name, "batch": w.batch, "seq_len": int(w.seq_lens[0]), "num_q_heads": w.num_q_heads,
+            "num_kv_heads": w.num_kv_heads, "head_dim": 128, "page_size": w.page_size,
+            "kv_cache": "nvfp4 (e2m1 + e4m3 per 16, tensor scale 1.0)",
+            "l2": "inputs larger than L2 (2.42 GB cache vs 129 MB L2), no flush",
+            "parallelism": "replicas" if world > 1 else "single GPU"}
+
+
 def run_reference(args):
     import workloads
     world, rank, local, dist = init_dist()
@@ -308,7 +317,8 @@ def run_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "sample": sample},
+            "config": dict(workload_config(w, world), step="paged decode attention of the sampled sequences",
+                           sample=sample),
             "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -783,12 +793,9 @@ def run_ours(args):
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f16xf16->f32", "data": "synthetic",
-        "config": {"workload": w.name, "batch": B, "seq_len": S, "num_q_heads": Hq, "num_kv_heads": Hkv,
-                   "head_dim": 128, "page_size": P, "kv_cache": "nvfp4 (e2m1 + e4m3 per 16, tensor scale 1.0)",
-                   "step": "quantize-append of 1 new token per sequence + paged decode attention, one fused call",
-                   "l2": "inputs larger than L2 (2.42 GB cache vs 129 MB L2), no flush",
-                   "parallelism": "replicas" if world > 1 else "single GPU",
-                   "num_splits": args.num_splits or m.decode_auto_splits(cache, Hq)},
+        "config": dict(workload_config(w, world),
+                       step="quantize-append of 1 new token per sequence + paged decode attention, one fused call",
+                       num_splits=args.num_splits or m.decode_auto_splits(cache, Hq)),
         "us_per_step": ms_step * 1e3, "kv_tokens_per_s": kv_tokens_per_s,
         "pct_of_nominal_8tbps": 100.0 * (value / world) / NOMINAL_HBM_GBS,
         "pct_of_measured_hbm": 100.0 * (value / world) / peak,

@@ -56,3 +56,12 @@ def test_no_traffic_without_a_summary(fake_root):
     src.parent.mkdir(parents=True)
     src.write_bytes(b"x")
     assert bench.decode_kernel_traffic(64, 0) is None
+
+
+def test_both_arms_report_the_same_workload_keys():
+    import workloads
+    w = workloads.decode_32k()
+    c = bench.workload_config(w, 1)
+    assert c["workload"] == w.name and c["batch"] == 64 and c["seq_len"] == 32768
+    assert (c["num_q_heads"], c["num_kv_heads"], c["head_dim"], c["page_size"]) == (64, 8, 128, 64)
+    assert c["parallelism"] == "single GPU" and bench.workload_config(w, 4)["parallelism"] == "replicas"
