@@ -175,3 +175,29 @@ def test_prefix_dequant_round_trips_grid_values(dtype):
     for r, n in enumerate(lens):
         assert np.array_equal(bf16_bits_to_f64(kw[cu[r]:cu[r] + n]), ks[r])
         assert np.array_equal(bf16_bits_to_f64(vw[cu[r]:cu[r] + n]), vs[r])
+
+
+@pytest.mark.parametrize("q_gain", [1.0, 300.0, 3.0e4])
+def test_attention_agrees_with_extended_precision_over_wide_score_ranges(q_gain):
+    """Scores up to ~1e7 (q scaled before BF16 rounding): the fp64 oracle must
+    equal a brute-force softmax in extended precision (numpy longdouble,
+    max-shifted) over the same lossless K/V; an unshifted exponential would
+    overflow here."""
+    if np.finfo(np.longdouble).eps >= np.finfo(np.float64).eps:
+        pytest.skip("no extended precision on this host")
+    rng = np.random.default_rng(int(q_gain) + 7)
+    lens, Hq, Hkv, P = [45, 130], 8, 2, 16
+    pool, bt, ks, vs = build_cache(rng, lens, Hkv, P)
+    q_bits = to_bf16_bits(rng.standard_normal((len(lens), Hq, 128)) * q_gain)
+    out = oracle.decode_attention(pool, q_bits, bt, np.array(lens, dtype=np.int32), SM, nthreads=2)
+    q = bf16_bits_to_f64(q_bits).astype(np.longdouble)
+    G = Hq // Hkv
+    for b, n in enumerate(lens):
+        k = ks[b].astype(np.longdouble)
+        v = vs[b].astype(np.longdouble)
+        for h in range(Hq):
+            kv = h // G
+            s = (k[:, kv, :] @ q[b, h]) * np.longdouble(SM)
+            p = np.exp(s - s.max())
+            ref = (p[:, None] * v[:, kv, :]).sum(axis=0) / p.sum()
+            np.testing.assert_allclose(out[b, h], ref.astype(np.float64), rtol=1e-11, atol=1e-11 * float(np.abs(ref).max()))
