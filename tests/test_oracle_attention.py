@@ -131,6 +131,11 @@ def test_sequence_attention_agrees_with_paged_attention():
         o = oracle.sequence_attention(q[0, kv * 5:(kv + 1) * 5], to_bf16_bits(ks[0][:, kv]),
                                       to_bf16_bits(vs[0][:, kv]), SM)
         assert np.array_equal(o, out[0, kv * 5:(kv + 1) * 5])
+        # rows wider than one head (the head's 128 values at each row start)
+        kr = to_bf16_bits(ks[0].reshape(lens[0], -1))[:, kv * 128:]
+        vr = to_bf16_bits(vs[0].reshape(lens[0], -1))[:, kv * 128:]
+        o = oracle.sequence_attention(q[0, kv * 5:(kv + 1) * 5], kr, vr, SM)
+        assert np.array_equal(o, out[0, kv * 5:(kv + 1) * 5])
 
 
 def test_fp8_cache_attention_equals_sdpa_on_e4m3_values():
