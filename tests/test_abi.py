@@ -148,3 +148,17 @@ def test_paged_extend_and_launch_count_arguments(m):
     assert lib.nvfp4kv_decode_launch_count(d, 4, 8, 0, 128) == 4
     assert lib.nvfp4kv_decode_launch_count(d, 0, 8, 0, 0) == 0
     assert lib.nvfp4kv_decode_launch_count(d, 4, 3, 0, 0) == 0
+
+
+def test_binding_refuses_host_tensors(m):
+    """The product path has no CPU fallback: host tensors are rejected before
+    any library call, for the pool and for every per-call input."""
+    import torch
+    with pytest.raises(ValueError):
+        m.PagedCache(4, 16, 1, device="cpu")
+    pool = torch.zeros((4, 1, m.slab_bytes(m.DTYPE_NVFP4, 16)), dtype=torch.uint8)
+    with pytest.raises(ValueError):
+        m.PagedCache(4, 16, 1, pool=pool)
+    k = torch.zeros((2, 1, 128), dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        m.calibrate_global_scales(k, k, 1)
