@@ -818,7 +818,8 @@ def run_ours(args):
         "clocks": sampler.summary(t_wall0, t_wall1),
     }
 
-    if not args.no_comparisons and rank == 0:
+    # single-GPU comparisons: reported at N = 1 only (under torchrun the other GPUs would wait idle)
+    if not args.no_comparisons and rank == 0 and world == 1:
         comp = {"two_call_step": {"ms_per_step": two_call_ms, "value": world * step_bytes / (two_call_ms * 1e-3) / 1e9,
                                   "unit": "GB/s", "note": "quantize_append then paged_decode_attention (4 launches)"}}
         del cache
