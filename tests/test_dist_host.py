@@ -48,3 +48,31 @@ def test_single_process_needs_no_process_group():
     w, r, local, dist = bench.init_dist()
     assert (w, r, dist) == (1, 0, None)
     assert bench.max_over_ranks(None, 3.0) == 3.0
+
+
+def _reference_rank(rank, world, port, outdir):
+    import argparse
+    import contextlib
+    os.environ.update({"RANK": str(rank), "WORLD_SIZE": str(world), "LOCAL_RANK": str(rank),
+                       "MASTER_ADDR": "127.0.0.1", "MASTER_PORT": str(port)})
+    import bench
+    with open(os.path.join(outdir, "rank%d.txt" % rank), "w") as f, contextlib.redirect_stdout(f):
+        bench.run_reference(argparse.Namespace(steps=1, warmup=0, gpus=world))
+
+
+def test_reference_arm_under_two_ranks_prints_one_line_from_rank_zero(tmp_path):
+    import json
+    ctx = mp.get_context("spawn")
+    port = _free_port()
+    procs = [ctx.Process(target=_reference_rank, args=(r, 2, port, str(tmp_path))) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=600)
+        assert p.exitcode == 0
+    assert (tmp_path / "rank1.txt").read_text() == ""
+    lines = (tmp_path / "rank0.txt").read_text().strip().splitlines()
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["e2e"]["h2d_bytes_per_step"] == 0
