@@ -162,3 +162,25 @@ def test_binding_refuses_host_tensors(m):
     k = torch.zeros((2, 1, 128), dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         m.calibrate_global_scales(k, k, 1)
+
+
+def test_header_is_plain_c(tmp_path):
+    """The boundary is a C ABI: the header compiles as C11 (no C++ or torch
+    types), and every declared entry point links against the library from C."""
+    import shutil
+    cuda_inc = "/usr/local/cuda/include"
+    if not shutil.which("gcc") or not os.path.exists(os.path.join(cuda_inc, "cuda_runtime_api.h")):
+        pytest.skip("gcc or the CUDA headers are missing")
+    names = declared_functions()
+    src = tmp_path / "use_header.c"
+    src.write_text('#include "nvfp4kv.h"\ntypedef void (*fn_t)(void);\nstatic const fn_t fns[] = {\n' +
+                   "".join("    (fn_t)&%s,\n" % n for n in names) +
+                   "};\nint main(void) {\n    int ok = 1;\n    for (unsigned i = 0; i < sizeof fns / sizeof fns[0]; i++)"
+                   " ok &= fns[i] != 0;\n    return ok ? 0 : 1;\n}\n")
+    lib = _lib_path()
+    exe = tmp_path / "use_header"
+    r = subprocess.run(["gcc", "-std=c11", "-Wall", "-Werror", "-pedantic", "-I", os.path.join(ROOT, "include"),
+                        "-I", cuda_inc, str(src), "-o", str(exe), "-L", os.path.dirname(lib), "-lnvfp4kv",
+                        "-Wl,-rpath," + os.path.dirname(lib)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    assert subprocess.run([str(exe)]).returncode == 0
