@@ -184,3 +184,49 @@ def test_header_is_plain_c(tmp_path):
                         "-Wl,-rpath," + os.path.dirname(lib)], capture_output=True, text=True)
     assert r.returncode == 0, r.stderr
     assert subprocess.run([str(exe)]).returncode == 0
+
+
+def _declared_signatures():
+    """{name: (return C type, [parameter C types])} parsed from the header."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    sigs = {}
+    for ret, name, params in re.findall(r"NVFP4KV_API\s+([\w\s\*]+?)\s*\b(nvfp4\w+)\s*\(([^)]*)\)\s*;", text):
+        params = " ".join(params.split())
+        types = [] if params in ("", "void") else [re.sub(r"\s*\b\w+$", "", p.strip()) for p in params.split(",")]
+        sigs[name] = (ret.strip(), types)
+    return sigs
+
+
+def _ctype_of(c):
+    """The ctypes class a C parameter type must be declared with."""
+    if c.replace(" ", "") == "constnvfp4kv_cache*":
+        return "desc"
+    if "*" in c or c in ("cudaStream_t",):
+        return ctypes.c_void_p
+    return {"int": ctypes.c_int, "unsigned": ctypes.c_uint, "int64_t": ctypes.c_int64, "size_t": ctypes.c_size_t,
+            "float": ctypes.c_float}[c]
+
+
+def test_binding_argtypes_match_the_header(m):
+    """Every ctypes signature of the binding has the header's parameter count
+    and types (a mismatch would shift arguments silently)."""
+    lib = m.library()
+    sigs = _declared_signatures()
+    assert set(sigs) == set(declared_functions())
+    for name, (ret, params) in sigs.items():
+        fn = getattr(lib, name)
+        assert len(fn.argtypes) == len(params), name
+        for got, c in zip(fn.argtypes, params):
+            want = _ctype_of(c)
+            if want == "desc":
+                assert got is ctypes.POINTER(m._CacheDesc), (name, c)
+            else:
+                assert got is want, (name, c, got)
+        want_ret = {"int": ctypes.c_int, "size_t": ctypes.c_size_t, "const char *": ctypes.c_char_p}[ret]
+        assert fn.restype is want_ret, (name, ret)
+
+
+def test_noalloc_scratch_size_matches_the_header(m):
+    text = open(HEADER).read()
+    mo = re.search(r"#define\s+NVFP4KV_NOALLOC_SCRATCH_BYTES\s+\((\d+)u\s*<<\s*(\d+)\)", text)
+    assert mo and m.NOALLOC_SCRATCH_BYTES == int(mo.group(1)) << int(mo.group(2))
