@@ -42,6 +42,7 @@ METRIC = "NVFP4 paged decode-attn: HBM GB/s (% of GB300 peak), KV-tokens/s, µs/
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 PROFILE_EVERY = 8   # decode-kernel events on every 8th timed step (events between launches cost overlap)
+ROOFLINE_LAUNCHES = 256   # decode launches timed one by one after the timed region, whatever --steps is
 
 
 def parse_args():
@@ -679,13 +680,31 @@ def run_ours(args):
     t_wall1 = time.time()
     barrier(dist)
     m.profile_decode([], [])
-    time.sleep(0.1)
-    sampler.stop()
     assert m.check_device_errors() == 0
     ms_step = max_over_ranks(dist, ev0.elapsed_time(ev1) / K)
-    dec_samples = sorted(b.elapsed_time(a) * 1e3 for b, a in zip(before, after))
-    dec_us = max_over_ranks(dist, sum(dec_samples) / n_prof)
-    dec_median_us = max_over_ranks(dist, dec_samples[len(dec_samples) // 2])
+    region_samples = sorted(b.elapsed_time(a) * 1e3 for b, a in zip(before, after))
+    region_us = max_over_ranks(dist, sum(region_samples) / n_prof)
+
+    # the roofline kernel on its own: ROOFLINE_LAUNCHES more steps, each with its
+    # decode-kernel launch bracketed by events (the step's other launches run too)
+    nr = ROOFLINE_LAUNCHES
+    rb = [torch.cuda.Event(enable_timing=True) for _ in range(nr)]
+    ra = [torch.cuda.Event(enable_timing=True) for _ in range(nr)]
+    m.profile_decode(rb, ra, 1)
+    torch.cuda.synchronize()
+    t_roof0 = time.time()
+    for _ in range(nr):
+        step()
+    torch.cuda.synchronize()
+    t_roof1 = time.time()
+    m.profile_decode([], [])
+    assert m.check_device_errors() == 0
+    dec_samples = sorted(b.elapsed_time(a) * 1e3 for b, a in zip(rb, ra))
+    dec_us = max_over_ranks(dist, sum(dec_samples) / nr)
+    dec_median_us = max_over_ranks(dist, dec_samples[nr // 2])
+
+    time.sleep(0.1)
+    sampler.stop()
 
     dbytes = decode_bytes(B, S, Hq, Hkv, w.max_pages, 144)
     abytes = append_bytes(B, Hkv, 144)
@@ -814,7 +833,13 @@ def run_ours(args):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic, "peak_kind": peak_kind,
                      "kernel": "decode_kernel<nvfp4>", "us_per_launch": dec_us, "median_us_per_launch": dec_median_us,
-                     "timed_launches": n_prof, "algorithmic_bytes_per_launch": dbytes},
+                     "min_us_per_launch": dec_samples[0], "max_us_per_launch": dec_samples[-1],
+                     "timed_launches": nr, "algorithmic_bytes_per_launch": dbytes,
+                     "timing": "%d fused steps after the timed region, the decode-kernel launch of each bracketed by "
+                               "CUDA events on its stream" % nr,
+                     "clocks": sampler.summary(t_roof0, t_roof1),
+                     "in_timed_region": {"us_per_launch": region_us, "timed_launches": n_prof,
+                                         "every": PROFILE_EVERY}},
         "clocks": sampler.summary(t_wall0, t_wall1),
     }
 
@@ -828,14 +853,21 @@ def run_ours(args):
         comp["fp8_e4m3_cache_same_workload"] = {
             "decode_us": fp8_us, "call_us": fp8_call, "nvfp4_decode_us": dec_us, "nvfp4_over_fp8_time": dec_us / fp8_us,
             "fp8_gb_per_s": decode_bytes(B, S, Hq, Hkv, w.max_pages, 256) / fp8_us / 1e3,
-            "kv_byte_ratio": 144 / 256}
+            "pct_of_nominal_8tbps": 100.0 * decode_bytes(B, S, Hq, Hkv, w.max_pages, 256) / fp8_us / 1e3 /
+            NOMINAL_HBM_GBS, "kv_byte_ratio": 144 / 256}
         w4 = workloads.decode_1m()
         us4, call4 = time_decode_only(m, w4, 0, device, 50, 5)
         b4 = decode_bytes(w4.batch, int(w4.seq_lens[0]), w4.num_q_heads, w4.num_kv_heads, w4.max_pages, 144)
+        fp8_us4, fp8_call4 = time_decode_only(m, w4, 1, device, 50, 5)
+        b4_fp8 = decode_bytes(w4.batch, int(w4.seq_lens[0]), w4.num_q_heads, w4.num_kv_heads, w4.max_pages, 256)
         comp["decode_1m"] = {"workload": w4.name, "decode_us": us4, "gb_per_s": b4 / us4 / 1e3,
                              "pct_of_measured_hbm": 100.0 * b4 / us4 / 1e3 / peak,
+                             "pct_of_nominal_8tbps": 100.0 * b4 / us4 / 1e3 / NOMINAL_HBM_GBS,
                              "call_us": call4, "call_gb_per_s": b4 / call4 / 1e3,
-                             "kv_tokens_per_s": 2 * 1048576 / (call4 * 1e-6)}
+                             "kv_tokens_per_s": 2 * 1048576 / (call4 * 1e-6),
+                             "fp8_e4m3_cache": {"decode_us": fp8_us4, "call_us": fp8_call4,
+                                                "fp8_gb_per_s": b4_fp8 / fp8_us4 / 1e3,
+                                                "nvfp4_over_fp8_time": us4 / fp8_us4, "kv_byte_ratio": 144 / 256}}
         comp["append_65k"] = time_append(m, device, 50, 5)
         comp["calibrate_65k"] = time_calibrate(m, device, 50, 5)
         comp["extend_agent_mix"] = time_extend(m, device, 10, 2, load_bf16_peak())

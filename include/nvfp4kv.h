@@ -263,8 +263,11 @@ NVFP4KV_API int nvfp4_paged_decode_attention_append(const nvfp4kv_cache *cache, 
  *     num_splits) <= NVFP4KV_NOALLOC_SCRATCH_BYTES; a larger request returns
  *     NVFP4KV_EUNSUPPORTED and launches nothing.
  *   - The first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress, with that device current); make that first call
- *     before any stream capture.
+ *     (cudaGetSymbolAddress, with that device current) and keeps it for the
+ *     life of the process; make that first call before any stream capture.
+ *     A cudaDeviceReset (or anything else that destroys the device's primary
+ *     context) invalidates the kept address: do not call this entry point on
+ *     a device after resetting it.
  *   - Every call shares the one array, which keeps the last call's contents:
  *     calls that overlap on the GPU (e.g. on unordered streams) race.  No part
  *     of the array needs to start at zero.

@@ -58,7 +58,7 @@ def _load():
         i32, i64, f32, f64 = ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_double
         sig = {
             "oracle_calibrate_global_scale": (f32, [P, i64]),
-            "oracle_extend_attention": (i32, [P, P, P, P, P, P, P, i32, i32, i32, f64, P, i32]),
+            "oracle_extend_attention": (i32, [P, P, P, P, P, P, P, i32, i32, i32, f64, P, P, i32]),
             "oracle_bf16_value": (f64, [ctypes.c_uint16]),
             "oracle_bf16_from_float": (ctypes.c_uint16, [f32]),
             "oracle_e4m3_value": (f64, [ctypes.c_uint8]),
@@ -71,8 +71,8 @@ def _load():
             "oracle_slab_bytes": (i64, [i32, i32]),
             "oracle_quantize_append": (i32, [P, i64, i32, i32, i32, f32, f32, P, P, i64, i64, P]),
             "oracle_decode_attention": (i32, [P, i64, i32, i32, i32, f32, f32, P, i32, i32, P, i32, P, f64,
-                                              P, i32]),
-            "oracle_sequence_attention": (i32, [P, i32, P, P, i64, i64, i32, f32, f32, f64, P]),
+                                              P, P, i32]),
+            "oracle_sequence_attention": (i32, [P, i32, P, P, i64, i64, i32, f32, f32, f64, P, P]),
             "oracle_prefix_dequant": (i32, [P, i64, i32, i32, i32, f32, f32, P, i32, P, P, i32, P, P]),
         }
         for name, (res, args) in sig.items():
@@ -178,35 +178,45 @@ def quantize_append(pool: OraclePool, k: np.ndarray, v: np.ndarray, slot_mapping
     _check(rc, "quantize_append")
 
 
+def _spread_arg(spread: bool, out: np.ndarray):
+    sp = np.zeros_like(out) if spread else None
+    return sp, (_ptr(sp) if spread else None)
+
+
 def decode_attention(pool: OraclePool, q: np.ndarray, block_table: np.ndarray, seq_lens: np.ndarray,
-                     sm_scale: float, nthreads: int = 0) -> np.ndarray:
-    """q: uint16 BF16 bits [B][Hq][128]; returns float64 [B][Hq][128]."""
+                     sm_scale: float, nthreads: int = 0, spread: bool = False):
+    """q: uint16 BF16 bits [B][Hq][128]; returns float64 [B][Hq][128], or with
+    spread=True (out, spread): spread[b][h][d] = sum_t w_t |v_t[d] - out[b][h][d]|
+    over the softmax weights w_t (the error scale the parity tests use)."""
     q = np.ascontiguousarray(q, dtype=np.uint16)
     B, Hq = int(q.shape[0]), int(q.shape[1])
     bt = np.ascontiguousarray(block_table, dtype=np.int32)
     sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
     out = np.zeros((B, Hq, HEAD_DIM), dtype=np.float64)
+    sp, sp_ptr = _spread_arg(spread, out)
     rc = _load().oracle_decode_attention(*pool._hdr(), _ptr(q), B, Hq, _ptr(bt), bt.shape[1], _ptr(sl),
-                                         float(sm_scale), _ptr(out), int(nthreads))
+                                         float(sm_scale), _ptr(out), sp_ptr, int(nthreads))
     _check(rc, "decode_attention")
-    return out
+    return (out, sp) if spread else out
 
 
 def sequence_attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, sm_scale: float, dtype: int = DTYPE_NVFP4,
-                       gk: float = 1.0, gv: float = 1.0) -> np.ndarray:
+                       gk: float = 1.0, gv: float = 1.0, spread: bool = False):
     """Attention of G query heads over one sequence given as BF16 K/V rows.
 
-    q: uint16 [G][128]; k, v: uint16 [n][128] (one KV head).  Returns float64 [G][128].
+    q: uint16 [G][128]; k, v: uint16 [n][128] (one KV head).  Returns float64
+    [G][128], or (out, spread) as decode_attention does.
     """
     q = np.ascontiguousarray(q, dtype=np.uint16)
     k = np.ascontiguousarray(k, dtype=np.uint16)
     v = np.ascontiguousarray(v, dtype=np.uint16)
     G, n = int(q.shape[0]), int(k.shape[0])
     out = np.zeros((G, HEAD_DIM), dtype=np.float64)
+    sp, sp_ptr = _spread_arg(spread, out)
     rc = _load().oracle_sequence_attention(_ptr(q), G, _ptr(k), _ptr(v), n, k.shape[1], int(dtype), float(gk),
-                                           float(gv), float(sm_scale), _ptr(out))
+                                           float(gv), float(sm_scale), _ptr(out), sp_ptr)
     _check(rc, "sequence_attention")
-    return out
+    return (out, sp) if spread else out
 
 
 def prefix_dequant(pool: OraclePool, block_table: np.ndarray, prefix_lens: np.ndarray,
@@ -235,11 +245,12 @@ def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
 
 def extend_attention(q: np.ndarray, k_prefix: np.ndarray, v_prefix: np.ndarray, cu_prefix: np.ndarray,
                      k_chunk: np.ndarray, v_chunk: np.ndarray, cu_q: np.ndarray, sm_scale: float,
-                     nthreads: int = 0) -> np.ndarray:
+                     nthreads: int = 0, spread: bool = False):
     """fp64 extend attention: chunk token i of request r attends to its prefix
     rows (BF16 bits [total_prefix][Hkv][128], rows cu_prefix[r]..cu_prefix[r+1])
     and to chunk tokens 0..i (BF16 bits [total_q][Hkv][128]); q: BF16 bits
-    [total_q][Hq][128].  Returns float64 [total_q][Hq][128]."""
+    [total_q][Hq][128].  Returns float64 [total_q][Hq][128], or (out, spread) as
+    decode_attention does."""
     q = np.ascontiguousarray(q, dtype=np.uint16)
     kp, vp = np.ascontiguousarray(k_prefix, dtype=np.uint16), np.ascontiguousarray(v_prefix, dtype=np.uint16)
     kn, vn = np.ascontiguousarray(k_chunk, dtype=np.uint16), np.ascontiguousarray(v_chunk, dtype=np.uint16)
@@ -251,7 +262,8 @@ def extend_attention(q: np.ndarray, k_prefix: np.ndarray, v_prefix: np.ndarray, 
     # a valid (never dereferenced) pointer for empty arrays
     kp = kp if kp.size else np.zeros(1, np.uint16)
     vp = vp if vp.size else np.zeros(1, np.uint16)
+    sp, sp_ptr = _spread_arg(spread, out)
     rc = _load().oracle_extend_attention(_ptr(q), _ptr(kp), _ptr(vp), _ptr(cp), _ptr(kn), _ptr(vn), _ptr(cq),
-                                         len(cq) - 1, hq, hkv, float(sm_scale), _ptr(out), int(nthreads))
+                                         len(cq) - 1, hq, hkv, float(sm_scale), _ptr(out), sp_ptr, int(nthreads))
     _check(rc, "extend_attention")
-    return out
+    return (out, sp) if spread else out

@@ -335,9 +335,15 @@ typedef int (*row_fn)(void *ctx, int which, int64_t t, double *out);
 /* out[h][:] = sum_t softmax_t(sm_scale * q_h . k_t) v_t over the n tokens of
  * one sequence, for the G query heads q[G][128] that share one KV head.
  * Two passes: the scores (max-shifted softmax needs all of them), then the
- * probability-weighted sum of V.  scores has room for G * n values. */
+ * probability-weighted sum of V.  scores has room for G * n values.
+ *
+ * spread (may be NULL): spread[h][d] = sum_t w_t |v_t[d] - out[h][d]| with
+ * w_t the softmax weights -- how far the values lie from the output on
+ * average.  Not part of the method: the parity tests bound a kernel's error
+ * by it (rounding each weight by a relative e moves the output by at most
+ * e * spread, to first order), and a third pass over V computes it. */
 static int attend_group(const double *q, int G, row_fn rows, void *ctx, int64_t n, double sm_scale, double *out,
-                        double *scores)
+                        double *scores, double *spread)
 {
     double krow[HEAD_DIM], vrow[HEAD_DIM], m[16], l[16];
     for (int h = 0; h < G; h++) {
@@ -345,6 +351,8 @@ static int attend_group(const double *q, int G, row_fn rows, void *ctx, int64_t 
         m[h] = -INFINITY;
         l[h] = 0.0;
     }
+    if (spread)
+        for (int i = 0; i < G * HEAD_DIM; i++) spread[i] = 0.0;
     if (n == 0) return ORACLE_OK;
     for (int64_t t = 0; t < n; t++) {
         if (rows(ctx, 0, t, krow)) return ORACLE_EPAGE;
@@ -366,6 +374,17 @@ static int attend_group(const double *q, int G, row_fn rows, void *ctx, int64_t 
     }
     for (int h = 0; h < G; h++)
         for (int d = 0; d < HEAD_DIM; d++) out[h * HEAD_DIM + d] /= l[h];
+    if (spread) {
+        for (int i = 0; i < G * HEAD_DIM; i++) spread[i] = 0.0;
+        for (int64_t t = 0; t < n; t++) {
+            if (rows(ctx, 1, t, vrow)) return ORACLE_EPAGE;
+            for (int h = 0; h < G; h++) {
+                double wt = exp(scores[h * n + t] - m[h]) / l[h];
+                for (int d = 0; d < HEAD_DIM; d++)
+                    spread[h * HEAD_DIM + d] += wt * fabs(vrow[d] - out[h * HEAD_DIM + d]);
+            }
+        }
+    }
     return ORACLE_OK;
 }
 
@@ -393,7 +412,7 @@ typedef struct {
     int max_pages;
     const int32_t *seq_lens;
     double sm_scale;
-    double *out;
+    double *out, *spread;
     int64_t next_unit; /* shared work counter */
     pthread_mutex_t lock;
     int status;
@@ -437,8 +456,9 @@ static void *decode_worker(void *arg)
                     oracle_bf16_value(j->q[((int64_t)b * j->num_q_heads + kv * G + h) * HEAD_DIM + d]);
         double *scores = malloc(sizeof(double) * (size_t)G * (size_t)(n > 0 ? n : 1));
         paged_rows_t ctx = {p, j->block_table + (int64_t)b * j->max_pages, kv};
-        int rc = attend_group(qd, G, paged_row, &ctx, n, j->sm_scale,
-                              j->out + ((int64_t)b * j->num_q_heads + (int64_t)kv * G) * HEAD_DIM, scores);
+        const int64_t o = ((int64_t)b * j->num_q_heads + (int64_t)kv * G) * HEAD_DIM;
+        int rc = attend_group(qd, G, paged_row, &ctx, n, j->sm_scale, j->out + o, scores,
+                              j->spread ? j->spread + o : NULL);
         free(scores);
         if (rc) set_status(j, rc);
     }
@@ -452,19 +472,19 @@ static int resolve_threads(int nthreads)
     return n > 0 ? (int)n : 1;
 }
 
-/* q: BF16 [batch][num_q_heads][128]; out: double [batch][num_q_heads][128].
- * nthreads <= 0 uses every online core; the units are independent, so the
- * thread count does not change any result. */
+/* q: BF16 [batch][num_q_heads][128]; out and spread (may be NULL): double
+ * [batch][num_q_heads][128].  nthreads <= 0 uses every online core; the units
+ * are independent, so the thread count does not change any result. */
 int oracle_decode_attention(const uint8_t *pool, int64_t num_pages, int page_size, int num_kv_heads, int dtype,
                             float gk, float gv, const uint16_t *q, int batch, int num_q_heads,
                             const int32_t *block_table, int max_pages, const int32_t *seq_lens, double sm_scale,
-                            double *out, int nthreads)
+                            double *out, double *spread, int nthreads)
 {
     if (num_kv_heads <= 0 || num_q_heads % num_kv_heads || num_q_heads / num_kv_heads > 16 ||
         oracle_slab_bytes(dtype, page_size) < 0)
         return ORACLE_EINVAL;
     pool_t p = {(uint8_t *)pool, num_pages, page_size, num_kv_heads, dtype, gk, gv};
-    decode_job_t j = {&p, q, batch, num_q_heads, block_table, max_pages, seq_lens, sm_scale, out, 0,
+    decode_job_t j = {&p, q, batch, num_q_heads, block_table, max_pages, seq_lens, sm_scale, out, spread, 0,
                       PTHREAD_MUTEX_INITIALIZER, 0};
     int nt = resolve_threads(nthreads);
     pthread_t *th = malloc(sizeof(pthread_t) * (size_t)nt);
@@ -500,7 +520,8 @@ static int bf16_row(void *ctx, int which, int64_t t, double *out)
  * start; q: BF16 [G][128]; out: double [G][128].  Used for sampled checks of
  * very long sequences and for CPU timing. */
 int oracle_sequence_attention(const uint16_t *q, int G, const uint16_t *k, const uint16_t *v, int64_t n,
-                              int64_t row_stride, int dtype, float gk, float gv, double sm_scale, double *out)
+                              int64_t row_stride, int dtype, float gk, float gv, double sm_scale, double *out,
+                              double *spread)
 {
     uint8_t slab[4096]; /* one 16-token group; rows are quantised into row 0 */
     if (G < 1 || G > 16 || oracle_slab_bytes(dtype, 16) < 0) return ORACLE_EINVAL;
@@ -508,7 +529,7 @@ int oracle_sequence_attention(const uint16_t *q, int G, const uint16_t *k, const
     double qd[16 * HEAD_DIM];
     for (int i = 0; i < G * HEAD_DIM; i++) qd[i] = oracle_bf16_value(q[i]);
     double *scores = malloc(sizeof(double) * (size_t)G * (size_t)(n > 0 ? n : 1));
-    int rc = attend_group(qd, G, bf16_row, &ctx, n, sm_scale, out, scores);
+    int rc = attend_group(qd, G, bf16_row, &ctx, n, sm_scale, out, scores, spread);
     free(scores);
     return ctx.status ? ctx.status : rc;
 }
@@ -579,7 +600,7 @@ typedef struct {
     const int32_t *cu_prefix, *cu_q;
     int num_reqs, num_q_heads, num_kv_heads;
     double sm_scale;
-    double *out;
+    double *out, *spread;
     int64_t total_units, next_unit;
     pthread_mutex_t lock;
     int status;
@@ -608,8 +629,9 @@ static void *extend_worker(void *arg)
         extend_rows_t ctx = {j->k_pre, j->v_pre, j->k_new, j->v_new, j->cu_prefix[r], j->cu_q[r], n_prefix, Hkv, kv};
         int64_t n = n_prefix + i + 1;
         double *scores = malloc(sizeof(double) * (size_t)G * (size_t)n);
-        int rc = attend_group(qd, G, extend_row, &ctx, n, j->sm_scale,
-                              j->out + (row * j->num_q_heads + (int64_t)kv * G) * HEAD_DIM, scores);
+        const int64_t o = (row * j->num_q_heads + (int64_t)kv * G) * HEAD_DIM;
+        int rc = attend_group(qd, G, extend_row, &ctx, n, j->sm_scale, j->out + o, scores,
+                              j->spread ? j->spread + o : NULL);
         free(scores);
         if (rc) {
             pthread_mutex_lock(&j->lock);
@@ -627,7 +649,8 @@ static void *extend_worker(void *arg)
  * [total_q][num_q_heads][128]. */
 int oracle_extend_attention(const uint16_t *q, const uint16_t *k_pre, const uint16_t *v_pre, const int32_t *cu_prefix,
                             const uint16_t *k_new, const uint16_t *v_new, const int32_t *cu_q, int num_reqs,
-                            int num_q_heads, int num_kv_heads, double sm_scale, double *out, int nthreads)
+                            int num_q_heads, int num_kv_heads, double sm_scale, double *out, double *spread,
+                            int nthreads)
 {
     if (num_reqs < 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads || num_q_heads / num_kv_heads > 16)
         return ORACLE_EINVAL;
@@ -636,7 +659,7 @@ int oracle_extend_attention(const uint16_t *q, const uint16_t *k_pre, const uint
     int64_t total_q = num_reqs ? cu_q[num_reqs] - cu_q[0] : 0;
     if (num_reqs && cu_q[0] != 0) return ORACLE_EINVAL;
     extend_job_t j = {q, k_pre, v_pre, k_new, v_new, cu_prefix, cu_q, num_reqs, num_q_heads, num_kv_heads, sm_scale,
-                      out, total_q * num_kv_heads, 0, PTHREAD_MUTEX_INITIALIZER, 0};
+                      out, spread, total_q * num_kv_heads, 0, PTHREAD_MUTEX_INITIALIZER, 0};
     int nt = resolve_threads(nthreads);
     pthread_t *th = malloc(sizeof(pthread_t) * (size_t)nt);
     for (int i = 0; i < nt; i++) pthread_create(&th[i], NULL, extend_worker, &j);

@@ -73,8 +73,12 @@ M = {
                         "while (r + 1 < j->num_reqs && j->cu_q[r + 1] < row) r++;")],
     "ties_low": [("if (a < mid) return lo;", "if (a <= mid) return lo;")],
     "calib_zero_gives_zero": [("if (amax == 0.0) return 1.0f;", "if (amax == 0.0) return 0.0f;")],
-    "decode_out_offset": [("j->out + ((int64_t)b * j->num_q_heads + (int64_t)kv * G) * HEAD_DIM, scores);",
-                           "j->out + ((int64_t)b * j->num_q_heads + (int64_t)kv) * HEAD_DIM, scores);")],
+    "decode_out_offset": [("const int64_t o = ((int64_t)b * j->num_q_heads + (int64_t)kv * G) * HEAD_DIM;",
+                           "const int64_t o = ((int64_t)b * j->num_q_heads + (int64_t)kv) * HEAD_DIM;")],
+    "spread_signed": [("spread[h * HEAD_DIM + d] += wt * fabs(vrow[d] - out[h * HEAD_DIM + d]);",
+                       "spread[h * HEAD_DIM + d] += wt * (vrow[d] - out[h * HEAD_DIM + d]);")],
+    "spread_unnormalised": [("double wt = exp(scores[h * n + t] - m[h]) / l[h];",
+                             "double wt = exp(scores[h * n + t] - m[h]);")],
 }
 
 

@@ -90,5 +90,6 @@ def test_calibrated_cache_and_decode_match_oracle(m):
     out = m.paged_decode_attention(cache, q, w.block_table.cuda(), w.seq_lens.cuda(), w.sm_scale)
     torch.cuda.synchronize()
     assert m.check_device_errors() == 0
-    ref = oracle.decode_attention(pool, bits(q), w.block_table.numpy(), w.seq_lens.numpy(), w.sm_scale)
-    check_attention(out / 5e3, ref / 5e3, "calibrated decode (in units of the V scale-up)")
+    ref, spread = oracle.decode_attention(pool, bits(q), w.block_table.numpy(), w.seq_lens.numpy(), w.sm_scale,
+                                          spread=True)
+    check_attention(out / 5e3, ref / 5e3, "calibrated decode (in units of the V scale-up)", spread=spread / 5e3)

@@ -25,8 +25,8 @@ def test_tiny_decode_workload(m):
     cache, pool = fill_both(w, m)
     assert np.array_equal(cache.pool.cpu().numpy(), pool.data)
     for splits in (0, 1, 2, 9):
-        out, ref = decode_both(w, m, cache, pool, num_splits=splits)
-        check_attention(out, ref, "tiny splits=%d" % splits)
+        out, ref, spread = decode_both(w, m, cache, pool, num_splits=splits)
+        check_attention(out, ref, "tiny splits=%d" % splits, spread=spread)
 
 
 @pytest.mark.parametrize("P", [16, 32, 64, 128])
@@ -35,8 +35,8 @@ def test_decode_page_sizes_and_groups(m, P, Hq, Hkv):
     lens = [1, 63, 64, 65, 300, 1000, 0, 129]
     w = workloads.make_decode("t", 31 + P + Hq, lens, Hq, Hkv, P, recipe=workloads.ValueRecipe(outlier_p=0.01))
     cache, pool = fill_both(w, m)
-    out, ref = decode_both(w, m, cache, pool)
-    check_attention(out, ref, "P=%d Hq=%d Hkv=%d" % (P, Hq, Hkv))
+    out, ref, spread = decode_both(w, m, cache, pool)
+    check_attention(out, ref, "P=%d Hq=%d Hkv=%d" % (P, Hq, Hkv), spread=spread)
     assert not out[6].float().abs().sum().item()   # empty sequence -> zeros
 
 
@@ -48,31 +48,33 @@ def test_decode_page_sizes_and_groups(m, P, Hq, Hkv):
 def test_split_count_does_not_change_the_result_beyond_tolerance(m, splits):
     w = workloads.make_decode("s", 5, [4000, 2500, 31, 1], 16, 2, 64)
     cache, pool = fill_both(w, m)
-    out, ref = decode_both(w, m, cache, pool, num_splits=splits)
-    check_attention(out, ref, "splits=%d" % splits)
+    out, ref, spread = decode_both(w, m, cache, pool, num_splits=splits)
+    check_attention(out, ref, "splits=%d" % splits, spread=spread)
 
 
 def test_channel_outliers_long_sequence(m):
     w = workloads.make_decode("c", 6, [20000, 7], 40, 8, 64, recipe=workloads.ValueRecipe(channel_lognormal=True))
     cache, pool = fill_both(w, m)
-    out, ref = decode_both(w, m, cache, pool)
-    check_attention(out, ref, "channel outliers")
+    out, ref, spread = decode_both(w, m, cache, pool)
+    check_attention(out, ref, "channel outliers", spread=spread)
 
 
 def test_shared_prefix_pages(m):
     w = workloads.make_decode("p", 8, [3300, 5000, 3201, 4000], 32, 8, 64, shared_prefix_tokens=3200)
     cache, pool = fill_both(w, m)
-    out, ref = decode_both(w, m, cache, pool)
-    check_attention(out, ref, "shared prefix")
+    out, ref, spread = decode_both(w, m, cache, pool)
+    check_attention(out, ref, "shared prefix", spread=spread)
 
 
-@pytest.mark.parametrize("P", [16, 64, 128])
-def test_fp8_cache_decode(m, P):
-    w = workloads.make_decode("f", 9 + P, [1, 100, 2000, 64], 32, 4, P)
+@pytest.mark.parametrize("P,Hq,Hkv", [(16, 32, 4), (64, 32, 4), (128, 32, 4), (64, 32, 2), (16, 16, 1), (64, 40, 8)])
+def test_fp8_cache_decode(m, P, Hq, Hkv):
+    """G = 8 and 5 take one 8-wide N tile of the FP8 kernel, G = 16 two."""
+    w = workloads.make_decode("f", 9 + P + Hq, [1, 100, 2000, 64], Hq, Hkv, P,
+                              recipe=workloads.ValueRecipe(outlier_p=0.01))
     cache, pool = fill_both(w, m, dtype=1)
     assert np.array_equal(cache.pool.cpu().numpy(), pool.data)
-    out, ref = decode_both(w, m, cache, pool)
-    check_attention(out, ref, "fp8 P=%d" % P)
+    out, ref, spread = decode_both(w, m, cache, pool)
+    check_attention(out, ref, "fp8 P=%d G=%d" % (P, Hq // Hkv), spread=spread)
 
 
 def test_tensor_scales_and_custom_sm_scale(m):
@@ -80,8 +82,8 @@ def test_tensor_scales_and_custom_sm_scale(m):
     cache, pool = fill_both(w, m, gk=0.75, gv=3.0)
     q = w.q("cuda")
     out = m.paged_decode_attention(cache, q, w.block_table.cuda(), w.seq_lens.cuda(), sm_scale=0.3)
-    ref = oracle.decode_attention(pool, bits(q), w.block_table.numpy(), w.seq_lens.numpy(), 0.3)
-    check_attention(out, ref, "tensor scales")
+    ref, spread = oracle.decode_attention(pool, bits(q), w.block_table.numpy(), w.seq_lens.numpy(), 0.3, spread=True)
+    check_attention(out, ref, "tensor scales", spread=spread)
 
 
 def test_large_query_values(m):
@@ -91,8 +93,8 @@ def test_large_query_values(m):
     q = (w.q("cuda").float() * 3.0e5).to(torch.bfloat16)
     q[0, 3] = (q[0, 3].float() * 1e-30).to(torch.bfloat16)
     out = m.paged_decode_attention(cache, q, w.block_table.cuda(), w.seq_lens.cuda(), sm_scale=1e-6)
-    ref = oracle.decode_attention(pool, bits(q), w.block_table.numpy(), w.seq_lens.numpy(), 1e-6)
-    check_attention(out, ref, "large q")
+    ref, spread = oracle.decode_attention(pool, bits(q), w.block_table.numpy(), w.seq_lens.numpy(), 1e-6, spread=True)
+    check_attention(out, ref, "large q", spread=spread)
 
 
 def test_bad_block_table_entry_is_reported_not_read(m):

@@ -13,7 +13,7 @@ import torch
 
 import oracle
 import workloads
-from gpu_common import bits, check_attention, fill_both
+from gpu_common import EPS_BF16_P, bits, check_attention, fill_both
 
 pytestmark = pytest.mark.gpu
 SM = 1.0 / math.sqrt(128)
@@ -41,7 +41,8 @@ def _case(m, prefix_lens, chunk_lens, Hq, Hkv, seed, max_q_len=None):
     out = m.extend_attention(q, kp, vp, cu_p.cuda(), kn, vn, cu_q.cuda(), max_q_len or max(chunk_lens), SM)
     torch.cuda.synchronize()
     assert m.check_device_errors() == 0
-    ref = oracle.extend_attention(bits(q), bits(kp), bits(vp), cu_p.numpy(), bits(kn), bits(vn), cu_q.numpy(), SM)
+    ref = oracle.extend_attention(bits(q), bits(kp), bits(vp), cu_p.numpy(), bits(kn), bits(vn), cu_q.numpy(), SM,
+                                  spread=True)
     return out, ref
 
 
@@ -56,8 +57,9 @@ def _case(m, prefix_lens, chunk_lens, Hq, Hkv, seed, max_q_len=None):
     ([128, 383], [96, 33], 16, 2),
 ])
 def test_extend_matches_oracle(m, prefix_lens, chunk_lens, Hq, Hkv):
-    out, ref = _case(m, prefix_lens, chunk_lens, Hq, Hkv, sum(prefix_lens) + sum(chunk_lens) + Hq)
-    check_attention(out, ref, "extend %s %s G=%d" % (prefix_lens, chunk_lens, Hq // Hkv))
+    out, (ref, spread) = _case(m, prefix_lens, chunk_lens, Hq, Hkv, sum(prefix_lens) + sum(chunk_lens) + Hq)
+    check_attention(out, ref, "extend %s %s G=%d" % (prefix_lens, chunk_lens, Hq // Hkv), eps=EPS_BF16_P,
+                    spread=spread)
 
 
 def test_chunk_longer_than_bound_is_flagged(m):
@@ -89,8 +91,9 @@ def test_path2_prefix_dequant_then_extend(m):
     assert m.check_device_errors() == 0
     rk, rv = oracle.prefix_dequant(pool, w.block_table.numpy(), lens.numpy(), cu_p.numpy())
     assert np.array_equal(bits(kw), rk) and np.array_equal(bits(vw), rv)
-    ref = oracle.extend_attention(bits(q), rk, rv, cu_p.numpy(), bits(kn), bits(vn), cu_q.numpy(), SM)
-    check_attention(out, ref, "path 2")
+    ref, spread = oracle.extend_attention(bits(q), rk, rv, cu_p.numpy(), bits(kn), bits(vn), cu_q.numpy(), SM,
+                                          spread=True)
+    check_attention(out, ref, "path 2", eps=EPS_BF16_P, spread=spread)
 
 
 def _paged_case(m, lens, chunk, Hq, Hkv, P, seed, gk=1.0, gv=1.0):
@@ -131,8 +134,9 @@ def test_paged_extend_with_tensor_scales_matches_oracle(m):
                                                                   gk=0.37, gv=2.5)
     assert torch.equal(paged, two)
     rk, rv = oracle.prefix_dequant(pool, w.block_table.numpy(), pl.numpy(), cu_p.numpy())
-    ref = oracle.extend_attention(bits(q), rk, rv, cu_p.numpy(), bits(kn), bits(vn), cu_q.numpy(), SM)
-    check_attention(paged, ref, "paged extend g != 1")
+    ref, spread = oracle.extend_attention(bits(q), rk, rv, cu_p.numpy(), bits(kn), bits(vn), cu_q.numpy(), SM,
+                                          spread=True)
+    check_attention(paged, ref, "paged extend g != 1", eps=EPS_BF16_P, spread=spread)
 
 
 def test_paged_extend_bad_page_is_flagged(m):

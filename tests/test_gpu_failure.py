@@ -40,8 +40,8 @@ def test_context_usable_after_a_timeout(m):
     assert int(r.item()) == 1 and m.check_device_errors() == -4
     w = workloads.tiny_decode()
     cache, pool = fill_both(w, m)
-    out, ref = decode_both(w, m, cache, pool)
-    check_attention(out, ref, "decode after a timeout")
+    out, ref, spread = decode_both(w, m, cache, pool)
+    check_attention(out, ref, "decode after a timeout", spread=spread)
 
 
 def test_selftest_rejects_bad_arguments(m):

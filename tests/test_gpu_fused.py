@@ -99,8 +99,9 @@ def test_fused_matches_oracle(m):
         k, v = w.seq_kv(b, "cuda")
         oracle.quantize_append(pool, bits(k), bits(v), w.slots(b).numpy())
     assert np.array_equal(c_fused.pool.cpu().numpy(), pool.data)
-    ref = oracle.decode_attention(pool, bits(q), w.block_table.numpy(), w.seq_lens.numpy(), w.sm_scale)
-    check_attention(out, ref, "fused decode")
+    ref, spread = oracle.decode_attention(pool, bits(q), w.block_table.numpy(), w.seq_lens.numpy(), w.sm_scale,
+                                          spread=True)
+    check_attention(out, ref, "fused decode", spread=spread)
 
 
 def test_bad_page_for_the_new_token_is_flagged(m):

@@ -206,3 +206,51 @@ def test_attention_agrees_with_extended_precision_over_wide_score_ranges(q_gain)
             p = np.exp(s - s.max())
             ref = (p[:, None] * v[:, kv, :]).sum(axis=0) / p.sum()
             np.testing.assert_allclose(out[b, h], ref.astype(np.float64), rtol=1e-11, atol=1e-11 * float(np.abs(ref).max()))
+
+
+def test_spread_closed_forms_and_sdpa_weights():
+    """spread[h][d] = sum_t w_t |v_t[d] - out[h][d]|: zero for one token; half the
+    gap for two tokens under equal weights; and, on grid values, the same sum
+    formed from torch's float64 softmax weights (a library routine)."""
+    rng = np.random.default_rng(21)
+    pool, bt, ks, vs = build_cache(rng, [1, 2, 37], 1, 16)
+    q = to_bf16_bits(rng.standard_normal((3, 2, 128)))
+    lens = np.array([1, 2, 37], dtype=np.int32)
+    out, spread = oracle.decode_attention(pool, q, bt, lens, SM, spread=True)
+    assert np.array_equal(out, oracle.decode_attention(pool, q, bt, lens, SM))   # the output is unchanged
+    assert not spread[0].any()
+    qf = torch.from_numpy(bf16_bits_to_f64(q))
+    for b, n in ((1, 2), (2, 37)):
+        k = torch.from_numpy(ks[b][:, 0])
+        v = torch.from_numpy(vs[b][:, 0])
+        wts = torch.softmax(qf[b] @ k.T * SM, dim=-1)                       # [2][n]
+        want = (wts[:, :, None] * (v[None] - torch.from_numpy(out[b])[:, None]).abs()).sum(1)
+        np.testing.assert_allclose(spread[b], want.numpy(), rtol=1e-12, atol=1e-14)
+    # identical keys: equal weights, spread = |v0 - v1| / 2
+    pool2 = oracle.OraclePool(1, 16, 1)
+    k = grid_rows(rng, 1).reshape(1, 128).repeat(2, 0)
+    v = grid_rows(rng, 2).reshape(2, 128)
+    oracle.quantize_append(pool2, to_bf16_bits(k), to_bf16_bits(v), np.arange(2, dtype=np.int64))
+    _, s2 = oracle.decode_attention(pool2, q[:1, :1], np.zeros((1, 1), np.int32), np.array([2], np.int32), SM,
+                                    spread=True)
+    assert np.array_equal(s2[0, 0], np.abs(v[0] - v[1]) / 2)
+
+
+def test_spread_of_sequence_and_extend_attention_match_decode():
+    """The same spread from the oracle's three attention entry points on one sequence."""
+    rng = np.random.default_rng(22)
+    n = 45
+    k = grid_rows(rng, n).reshape(n, 128)
+    v = grid_rows(rng, n).reshape(n, 128)
+    q = to_bf16_bits(rng.standard_normal((1, 4, 128)))
+    pool = oracle.OraclePool(3, 16, 1)
+    oracle.quantize_append(pool, to_bf16_bits(k), to_bf16_bits(v), np.arange(n, dtype=np.int64))
+    o1, s1 = oracle.decode_attention(pool, q, np.arange(3, dtype=np.int32)[None], np.array([n], np.int32), SM,
+                                     spread=True)
+    o2, s2 = oracle.sequence_attention(q[0], to_bf16_bits(k), to_bf16_bits(v), SM, spread=True)
+    kb, vb = to_bf16_bits(k).reshape(n, 1, 128), to_bf16_bits(v).reshape(n, 1, 128)
+    o3, s3 = oracle.extend_attention(q, kb[:n - 1], vb[:n - 1], np.array([0, n - 1], np.int32), kb[n - 1:],
+                                     vb[n - 1:], np.array([0, 1], np.int32), SM, spread=True)
+    assert np.array_equal(o1[0], o2) and np.array_equal(s1[0], s2)
+    np.testing.assert_allclose(o3[0], o2, rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(s3[0], s2, rtol=1e-12, atol=1e-13)
