@@ -92,8 +92,8 @@ typedef struct {
     int32_t num_kv_heads;   /* >= 1 */
     int32_t head_dim;       /* must be 128 */
     int32_t dtype;          /* nvfp4kv_dtype */
-    float k_global_scale;   /* FP32 tensor scale of K, > 0 and finite (1.0 on the page) */
-    float v_global_scale;   /* FP32 tensor scale of V, > 0 and finite */
+    float k_global_scale;   /* FP32 tensor scale of K, a positive normal FP32 number (>= 2^-126; 1.0 on the page) */
+    float v_global_scale;   /* FP32 tensor scale of V, a positive normal FP32 number */
 } nvfp4kv_cache;
 
 /* Bytes of one (page, kv_head) slab: 144*P (NVFP4) or 256*P (FP8); 0 if the
@@ -119,8 +119,10 @@ NVFP4KV_API size_t nvfp4kv_pool_bytes(const nvfp4kv_cache *cache);
  *   scale  = E4M3(amax_i |x_i| / (6 g)),  round to nearest even, saturating;
  *   code_i = E2M1(x_i / (scale g)),       round to nearest even, saturating;
  *            a block whose scale is 0 stores signed zeros.
- * The quotients are formed in FP32 (for g = 1 this equals exact rounding).
- * FP8 pools store E4M3(x_i / g) per value.  Two tokens writing the same slot
+ * Each scale and code is the rounding of the exact quotient, for every tensor
+ * scale g (the kernel decides the cases an FP32 quotient would get wrong with
+ * exact fused multiply-add comparisons against the rounding midpoints).
+ * FP8 pools store E4M3(x_i / g) per value, rounded the same way.  Two tokens writing the same slot
  * in one call is a caller error (the result is one of the two rows).
  * num_tokens == 0 is a no-op.
  */
@@ -290,8 +292,9 @@ NVFP4KV_API int nvfp4_paged_decode_attention_noalloc(const nvfp4kv_cache *cache,
  *   total_prefix_tokens  host copy of cu[num_reqs] (sizes the launch)
  *   k_ws, v_ws      device BF16 [total_prefix_tokens][num_kv_heads][128],
  *                   16-byte aligned; row cu[r] + t receives prefix token t of
- *                   request r:  value = e2m1 * e4m3 * g, rounded to BF16
- *                   (exact for g = 1).
+ *                   request r:  value = the exact product e2m1 * e4m3 * g
+ *                   rounded once to BF16, nearest-even (exact for g = 1);
+ *                   FP8 pools: e4m3 * g rounded the same way.
  */
 NVFP4KV_API int nvfp4_prefix_dequant(const nvfp4kv_cache *cache, const int32_t *block_table, int max_pages_per_seq,
                          const int32_t *prefix_lens, const int32_t *cu_prefix_lens, int num_reqs,

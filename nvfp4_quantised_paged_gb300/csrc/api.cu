@@ -48,7 +48,9 @@ unsigned *error_word(cudaError_t *status) {
 
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-bool finite_positive(float x) { return isfinite(x) && x > 0.0f; }
+// A tensor scale is a positive normal FP32 number (the exact-rounding argument of
+// the g != 1 quantiser needs g >= 2^-126).
+bool normal_positive(float x) { return isfinite(x) && x >= 0x1p-126f; }
 
 // Validates the cache descriptor; returns NVFP4KV_OK or a negative status.
 int check_cache(const nvfp4kv_cache *c) {
@@ -58,7 +60,7 @@ int check_cache(const nvfp4kv_cache *c) {
     if (c->page_size != 16 && c->page_size != 32 && c->page_size != 64 && c->page_size != 128)
         return NVFP4KV_EUNSUPPORTED;
     if (c->num_kv_heads < 1 || c->num_pages < 1) return NVFP4KV_EINVAL;
-    if (!finite_positive(c->k_global_scale) || !finite_positive(c->v_global_scale)) return NVFP4KV_EINVAL;
+    if (!normal_positive(c->k_global_scale) || !normal_positive(c->v_global_scale)) return NVFP4KV_EINVAL;
     if (!c->pool || !aligned(c->pool, 256)) return NVFP4KV_EINVAL;
     return NVFP4KV_OK;
 }

@@ -3,7 +3,8 @@
 // Shared by the quantise-append kernel and the decode kernel's fused append.
 // Source: "Accelerating Long-Context and Agentic Inference with NVFP4 KV
 // Cache", section A3 and Fig. 1 (E2M1 values, one E4M3 scale per 16 values,
-// FP32 tensor scale); the rounding argument is in quantize_append.cu.
+// FP32 tensor scale); the rounding argument for g = 1 is in quantize_append.cu,
+// the one for other tensor scales beside e4m3_code_exact below.
 #pragma once
 
 #include "common.cuh"
@@ -49,6 +50,91 @@ __device__ __forceinline__ float rcp_approx(float x) {
 // unit-scale path multiplies where the scale decision is defined by a division.
 constexpr float kOneSixth = 0.16666667163372039794921875f;
 
+// ---------------------------------------------------------------------------
+// Tensor scale g != 1: every scale and code is the rounding of the EXACT
+// quotient (amax / (6 g), x / (s g), x / g), nearest-even, saturating.  An FP32
+// estimate (a / g) / den lands within two units in its last place of the exact
+// quotient, so its rounding is right or one code off; each neighbouring midpoint mu is then
+// checked exactly: quotient >= mu  <=>  a <= mu' g, where mu' (= mu, 6 mu or
+// mu s, at most 7 significant bits) is exact in FP32 and fma(mu', g, -a) is the
+// exact difference rounded once, so its sign (and zero) is exact.  That holds
+// while mu' g >= 2^-117 (the difference is then a multiple of 2^-148, never
+// lost to underflow); below g = 2^-100 both sides are scaled by 2^64 first.
+// ---------------------------------------------------------------------------
+
+constexpr float kTinyTensorScale = 0x1p-100f;
+constexpr float kTinyRescale = 0x1p64f;
+
+// Magnitude of E2M1 code c (0..7): 0, 0.5, 1, 1.5, 2, 3, 4, 6.
+__device__ __forceinline__ float e2m1_magnitude(uint32_t c) {
+    const uint32_t e = c >> 1, m = c & 1u;
+    return e == 0 ? 0.5f * (float)m : __uint_as_float(((e + 126u) << 23) | (m << 22));
+}
+
+// Magnitude of E4M3 code c (0..126), exact.
+__device__ __forceinline__ float e4m3_magnitude(uint32_t c) {
+    return __half2float(__ushort_as_half((uint16_t)(e4m3x2_to_f16x2(c) & 0xffffu)));
+}
+
+// Move magnitude code c (0..cmax) to the exact rounding of a / (den g), where
+// the caller's estimate c is at most one code off.  mag(k) = value of code k;
+// the midpoint between k and k+1, times den, is exact in FP32.
+template <typename Mag>
+__device__ __forceinline__ uint32_t fix_code(uint32_t c, uint32_t cmax, float a, float den, float g, Mag mag) {
+    if (c < cmax) {
+        const float mu = 0.5f * (mag(c) + mag(c + 1)) * den;
+        const float d = __fmaf_rn(mu, g, -a);            // sign of mu g - a, exact
+        if (d < 0.0f || (d == 0.0f && ((c + 1) & 1u) == 0)) return c + 1;
+    }
+    if (c > 0) {
+        const float mu = 0.5f * (mag(c - 1) + mag(c)) * den;
+        const float d = __fmaf_rn(mu, g, -a);
+        if (d > 0.0f || (d == 0.0f && ((c - 1) & 1u) == 0)) return c - 1;
+    }
+    return c;
+}
+
+// The estimate divides by g first: den g may overflow FP32 (g near its
+// largest value), a / g cannot go wrong by more than a code (it overflows only
+// where every code saturates and underflows only where every code is 0).
+__device__ __forceinline__ uint32_t e4m3_code_exact(float a, float den, float g) {
+    const uint32_t c = f32x2_to_e4m3x2(0.0f, __fdiv_rn(__fdiv_rn(a, g), den)) & 0x7fu;
+    return fix_code(c, 126u, a, den, g, [](uint32_t k) { return e4m3_magnitude(k); });
+}
+
+__device__ __forceinline__ uint32_t e2m1_code_exact(float a, float den, float g) {
+    const uint32_t c = f32x2_to_e2m1x2(0.0f, __fdiv_rn(__fdiv_rn(a, g), den)) & 7u;
+    return fix_code(c, 7u, a, den, g, [](uint32_t k) { return e2m1_magnitude(k); });
+}
+
+// The e2m1 * e4m3 (or e4m3) value p, exact in FP32, times g, rounded once to
+// BF16 (nearest-even; subnormal steps of 2^-133; infinity on overflow).
+// hi = fl(p g) and lo = p g - hi exactly (an FMA, exact while p g >= 2^-118);
+// hi decides the rounding unless it sits exactly on a BF16 midpoint, where the
+// sign of lo does.  Below g = 2^-100 the product is formed at g 2^64.
+__device__ __forceinline__ uint32_t bf16_of_product(float p, float g) {
+    const uint32_t sign = (__float_as_uint(p) >> 16) & 0x8000u;
+    const float a = fabsf(p);
+    if (a == 0.0f) return sign;
+    const bool tiny = g < kTinyTensorScale;
+    const float gs = tiny ? g * kTinyRescale : g;
+    const float hi = a * gs;
+    const float lo = __fmaf_rn(a, gs, -hi);
+    if (!tiny || hi >= 0x1p-62f) {      // a BF16 normal (or infinity) after unscaling
+        uint32_t b = __float_as_uint(hi);
+        if ((b & 0xffffu) == 0x8000u && lo != 0.0f) b += (lo > 0.0f) ? 1u : 0xffffffffu;  // off the tie, toward p g
+        uint32_t r = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(b)));
+        if (tiny) r = __float_as_uint(__uint_as_float(r << 16) * (1.0f / kTinyRescale)) >> 16;  // exact: >= 2^-126
+        return r | sign;
+    }
+    // below 2^-126 after unscaling: BF16 steps of 2^-133, i.e. units of hi 2^69
+    const float t = hi * 0x1p69f;
+    float f = floorf(t);
+    const float r = t - f;
+    if (r > 0.5f || (r == 0.5f && (lo > 0.0f || (lo == 0.0f && fmodf(f, 2.0f) != 0.0f)))) f += 1.0f;
+    return (uint32_t)f | sign;
+}
+
 template <bool kUnitScale>
 __device__ __forceinline__ void quantize_block16(const uint4 &a, const uint4 &b, float g, uint2 &codes,
                                                  uint32_t &scale_byte) {
@@ -58,9 +144,12 @@ __device__ __forceinline__ void quantize_block16(const uint4 &a, const uint4 &b,
 #pragma unroll
     for (int i = 0; i < 8; i++) m = max_u16x2(m, w[i] & 0x7fff7fffu);
     const uint32_t amax_bits = (m >> 16) > (m & 0xffffu) ? (m >> 16) : (m & 0xffffu);
-    const float amax = __uint_as_float(amax_bits << 16);
-    const float q = kUnitScale ? __fmul_rn(amax, kOneSixth) : __fdiv_rn(amax, __fmul_rn(6.0f, g));
-    const uint32_t s = f32x2_to_e4m3x2(0.0f, q) & 0xffu;
+    float amax = __uint_as_float(amax_bits << 16);
+    const bool tiny = !kUnitScale && g < kTinyTensorScale;   // decide at (x, g) 2^64: same quotients
+    const float gs = tiny ? g * kTinyRescale : g;
+    if (tiny) amax *= kTinyRescale;
+    const uint32_t s = kUnitScale ? f32x2_to_e4m3x2(0.0f, __fmul_rn(amax, kOneSixth)) & 0xffu
+                                  : e4m3_code_exact(amax, 6.0f, gs);
     scale_byte = s;
     const float sd = __half2float(__ushort_as_half((uint16_t)(e4m3x2_to_f16x2(s) & 0xffffu)));
     uint32_t packed[2] = {0u, 0u};
@@ -80,12 +169,12 @@ __device__ __forceinline__ void quantize_block16(const uint4 &a, const uint4 &b,
             packed[i / 4] |= f32x2_to_e2m1x2(snap13(y.y), snap13(y.x)) << (8 * (i % 4));
         }
     } else {
-        const float d = __fmul_rn(sd, g);
+        const float xs = tiny ? kTinyRescale : 1.0f;
 #pragma unroll
         for (int i = 0; i < 8; i++) {
-            const float lo = __fdiv_rn(bf16_lo(w[i]), d);
-            const float hi = __fdiv_rn(bf16_hi(w[i]), d);
-            packed[i / 4] |= f32x2_to_e2m1x2(hi, lo) << (8 * (i % 4));
+            const uint32_t clo = e2m1_code_exact(fabsf(bf16_lo(w[i])) * xs, sd, gs) | ((w[i] >> 12) & 8u);
+            const uint32_t chi = e2m1_code_exact(fabsf(bf16_hi(w[i])) * xs, sd, gs) | ((w[i] >> 28) & 8u);
+            packed[i / 4] |= (clo | (chi << 4)) << (8 * (i % 4));
         }
     }
     codes = make_uint2(packed[0], packed[1]);
@@ -100,15 +189,17 @@ __device__ __forceinline__ uint32_t f32x2_to_bf16x2(float hi, float lo) {
     return r;
 }
 
-// f16x2 holding exact values -> bf16x2 of (value * g), one rounding to BF16
-// after the FP32 product (exact when g = 1).
+// f16x2 holding exact values -> bf16x2 of (value * g), each the exact product
+// rounded to BF16 once (a plain conversion when g = 1).
 __device__ __forceinline__ uint32_t f16x2_to_bf16x2_scaled(uint32_t x, float g) {
-    return f32x2_to_bf16x2(__fmul_rn(f16_hi(x), g), __fmul_rn(f16_lo(x), g));
+    if (g == 1.0f) return f32x2_to_bf16x2(f16_hi(x), f16_lo(x));
+    return bf16_of_product(f16_lo(x), g) | (bf16_of_product(f16_hi(x), g) << 16);
 }
 
 // One NVFP4 16-value block (8 code bytes, one E4M3 scale byte) -> 8 BF16 pairs
-// of e2m1 * e4m3 * g, rounded to BF16 once (exact for g = 1): the prefix
-// dequant kernel and the paged extend kernel both expand blocks this way.
+// of e2m1 * e4m3 * g, the exact product rounded to BF16 once (exact for g = 1:
+// at most 6 significant bits): the prefix dequant kernel and the paged extend
+// kernel both expand blocks this way.
 __device__ __forceinline__ void nvfp4_block_to_bf16(uint2 codes, uint32_t sbyte, float g, uint32_t (&o)[8]) {
     const uint32_t s2 = e4m3x2_to_f16x2(sbyte | (sbyte << 8));  // {s, s}
     uint32_t f[8];
@@ -139,14 +230,21 @@ __device__ __forceinline__ void store_block_values(uint8_t *slab_base, int dtype
         uint32_t out[4];
 #pragma unroll
         for (int i = 0; i < 4; i++) {
-            float e0 = bf16_lo(w[2 * i]), e1 = bf16_hi(w[2 * i]), e2 = bf16_lo(w[2 * i + 1]), e3 = bf16_hi(w[2 * i + 1]);
-            if (!kUnitScale) {
-                e0 = __fdiv_rn(e0, g);
-                e1 = __fdiv_rn(e1, g);
-                e2 = __fdiv_rn(e2, g);
-                e3 = __fdiv_rn(e3, g);
+            const float e0 = bf16_lo(w[2 * i]), e1 = bf16_hi(w[2 * i]), e2 = bf16_lo(w[2 * i + 1]),
+                        e3 = bf16_hi(w[2 * i + 1]);
+            if (kUnitScale) {
+                out[i] = f32x2_to_e4m3x2(e1, e0) | (f32x2_to_e4m3x2(e3, e2) << 16);
+            } else {
+                const bool tiny = g < kTinyTensorScale;
+                const float gs = tiny ? g * kTinyRescale : g, xs = tiny ? kTinyRescale : 1.0f;
+                const float e[4] = {e0, e1, e2, e3};
+                uint32_t o = 0;
+#pragma unroll
+                for (int j = 0; j < 4; j++)
+                    o |= (e4m3_code_exact(fabsf(e[j]) * xs, 1.0f, gs) | ((__float_as_uint(e[j]) >> 24) & 0x80u))
+                         << (8 * j);
+                out[i] = o;
             }
-            out[i] = f32x2_to_e4m3x2(e1, e0) | (f32x2_to_e4m3x2(e3, e2) << 16);
         }
         uint8_t *dst = slab_base + (r >> 4) * 4096 + (which ? 2048 : 0) + (r & 15) * 128 + blk * 16;
         *reinterpret_cast<uint4 *>(dst) = make_uint4(out[0], out[1], out[2], out[3]);

@@ -61,6 +61,7 @@ def _load():
             "oracle_extend_attention": (i32, [P, P, P, P, P, P, P, i32, i32, i32, f64, P, P, i32]),
             "oracle_bf16_value": (f64, [ctypes.c_uint16]),
             "oracle_bf16_from_float": (ctypes.c_uint16, [f32]),
+            "oracle_bf16_from_double": (ctypes.c_uint16, [f64]),
             "oracle_e4m3_value": (f64, [ctypes.c_uint8]),
             "oracle_e2m1_value": (f64, [ctypes.c_uint8]),
             "oracle_e4m3_encode": (ctypes.c_uint8, [f32]),
@@ -110,6 +111,11 @@ class OraclePool:
 
 def bf16_value(bits: int) -> float:
     return _load().oracle_bf16_value(int(bits))
+
+
+def bf16_from_double(x: float) -> int:
+    """BF16 bits of x rounded once, nearest-even (subnormals, overflow to infinity)."""
+    return int(_load().oracle_bf16_from_double(float(x)))
 
 
 def e4m3_value(code: int) -> float:

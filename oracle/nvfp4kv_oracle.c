@@ -26,11 +26,15 @@
  * Readings taken where the page is silent:
  *   E4M3 is the OCP FP8 "fn" variant (bias 7, no infinities, S.1111.111 NaN,
  *   max 448).  Both codecs round to nearest, ties to the even code, and
- *   saturate at their largest finite value.  The quotient that decides a code
- *   is formed in FP32, the precision of the GPU kernel (for a tensor scale of
- *   1.0 this equals exact rational rounding; the CPU tests prove it by brute
- *   force).  A block whose scale rounds to zero stores zero magnitudes and
- *   keeps each element's sign, like every other element that rounds to zero.
+ *   saturate at their largest finite value.  A scale or code is the rounding
+ *   of the exact quotient (amax / (6 g), x / (scale g), x / g): the oracle
+ *   decides it by comparing the dividend with exact products of the divisor
+ *   and the grid's values and midpoints, never by forming the quotient.  A
+ *   dequantised value stored in BF16 (the prefix workspace) is the exact
+ *   product e2m1 * e4m3 * g rounded to BF16 once.  The tensor scale g is a
+ *   positive normal FP32 number.  A block whose scale rounds to zero stores
+ *   zero magnitudes and keeps each element's sign, like every other element
+ *   that rounds to zero.
  *   Nibble order: element 2i in the low nibble of byte i.  Query head h reads
  *   KV head h / G (G = query heads per KV head).
  *
@@ -122,6 +126,47 @@ static int round_to_table(double a, const double *vals, int n)
     return (lo % 2 == 0) ? lo : hi;
 }
 
+/* The same rounding applied to the exact quotient a / den (a >= 0, den > 0),
+ * decided without forming it: a / den < v  <=>  a < v * den.  Every product
+ * compared here is exact in double: den is 6 g, scale * g or g (at most 27
+ * significant bits for a 24-bit g), a grid value or midpoint has at most 5,
+ * and the exponents stay far inside double's range for a normal FP32 g. */
+static int round_quotient_to_table(double a, double den, const double *vals, int n)
+{
+    if (a >= vals[n - 1] * den) return n - 1;
+    int hi = 1;
+    while (vals[hi] * den < a) hi++;
+    int lo = hi - 1;
+    if (vals[hi] * den == a) return hi;
+    double mid = 0.5 * (vals[lo] + vals[hi]);
+    if (a < mid * den) return lo;
+    if (a > mid * den) return hi;
+    return (lo % 2 == 0) ? lo : hi;
+}
+
+/* Round a finite double to BF16, nearest-even, once: 8 significant bits for
+ * magnitudes from 2^-126 up, steps of 2^-133 below (subnormals), infinity
+ * from 2^128 * (1 - 2^-9) up. */
+uint16_t oracle_bf16_from_double(double x)
+{
+    uint16_t sign = signbit(x) ? 0x8000u : 0u;
+    double a = fabs(x);
+    if (a == 0.0) return sign;
+    int e;
+    frexp(a, &e);                       /* a = m 2^e, m in [0.5, 1) */
+    int step_exp = (e - 1 >= -126) ? e - 8 : -133;
+    double q = ldexp(a, -step_exp);     /* a in units of the BF16 step: exact */
+    double f = floor(q), r = q - f;
+    if (r > 0.5 || (r == 0.5 && fmod(f, 2.0) != 0.0)) f += 1.0;
+    double v = ldexp(f, step_exp);      /* the rounded magnitude */
+    if (v >= ldexp(1.0, 128)) return sign | 0x7f80u;
+    if (v < ldexp(1.0, -126)) return sign | (uint16_t)f;      /* subnormal (or 0x0080 at the boundary) */
+    int ve;
+    double vm = frexp(v, &ve);          /* v = vm 2^ve, vm in [0.5, 1) */
+    uint16_t mant = (uint16_t)(ldexp(vm, 8) - 128.0);
+    return sign | (uint16_t)((ve - 1 + 127) << 7) | mant;
+}
+
 static double e4m3_mags[127]; /* codes 0x00..0x7E */
 static double e2m1_mags[8];
 static pthread_once_t tables_once = PTHREAD_ONCE_INIT;
@@ -161,27 +206,30 @@ void oracle_e4m3_encode_many(const float *x, int64_t n, uint8_t *out)
 /* NVFP4 block quantisation                                             */
 /* ------------------------------------------------------------------ */
 
+static int valid_tensor_scale(float g) { return isfinite(g) && g >= 0x1p-126f; }
+
 /* Quantise 16 BF16 values with tensor scale g:
  *   amax  = max |x_i|
  *   scale = E4M3(amax / (6 g))           (6 = largest E2M1 magnitude)
- *   code_i = E2M1(x_i / (scale g)),  or a signed zero when scale is 0.
- * Codes are returned one per byte (sign in bit 3). */
+ *   code_i = E2M1(x_i / (scale g)),  or a signed zero when scale is 0,
+ * each the rounding of the exact quotient.  Codes are returned one per byte
+ * (sign in bit 3). */
 int oracle_quantize_block16(const uint16_t *x_bf16, float g, uint8_t *codes16, uint8_t *scale_code)
 {
-    float x[BLOCK];
-    float amax = 0.0f;
+    pthread_once(&tables_once, build_tables);
+    if (!valid_tensor_scale(g)) return ORACLE_EINVAL;
+    double x[BLOCK];
+    double amax = 0.0;
     for (int i = 0; i < BLOCK; i++) {
-        x[i] = (float)oracle_bf16_value(x_bf16[i]);
+        x[i] = oracle_bf16_value(x_bf16[i]);
         if (!isfinite(x[i])) return ORACLE_ENONFINITE;
-        if (fabsf(x[i]) > amax) amax = fabsf(x[i]);
+        if (fabs(x[i]) > amax) amax = fabs(x[i]);
     }
-    uint8_t s = oracle_e4m3_encode(amax / (6.0f * g));
-    float sd = (float)oracle_e4m3_value(s);
+    uint8_t s = (uint8_t)round_quotient_to_table(amax, 6.0 * (double)g, e4m3_mags, 127);
+    double sd = oracle_e4m3_value(s);
     for (int i = 0; i < BLOCK; i++) {
-        if (sd == 0.0f)
-            codes16[i] = signbit(x[i]) ? 8 : 0;
-        else
-            codes16[i] = oracle_e2m1_encode(x[i] / (sd * g));
+        int c = (sd == 0.0) ? 0 : round_quotient_to_table(fabs(x[i]), sd * (double)g, e2m1_mags, 8);
+        codes16[i] = (uint8_t)(signbit(x[i]) ? (8 | c) : c);
     }
     *scale_code = s;
     return ORACLE_OK;
@@ -278,6 +326,7 @@ static void dequant_row(const pool_t *p, int64_t page, int kv, int which, int ro
 /* Quantise one head_dim row of BF16 values and store it at (page, kv, row). */
 static int store_row(const pool_t *p, int64_t page, int kv, int which, int row, const uint16_t *x)
 {
+    pthread_once(&tables_once, build_tables);
     uint8_t *slab = slab_ptr(p, page, kv);
     uint8_t *c = codes_row(p, slab, which, row);
     float g = which ? p->gv : p->gk;
@@ -290,10 +339,12 @@ static int store_row(const pool_t *p, int64_t page, int kv, int which, int row, 
                 c[b * 8 + i] = (uint8_t)(codes[2 * i] | (codes[2 * i + 1] << 4));
         }
     } else {
+        if (!valid_tensor_scale(g)) return ORACLE_EINVAL;
         for (int d = 0; d < HEAD_DIM; d++) {
-            float v = (float)oracle_bf16_value(x[d]);
+            double v = oracle_bf16_value(x[d]);
             if (!isfinite(v)) return ORACLE_ENONFINITE;
-            c[d] = oracle_e4m3_encode(v / g);
+            int m = round_quotient_to_table(fabs(v), (double)g, e4m3_mags, 127);
+            c[d] = (uint8_t)(signbit(v) ? (0x80 | m) : m);
         }
     }
     return ORACLE_OK;
@@ -540,8 +591,9 @@ int oracle_sequence_attention(const uint16_t *q, int G, const uint16_t *k, const
 
 /* For request r and prefix token t < prefix_lens[r], row cu_prefix_lens[r] + t
  * of k_ws / v_ws ([total][num_kv_heads][128] BF16) receives the dequantised
- * token, rounded to BF16 (exact when the tensor scale is 1.0: every
- * e2m1 x e4m3 product has at most 5 significant bits). */
+ * token, the exact e2m1 * e4m3 * g rounded to BF16 once (exact when the
+ * tensor scale is 1.0: every e2m1 x e4m3 product has at most 6 significant
+ * bits). */
 int oracle_prefix_dequant(const uint8_t *pool, int64_t num_pages, int page_size, int num_kv_heads, int dtype,
                           float gk, float gv, const int32_t *block_table, int max_pages, const int32_t *prefix_lens,
                           const int32_t *cu_prefix_lens, int num_reqs, uint16_t *k_ws, uint16_t *v_ws)
@@ -560,7 +612,7 @@ int oracle_prefix_dequant(const uint8_t *pool, int64_t num_pages, int page_size,
                 for (int which = 0; which < 2; which++) {
                     uint16_t *dst = (which ? v_ws : k_ws) + (dst_row * num_kv_heads + kv) * HEAD_DIM;
                     dequant_row(&p, page, kv, which, (int)(t % page_size), row);
-                    for (int d = 0; d < HEAD_DIM; d++) dst[d] = oracle_bf16_from_float((float)row[d]);
+                    for (int d = 0; d < HEAD_DIM; d++) dst[d] = oracle_bf16_from_double(row[d]);
                 }
             }
         }

@@ -23,10 +23,16 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 C = os.path.join("oracle", "nvfp4kv_oracle.c")
 
 M = {
-    "ties_away": [("return (lo % 2 == 0) ? lo : hi;", "return hi;")],
-    "scale_drops_g": [("oracle_e4m3_encode(amax / (6.0f * g))", "oracle_e4m3_encode(amax / 6.0f)")],
-    "code_drops_g": [("oracle_e2m1_encode(x[i] / (sd * g))", "oracle_e2m1_encode(x[i] / sd)")],
-    "zero_scale_unsigned": [("codes16[i] = signbit(x[i]) ? 8 : 0;", "codes16[i] = 0;")],
+    "ties_away": [("if (a > mid * den) return hi;\n    return (lo % 2 == 0) ? lo : hi;",
+                   "if (a > mid * den) return hi;\n    return hi;")],
+    "scale_drops_g": [("round_quotient_to_table(amax, 6.0 * (double)g, e4m3_mags, 127)",
+                       "round_quotient_to_table(amax, 6.0, e4m3_mags, 127)")],
+    "code_drops_g": [("round_quotient_to_table(fabs(x[i]), sd * (double)g, e2m1_mags, 8)",
+                      "round_quotient_to_table(fabs(x[i]), sd, e2m1_mags, 8)")],
+    "zero_code_unsigned": [("codes16[i] = (uint8_t)(signbit(x[i]) ? (8 | c) : c);",
+                            "codes16[i] = (uint8_t)(signbit(x[i]) && c ? (8 | c) : c);")],
+    "zero_scale_codes_kept": [("int c = (sd == 0.0) ? 0 : round_quotient_to_table",
+                               "int c = (sd == 0.0) ? 1 : round_quotient_to_table")],
     "dequant_drops_g": [("return oracle_e2m1_value(code) * oracle_e4m3_value(scale) * (double)g;",
                          "return oracle_e2m1_value(code) * oracle_e4m3_value(scale);")],
     "nibble_read_swapped": [("uint8_t code = (d % 2 == 0) ? (byte & 15) : (byte >> 4);",
@@ -45,11 +51,23 @@ M = {
                          "oracle_bf16_value(j->q[((int64_t)b * j->num_q_heads + h * Hkv + kv) * HEAD_DIM + d]);")],
     "extend_causal_short": [("int64_t n = n_prefix + i + 1;", "int64_t n = n_prefix + i + (i > 0 ? 0 : 1);")],
     "prefix_dst_no_cu": [("int64_t dst_row = (int64_t)cu_prefix_lens[r] + t;", "int64_t dst_row = (int64_t)r * 0 + t + cu_prefix_lens[0];")],
-    "fp8_drops_g": [("c[d] = oracle_e4m3_encode(v / g);", "c[d] = oracle_e4m3_encode(v);")],
+    "fp8_drops_g": [("int m = round_quotient_to_table(fabs(v), (double)g, e4m3_mags, 127);",
+                     "int m = round_quotient_to_table(fabs(v), 1.0, e4m3_mags, 127);")],
+    "fp8_fp32_quotient": [("int m = round_quotient_to_table(fabs(v), (double)g, e4m3_mags, 127);",
+                           "int m = oracle_e4m3_encode((float)fabs(v) / g) & 0x7F;")],
+    "scale_fp32_quotient": [("uint8_t s = (uint8_t)round_quotient_to_table(amax, 6.0 * (double)g, e4m3_mags, 127);",
+                             "uint8_t s = oracle_e4m3_encode((float)amax / (6.0f * g));")],
+    "code_fp32_quotient": [("int c = (sd == 0.0) ? 0 : round_quotient_to_table(fabs(x[i]), sd * (double)g, e2m1_mags, 8);",
+                            "int c = (sd == 0.0) ? 0 : (oracle_e2m1_encode((float)fabs(x[i]) / ((float)sd * g)) & 7);")],
+    "dequant_two_roundings": [("dst[d] = oracle_bf16_from_double(row[d]);",
+                               "dst[d] = oracle_bf16_from_float((float)row[d]);")],
+    "bf16_no_subnormal_step": [("int step_exp = (e - 1 >= -126) ? e - 8 : -133;", "int step_exp = e - 8;")],
+    "bf16_ties_up": [("if (r > 0.5 || (r == 0.5 && fmod(f, 2.0) != 0.0)) f += 1.0;", "if (r >= 0.5) f += 1.0;")],
+    "bf16_no_overflow": [("if (v >= ldexp(1.0, 128)) return sign | 0x7f80u;", "if (v > ldexp(1.0, 200)) return sign | 0x7f80u;")],
     "fp8_dequant_drops_g": [("for (int d = 0; d < HEAD_DIM; d++) out[d] = oracle_e4m3_value(c[d]) * (double)g;",
                              "for (int d = 0; d < HEAD_DIM; d++) out[d] = oracle_e4m3_value(c[d]);")],
     "e4m3_subnormal_step": [("ldexp((double)m, -9)", "ldexp((double)m, -10)")],
-    "amax_signed": [("if (fabsf(x[i]) > amax) amax = fabsf(x[i]);", "if (x[i] > amax) amax = x[i];")],
+    "amax_signed": [("if (fabs(x[i]) > amax) amax = fabs(x[i]);", "if (x[i] > amax) amax = x[i];")],
     "bf16_truncates": [("if (lower > 0x8000u || (lower == 0x8000u && (upper & 1u))) upper += 1u;", "(void)lower;")],
     "no_max_shift": [("double pt = exp(scores[h * n + t] - m[h]);", "double pt = exp(scores[h * n + t]);")],
     "extend_prefix_row_offset": [("src = (which ? c->v_pre : c->k_pre) + ((c->pre0 + t) * c->num_kv_heads + c->kv) * HEAD_DIM;",
@@ -64,7 +82,7 @@ M = {
                        "return p->pool + (kv * p->num_pages + page) * oracle_slab_bytes(p->dtype, p->page_size);")],
     "v_codes_offset": [("if (p->dtype == ORACLE_DTYPE_NVFP4) return slab + grp * 2304 + (which ? 1152 : 0) + r * 64;",
                         "if (p->dtype == ORACLE_DTYPE_NVFP4) return slab + grp * 2304 + (which ? 1088 : 0) + r * 64;")],
-    "scale_nonsat_zero": [("if (sd == 0.0f)", "if (sd == 0.0f && 0)")],
+    "scale_nonsat_zero": [("int c = (sd == 0.0) ? 0 :", "int c = (sd == 0.0 && 0) ? 0 :")],
     "bf16_row_stride": [("int rc = store_row(&c->p, 0, 0, which, 0, (which ? c->v : c->k) + t * c->row_stride);",
                          "int rc = store_row(&c->p, 0, 0, which, 0, (which ? c->v : c->k) + t * 128);")],
     "prefix_kv_index": [("uint16_t *dst = (which ? v_ws : k_ws) + (dst_row * num_kv_heads + kv) * HEAD_DIM;",

@@ -74,6 +74,7 @@ def _desc(m, **kw):
 @pytest.mark.parametrize("kw,status", [
     (dict(head_dim=64), -2), (dict(page_size=48), -2), (dict(dtype=7), -2), (dict(num_kv_heads=0), -1),
     (dict(k_global_scale=0.0), -1), (dict(v_global_scale=float("inf")), -1), (dict(pool=4097), -1),
+    (dict(k_global_scale=1e-40), -1), (dict(v_global_scale=-2.0), -1), (dict(k_global_scale=float("nan")), -1),
     (dict(pool=0), -1), (dict(num_pages=0), -1),
 ])
 def test_invalid_cache_descriptors_are_rejected_before_any_launch(m, kw, status):
