@@ -48,6 +48,8 @@
 // timeout is recorded in the device error word and ends every warp's loop.
 #include <cuda.h>
 
+#include <type_traits>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "quantize.cuh"
@@ -456,24 +458,32 @@ __global__ void __launch_bounds__(kPaged ? kEThreadsPaged : kEThreads, 1)
                 if (!ok) break;
                 const uint8_t *src = which ? rawv + s * kRawHalf : rawk;
                 uint8_t *tile = smem + (which ? kOffV : kOffK) + s * kKVTile;
+                const float g = which ? a.gv : a.gk;
+                auto expand = [&](auto unit) {  // unit: g = 1, chosen once per tile (the general form is long)
 #pragma unroll
-                for (int i = 0; i < kPer; i++) {
-                    const int b = dt + i * kDqThreads;
-                    if (b >= kBlocks) continue;
-                    const int key = b >> 3, blk = b & 7, tok = j * kKeys + key;
-                    uint32_t o[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
-                    if (tok < np) {
-                        const uint8_t *grp = src + (key >> 4) * kHalfGroup;  // codes [16][64] then scales
-                        const int rr = key & 15;
-                        const uint2 codes = *reinterpret_cast<const uint2 *>(grp + rr * 64 + blk * 8);
-                        const uint32_t sb = grp[1024 + (which ? blk * 16 + rr : rr * 8 + blk)];
-                        nvfp4_block_to_bf16(codes, sb, which ? a.gv : a.gk, o);
+                    for (int i = 0; i < kPer; i++) {
+                        const int b = dt + i * kDqThreads;
+                        if (b >= kBlocks) continue;
+                        const int key = b >> 3, blk = b & 7, tok = j * kKeys + key;
+                        uint32_t o[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+                        if (tok < np) {
+                            const uint8_t *grp = src + (key >> 4) * kHalfGroup;  // codes [16][64] then scales
+                            const int rr = key & 15;
+                            const uint2 codes = *reinterpret_cast<const uint2 *>(grp + rr * 64 + blk * 8);
+                            const uint32_t sb = grp[1024 + (which ? blk * 16 + rr : rr * 8 + blk)];
+                            nvfp4_block_to_bf16<decltype(unit)::value>(codes, sb, g, o);
+                        }
+                        uint8_t *cb = tile + (blk >> 2) * kKVBlock;  // column block of head_dim 64 (blk / 4) ..
+                        *reinterpret_cast<uint4 *>(cb + sw128_off(key, (blk & 3) * 2)) =
+                            make_uint4(o[0], o[1], o[2], o[3]);
+                        *reinterpret_cast<uint4 *>(cb + sw128_off(key, (blk & 3) * 2 + 1)) =
+                            make_uint4(o[4], o[5], o[6], o[7]);
                     }
-                    uint8_t *cb = tile + (blk >> 2) * kKVBlock;  // column block of head_dim 64 (blk / 4) ..
-                    *reinterpret_cast<uint4 *>(cb + sw128_off(key, (blk & 3) * 2)) = make_uint4(o[0], o[1], o[2], o[3]);
-                    *reinterpret_cast<uint4 *>(cb + sw128_off(key, (blk & 3) * 2 + 1)) =
-                        make_uint4(o[4], o[5], o[6], o[7]);
-                }
+                };
+                if (g == 1.0f)
+                    expand(std::true_type{});
+                else
+                    expand(std::false_type{});
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the tile for the tensor core
                 mbar_arrive(which ? &v_dq[s] : &k_dq[s]);
                 // the raw half is read: the tile after next (K) or the next (V) may land in it

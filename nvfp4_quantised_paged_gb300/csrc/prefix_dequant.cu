@@ -80,15 +80,26 @@ __global__ void __launch_bounds__(256) prefix_dequant_kernel(PrefixArgs a) {
         const uint8_t *grp = slab + (rp >> 4) * 2304;
         const uint2 codes = __ldg(reinterpret_cast<const uint2 *>(grp + (which ? 1152 : 0) + rr * 64 + blk * 8));
         const uint32_t sbyte = __ldg(grp + (which ? 2176 + blk * 16 + rr : 1024 + rr * 8 + blk));
-        nvfp4_block_to_bf16(codes, sbyte, g, o);
+        if (g == 1.0f)
+            nvfp4_block_to_bf16<true>(codes, sbyte, g, o);
+        else
+            nvfp4_block_to_bf16<false>(codes, sbyte, g, o);
     } else {
         const uint4 c = __ldg(
             reinterpret_cast<const uint4 *>(slab + (rp >> 4) * 4096 + (which ? 2048 : 0) + rr * 128 + blk * 16));
         const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+        if (g == 1.0f) {
 #pragma unroll
-        for (int i = 0; i < 4; i++) {
-            o[2 * i] = f16x2_to_bf16x2_scaled(e4m3x2_to_f16x2(w[i] & 0xffffu), g);
-            o[2 * i + 1] = f16x2_to_bf16x2_scaled(e4m3x2_to_f16x2(w[i] >> 16), g);
+            for (int i = 0; i < 4; i++) {
+                o[2 * i] = f16x2_to_bf16x2_scaled<true>(e4m3x2_to_f16x2(w[i] & 0xffffu), g);
+                o[2 * i + 1] = f16x2_to_bf16x2_scaled<true>(e4m3x2_to_f16x2(w[i] >> 16), g);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 4; i++) {
+                o[2 * i] = f16x2_to_bf16x2_scaled<false>(e4m3x2_to_f16x2(w[i] & 0xffffu), g);
+                o[2 * i + 1] = f16x2_to_bf16x2_scaled<false>(e4m3x2_to_f16x2(w[i] >> 16), g);
+            }
         }
     }
     uint4 *dst = (which ? a.v_ws : a.k_ws) + ((int64_t)row * a.Hkv + h) * (kHeadDim / 8) + blk * 2;

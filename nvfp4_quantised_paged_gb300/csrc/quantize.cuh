@@ -190,23 +190,26 @@ __device__ __forceinline__ uint32_t f32x2_to_bf16x2(float hi, float lo) {
 }
 
 // f16x2 holding exact values -> bf16x2 of (value * g), each the exact product
-// rounded to BF16 once (a plain conversion when g = 1).
+// rounded to BF16 once; kUnit (g = 1): a plain, exact conversion.  Callers pick
+// kUnit outside their loops (the general form is long).
+template <bool kUnit>
 __device__ __forceinline__ uint32_t f16x2_to_bf16x2_scaled(uint32_t x, float g) {
-    if (g == 1.0f) return f32x2_to_bf16x2(f16_hi(x), f16_lo(x));
+    if (kUnit) return f32x2_to_bf16x2(f16_hi(x), f16_lo(x));
     return bf16_of_product(f16_lo(x), g) | (bf16_of_product(f16_hi(x), g) << 16);
 }
 
 // One NVFP4 16-value block (8 code bytes, one E4M3 scale byte) -> 8 BF16 pairs
 // of e2m1 * e4m3 * g, the exact product rounded to BF16 once (exact for g = 1:
 // at most 6 significant bits): the prefix dequant kernel and the paged extend
-// kernel both expand blocks this way.
+// kernel both expand blocks this way.  kUnit: g = 1.
+template <bool kUnit>
 __device__ __forceinline__ void nvfp4_block_to_bf16(uint2 codes, uint32_t sbyte, float g, uint32_t (&o)[8]) {
     const uint32_t s2 = e4m3x2_to_f16x2(sbyte | (sbyte << 8));  // {s, s}
     uint32_t f[8];
     e2m1x8_to_f16x2x4(codes.x, f[0], f[1], f[2], f[3]);
     e2m1x8_to_f16x2x4(codes.y, f[4], f[5], f[6], f[7]);
 #pragma unroll
-    for (int i = 0; i < 8; i++) o[i] = f16x2_to_bf16x2_scaled(hmul2(f[i], s2), g);
+    for (int i = 0; i < 8; i++) o[i] = f16x2_to_bf16x2_scaled<kUnit>(hmul2(f[i], s2), g);
 }
 
 // Quantise block `blk` (0..7) of K (which = 0) or V (which = 1) of one
