@@ -65,3 +65,10 @@ def test_both_arms_report_the_same_workload_keys():
     assert c["workload"] == w.name and c["batch"] == 64 and c["seq_len"] == 32768
     assert (c["num_q_heads"], c["num_kv_heads"], c["head_dim"], c["page_size"]) == (64, 8, 128, 64)
     assert c["parallelism"] == "single GPU" and bench.workload_config(w, 4)["parallelism"] == "replicas"
+
+
+def test_roofline_kernel_is_timed_over_many_launches_whatever_the_steps():
+    """The decode kernel's roofline time is the mean of a fixed number of
+    dedicated launches after the timed region, not of a sample of it."""
+    assert bench.ROOFLINE_LAUNCHES >= 50
+    assert bench.PROFILE_EVERY >= 1
