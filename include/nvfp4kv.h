@@ -145,7 +145,11 @@ NVFP4KV_API int nvfp4_kv_quantize_append(const nvfp4kv_cache *cache, const void 
  *   scales        device float[2], 8-byte aligned, written with {g_K, g_V}
  *                 (also used as scratch while the call runs on `stream`).
  * Pass the results as k_global_scale / v_global_scale of the cache
- * descriptor before appending.  Returns NVFP4KV_EINVAL for a bad argument.
+ * descriptor before appending.  A tensor whose largest finite magnitude is
+ * below 2^-126 * 2688 (about 3.2e-35) gets a subnormal g, which the cache
+ * descriptor does not accept (a tensor scale is a positive normal FP32
+ * number): keep g = 1 for such a tensor.  Returns NVFP4KV_EINVAL for a bad
+ * argument.
  */
 NVFP4KV_API int nvfp4kv_calibrate_global_scales(const void *k, const void *v, int64_t num_tokens, int num_kv_heads,
                                                 int64_t token_stride, float *scales, cudaStream_t stream);
