@@ -164,9 +164,11 @@ NVFP4KV_API int nvfp4kv_decode_auto_splits(const nvfp4kv_cache *cache, int num_q
 
 /* Kernel launches one nvfp4_paged_decode_attention (shared_len = 0) or
  * nvfp4_cascade_decode_attention (shared_len > 0) call of this shape makes:
- * the plan, the decode kernel and the log-sum-exp reduction, plus the
- * shared-prefix kernel for a cascade call; the fused append variant makes as
- * many.  0 if the arguments are invalid (or batch = 0: nothing is launched). */
+ * the decode kernel and the log-sum-exp reduction (2) for a batch of at most
+ * 96 sequences, which every decode CTA plans itself from seq_lens; the plan
+ * kernel as well (3) for a larger batch; the plan and the shared-prefix kernel
+ * as well (4) for a cascade call.  The fused append variant makes as many.
+ * 0 if the arguments are invalid (or batch = 0: nothing is launched). */
 NVFP4KV_API int nvfp4kv_decode_launch_count(const nvfp4kv_cache *cache, int batch, int num_q_heads, int num_splits,
                                             int shared_len);
 

@@ -251,7 +251,8 @@ int nvfp4kv_decode_launch_count(const nvfp4kv_cache *cache, int batch, int num_q
     if (check_cache(cache) || batch < 1 || num_q_heads < 1 || num_q_heads % cache->num_kv_heads || num_splits < 0 ||
         shared_len < 0 || num_q_heads / cache->num_kv_heads > 16)
         return 0;
-    return shared_len > 0 ? 4 : 3;  // plan, (shared prefix,) decode, reduction
+    // (plan,) (shared prefix,) decode, reduction: a small batch without a shared prefix is planned in the decode CTAs
+    return decode_plans_in_cta(batch, shared_len > 0) ? 2 : shared_len > 0 ? 4 : 3;
 }
 
 size_t nvfp4kv_decode_workspace_bytes(const nvfp4kv_cache *cache, int batch, int num_q_heads, int num_splits) {

@@ -84,9 +84,17 @@ struct Group<NVFP4KV_DTYPE_FP8_E4M3> {
     static constexpr int kKq = 0, kVq = 2048;
 };
 
+// Batches of up to kPlanInCta sequences are planned inside every decode CTA
+// (the chunk prefix in shared memory, unsigned 32-bit: a sequence has at most
+// 2^25 chunks, as seq_lens are int32) instead of by a separate plan kernel,
+// whose launch and completion would sit between the previous work on the
+// stream and the first bulk copy.
+constexpr int kPlanInCta = 96;
+
 // Shared memory of one CTA: a ring of kSlots 64-token stages, their
 // mbarriers, the mask of groups each stage holds, the index of the chunk last
-// issued into each stage, and an abort flag.
+// issued into each stage, an abort flag and, for a batch planned in the CTA,
+// the chunk prefix (B + 1 entries).
 template <int DTYPE>
 struct Smem {
     static constexpr int kStage = kGroups * Group<DTYPE>::kBytes;
@@ -94,7 +102,10 @@ struct Smem {
     static constexpr int kFlags = kBars + kSlots * 8;       // int valid[kSlots]
     static constexpr int kSeq = kFlags + kSlots * 4;        // int seq[kSlots]
     static constexpr int kAbort = kSeq + kSlots * 4;        // int abort
-    static constexpr int kTotal = kAbort + 4;
+    static constexpr int kPrefix = (kAbort + 4 + 15) & ~15;  // u32 prefix[B + 1] (planned in the CTA)
+    static constexpr int kTotal = kAbort + 4;               // without the prefix
+    static constexpr int kMax = kPrefix + 4 * (kPlanInCta + 1);
+    static int bytes(int B, bool in_cta) { return in_cta ? kPrefix + 4 * (B + 1) : kTotal; }
 };
 
 struct DecodeArgs {
@@ -107,6 +118,7 @@ struct DecodeArgs {
     const int32_t *block_table;
     const int32_t *seq_lens;
     const int64_t *chunk_prefix;  // [B + 1], chunks of 64 tokens per sequence (exclusive scan)
+    int plan_in_cta;              // 1: every CTA computes the prefix into shared memory (chunk_prefix unused)
     float score_log2;             // sm_scale * g_K * log2(e)
     float gv;
     __nv_bfloat16 *out;
@@ -130,18 +142,39 @@ __device__ __forceinline__ int clamp_len(int32_t n, int64_t cap) {
     return (int64_t)n > cap ? (int)cap : n;
 }
 
+// 64-token chunks of a sequence of n tokens whose first `skip` are left to the
+// shared-prefix kernel, n clamped to the block table's capacity: the plan
+// kernel, the in-CTA plan and the reduction's own plan all count this way.
+__device__ __forceinline__ int64_t seq_chunks(int32_t n, int64_t max_tokens, int skip) {
+    const int64_t m = n < skip ? 0 : ((int64_t)n > max_tokens ? max_tokens : n) - skip;
+    return (m + kChunk - 1) / kChunk;
+}
+
+// Entry i of the chunk prefix: from this CTA's shared memory when the batch
+// is planned in the CTA, else from the plan kernel's array.
+template <int DTYPE>
+__device__ __forceinline__ int64_t chunk_prefix_at(const DecodeArgs &a, int i) {
+    if (a.plan_in_cta) {
+        extern __shared__ __align__(128) uint8_t smem[];
+        return reinterpret_cast<const uint32_t *>(smem + Smem<DTYPE>::kPrefix)[i];
+    }
+    return a.chunk_prefix[i];
+}
+
 // A unit of the CTA's range: chunk ch (of nch) of KV head kv of sequence b,
 // whose clamped length is n.
 struct Cursor {
     int b, kv, ch, nch, n;
 };
 
+template <int DTYPE>
 __device__ __forceinline__ void cursor_seq(Cursor &cu, const DecodeArgs &a) {
-    cu.nch = (int)(a.chunk_prefix[cu.b + 1] - a.chunk_prefix[cu.b]);
+    cu.nch = (int)(chunk_prefix_at<DTYPE>(a, cu.b + 1) - chunk_prefix_at<DTYPE>(a, cu.b));
     cu.n = clamp_len(a.seq_lens[cu.b], (int64_t)a.max_pages * a.P);
 }
 
 // Move the cursor `steps` units forward (the caller keeps it inside the range).
+template <int DTYPE>
 __device__ __forceinline__ void cursor_advance(Cursor &cu, const DecodeArgs &a, int steps) {
     cu.ch += steps;
     while (cu.ch >= cu.nch) {
@@ -150,9 +183,9 @@ __device__ __forceinline__ void cursor_advance(Cursor &cu, const DecodeArgs &a, 
         cu.kv = 0;
         do {
             ++cu.b;
-        } while (cu.b < a.B && a.chunk_prefix[cu.b + 1] == a.chunk_prefix[cu.b]);
+        } while (cu.b < a.B && chunk_prefix_at<DTYPE>(a, cu.b + 1) == chunk_prefix_at<DTYPE>(a, cu.b));
         if (cu.b >= a.B) return;
-        cursor_seq(cu, a);
+        cursor_seq<DTYPE>(cu, a);
     }
 }
 
@@ -174,11 +207,12 @@ __device__ __forceinline__ uint64_t part_src(const DecodeArgs &a, int64_t u0, in
     int lo = 0, hi = a.B - 1;
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if ((int64_t)a.Hkv * a.chunk_prefix[mid] <= u) lo = mid;
+        if ((int64_t)a.Hkv * chunk_prefix_at<DTYPE>(a, mid) <= u) lo = mid;
         else hi = mid - 1;
     }
-    const int nch = (int)(a.chunk_prefix[lo + 1] - a.chunk_prefix[lo]);
-    const int rem = (int)(u - (int64_t)a.Hkv * a.chunk_prefix[lo]);
+    const int64_t p_lo = chunk_prefix_at<DTYPE>(a, lo);
+    const int nch = (int)(chunk_prefix_at<DTYPE>(a, lo + 1) - p_lo);
+    const int rem = (int)(u - (int64_t)a.Hkv * p_lo);
     const int kv = rem / nch, ch = rem - kv * nch;
     const int n = clamp_len(a.seq_lens[lo], (int64_t)a.max_pages * a.P);
     const int span = a.P < kChunk ? a.P : kChunk;
@@ -598,21 +632,24 @@ __device__ __forceinline__ void fence_proxy_async_global() {
 // is the only one that reads the sequence's last token, so it quantises that
 // token (16 threads per pair: K and V x 8 blocks) before any of its copies
 // are issued.  Pairs are visited from the one holding unit u0 on.
+template <int DTYPE>
 __device__ __forceinline__ void fused_append(const DecodeArgs &a, int64_t u0, int64_t u1, int tid) {
     int lo = 0, hi = a.B - 1;  // the sequence holding unit u0
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if ((int64_t)a.Hkv * a.chunk_prefix[mid] <= u0) lo = mid;
+        if ((int64_t)a.Hkv * chunk_prefix_at<DTYPE>(a, mid) <= u0) lo = mid;
         else hi = mid - 1;
     }
-    const int nch0 = (int)(a.chunk_prefix[lo + 1] - a.chunk_prefix[lo]);
-    const int64_t first_pair = (int64_t)lo * a.Hkv + (u0 - (int64_t)a.Hkv * a.chunk_prefix[lo]) / nch0;
+    const int64_t p_lo = chunk_prefix_at<DTYPE>(a, lo);
+    const int nch0 = (int)(chunk_prefix_at<DTYPE>(a, lo + 1) - p_lo);
+    const int64_t first_pair = (int64_t)lo * a.Hkv + (u0 - (int64_t)a.Hkv * p_lo) / nch0;
     const int part = tid & 15, which = part >> 3, blk = part & 7;
     for (int64_t p = first_pair + (tid >> 4);; p += kThreads / 16) {
         const int b = (int)(p / a.Hkv), kv = (int)(p - (int64_t)b * a.Hkv);
         if (b >= a.B) break;
-        const int64_t nch = a.chunk_prefix[b + 1] - a.chunk_prefix[b];
-        const int64_t start = (int64_t)a.Hkv * a.chunk_prefix[b] + kv * nch;
+        const int64_t pb = chunk_prefix_at<DTYPE>(a, b);
+        const int64_t nch = chunk_prefix_at<DTYPE>(a, b + 1) - pb;
+        const int64_t start = (int64_t)a.Hkv * pb + kv * nch;
         if (start >= u1) break;
         if (nch == 0 || start + nch - 1 >= u1) continue;  // its last unit belongs to a later CTA
         const int t = clamp_len(a.seq_lens[b], (int64_t)a.max_pages * a.P) - 1;
@@ -640,18 +677,48 @@ __global__ void __launch_bounds__(kThreads, DTYPE == NVFP4KV_DTYPE_NVFP4 && NT =
     using S = Smem<DTYPE>;
     extern __shared__ __align__(128) uint8_t smem[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    // chunk_prefix comes from the plan kernel.  Behind the shared-prefix
-    // kernel, this grid starts only once every CTA of that kernel has waited
-    // for the plan to complete (and flush) and then triggered, so the plan's
-    // results are in global memory already and the wait moves to the exit:
-    // the decode then runs beside the shared-prefix kernel, and its own
-    // completion, which the reduction waits for, implies that kernel's.
+    // chunk_prefix comes from the plan kernel, or, for a batch planned in the
+    // CTA, from this CTA's own scan of seq_lens below.  Behind the
+    // shared-prefix kernel, this grid starts only once every CTA of that
+    // kernel has waited for the plan to complete (and flush) and then
+    // triggered, so the plan's results are in global memory already and the
+    // wait moves to the exit: the decode then runs beside the shared-prefix
+    // kernel, and its own completion, which the reduction waits for, implies
+    // that kernel's.
     if (!a.after_shared) pdl_wait();
     // The reduction may be scheduled once every CTA is past this point, so
-    // with the plan complete: it reads chunk_prefix before its own wait.
+    // with the plan (or, planned in the CTA, the work that wrote seq_lens)
+    // complete: it reads chunk_prefix (or seq_lens) before its own wait.
     pdl_launch_dependents();
 
-    const int64_t U = (int64_t)a.Hkv * a.chunk_prefix[a.B];
+    if (a.plan_in_cta) {  // exclusive scan of the chunk counts, B <= 2 * kThreads
+        uint32_t *sp = reinterpret_cast<uint32_t *>(smem + S::kPrefix);
+        uint32_t *wsum = reinterpret_cast<uint32_t *>(smem);  // scratch: no copy has been issued into the ring yet
+        const int64_t max_tokens = (int64_t)a.max_pages * a.P;
+        const int b0 = 2 * tid, b1 = b0 + 1;
+        uint32_t c0 = 0, c1 = 0;
+        if (b0 < a.B) c0 = (uint32_t)seq_chunks(a.seq_lens[b0], max_tokens, 0);
+        if (b1 < a.B) c1 = (uint32_t)seq_chunks(a.seq_lens[b1], max_tokens, 0);
+        if (blockIdx.x == 0 && ((b0 < a.B && (a.seq_lens[b0] < 0 || (int64_t)a.seq_lens[b0] > max_tokens)) ||
+                                (b1 < a.B && (a.seq_lens[b1] < 0 || (int64_t)a.seq_lens[b1] > max_tokens))))
+            flag_error(a.err, kErrSeqLen);
+        uint32_t incl = c0 + c1;
+#pragma unroll
+        for (int x = 1; x < 32; x <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xffffffffu, incl, x);
+            if (lane >= x) incl += y;
+        }
+        if (lane == 31) wsum[warp] = incl;
+        __syncthreads();
+        if (warp > 0) incl += wsum[0];
+        const uint32_t excl = incl - c0 - c1;
+        if (b0 < a.B) sp[b0] = excl;
+        if (b1 < a.B) sp[b1] = excl + c0;
+        if (tid == kThreads - 1) sp[a.B] = incl;
+        __syncthreads();
+    }
+
+    const int64_t U = (int64_t)a.Hkv * chunk_prefix_at<DTYPE>(a, a.B);
     const int64_t c = blockIdx.x;
     const int64_t u0 = c * U / a.grid, u1 = (c + 1) * U / a.grid;
     if (u0 >= u1) {
@@ -676,7 +743,7 @@ __global__ void __launch_bounds__(kThreads, DTYPE == NVFP4KV_DTYPE_NVFP4 && NT =
         fence_mbar_init();
     }
     if (a.k_new) {
-        fused_append(a, u0, u1, tid);
+        fused_append<DTYPE>(a, u0, u1, tid);
         fence_proxy_async_global();  // the stores above before this CTA's bulk reads of the same rows
     }
     __syncthreads();
@@ -707,12 +774,12 @@ __global__ void __launch_bounds__(kThreads, DTYPE == NVFP4KV_DTYPE_NVFP4 && NT =
         int lo = 0, hi = a.B - 1;
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
-            if ((int64_t)a.Hkv * a.chunk_prefix[mid] <= uw) lo = mid;
+            if ((int64_t)a.Hkv * chunk_prefix_at<DTYPE>(a, mid) <= uw) lo = mid;
             else hi = mid - 1;
         }
         cc.b = lo;
-        cursor_seq(cc, a);
-        const int rem = (int)(uw - (int64_t)a.Hkv * a.chunk_prefix[lo]);
+        cursor_seq<DTYPE>(cc, a);
+        const int rem = (int)(uw - (int64_t)a.Hkv * chunk_prefix_at<DTYPE>(a, lo));
         cc.kv = rem / cc.nch;
         cc.ch = rem - cc.kv * cc.nch;
     }
@@ -808,7 +875,7 @@ __global__ void __launch_bounds__(kThreads, DTYPE == NVFP4KV_DTYPE_NVFP4 && NT =
                                &valid[slot]);
             if (lane == 0) st_release_shared(&seq[slot], j);
         }
-        if (i + kWarps < nstages) cursor_advance(cc, a, kWarps);
+        if (i + kWarps < nstages) cursor_advance<DTYPE>(cc, a, kWarps);
         slot += kWarps;
         if (slot >= kSlots) {
             slot -= kSlots;
@@ -842,8 +909,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t *seq_lens, int
     for (int b = lo; b < hi; b++) {
         const int32_t n = seq_lens[b];
         if (n < skip || (int64_t)n > max_tokens) flag_error(err, kErrSeqLen);
-        const int64_t m = n < skip ? 0 : ((int64_t)n > max_tokens ? max_tokens : n) - skip;
-        local += (m + kChunk - 1) / kChunk;
+        local += seq_chunks(n, max_tokens, skip);
     }
     // block-wide exclusive scan of `local`
     const int lane = tid & 31, warp = tid >> 5;
@@ -868,16 +934,16 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t *seq_lens, int
     int64_t run = incl - local + (warp > 0 ? warp_sums[warp - 1] : 0);
     for (int b = lo; b < hi; b++) {
         prefix[b] = run;
-        const int32_t n = seq_lens[b];
-        const int64_t m = n < skip ? 0 : ((int64_t)n > max_tokens ? max_tokens : n) - skip;
-        run += (m + kChunk - 1) / kChunk;
+        run += seq_chunks(seq_lens[b], max_tokens, skip);
     }
     if (tid == 1023) prefix[B] = warp_sums[31];
 }
 
 struct ReduceArgs {
     int B, Hq, Hkv, G, grid;
-    const int64_t *chunk_prefix;
+    const int64_t *chunk_prefix;  // nullptr: the batch was planned in the decode CTAs (plan from seq_lens here)
+    const int32_t *seq_lens;
+    int64_t max_tokens;
     const float *part_acc;
     const float2 *part_ml;
     const float *casc_acc;  // shared-prefix partials [casc_splits][B * Hkv][G] (nullptr: none)
@@ -928,10 +994,31 @@ __global__ void __launch_bounds__(32 * kReduceWarps) reduce_kernel(ReduceArgs a,
         kv = h / a.G;
         hh = h % a.G;
         p = (int64_t)b * a.Hkv + kv;
-        const long long *cp = reinterpret_cast<const long long *>(a.chunk_prefix);
-        const int64_t pb = __ldcg(cp + b);
-        nch = __ldcg(cp + b + 1) - pb;
-        U = (int64_t)a.Hkv * __ldcg(cp + a.B);
+        int64_t pb = 0, total = 0;
+        if (a.chunk_prefix) {
+            const long long *cp = reinterpret_cast<const long long *>(a.chunk_prefix);
+            pb = __ldcg(cp + b);
+            nch = __ldcg(cp + b + 1) - pb;
+            total = __ldcg(cp + a.B);
+        } else {  // the warp scans the chunk counts itself, as each decode CTA did (row, so b, is warp-uniform)
+            for (int base = 0; base < a.B; base += 32) {
+                const int bb = base + lane;
+                const uint32_t cnt = bb < a.B ? (uint32_t)seq_chunks(a.seq_lens[bb], a.max_tokens, 0) : 0u;
+                uint32_t incl = cnt;
+#pragma unroll
+                for (int x = 1; x < 32; x <<= 1) {
+                    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, x);
+                    if (lane >= x) incl += y;
+                }
+                const int in_seg = b - base;
+                if (in_seg >= 0 && in_seg < 32) {
+                    pb = total + (int64_t)__shfl_sync(0xffffffffu, incl - cnt, in_seg);
+                    nch = (int64_t)__shfl_sync(0xffffffffu, cnt, in_seg);
+                }
+                total += (int64_t)__shfl_sync(0xffffffffu, incl, 31);
+            }
+        }
+        U = (int64_t)a.Hkv * total;
         if (nch > 0) {
             off = (int64_t)a.Hkv * pb + (int64_t)kv * nch;
             c0 = udiv64((off + 1) * a.grid - 1, U);
@@ -1047,13 +1134,14 @@ const void *kernel_fn() {
     return reinterpret_cast<const void *>(&decode_kernel<DTYPE, NT>);
 }
 
+// smem_bytes: the most the kernel is ever launched with (a batch planned in the CTA).
 const void *select_kernel(int dtype, int nt, int *smem_bytes) {
     if (dtype == NVFP4KV_DTYPE_NVFP4) {
-        *smem_bytes = Smem<0>::kTotal;
+        *smem_bytes = Smem<0>::kMax;
         if (nt == 1) return kernel_fn<0, 1>();
         return kernel_fn<0, 2>();
     }
-    *smem_bytes = Smem<1>::kTotal;
+    *smem_bytes = Smem<1>::kMax;
     if (nt == 1) return kernel_fn<1, 1>();
     return kernel_fn<1, 2>();
 }
@@ -1091,6 +1179,8 @@ cudaError_t prepare_kernel(int dtype, int nt, int *grid_out) {
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 }  // namespace
+
+bool decode_plans_in_cta(int batch, bool shared_prefix) { return !shared_prefix && batch <= kPlanInCta; }
 
 int decode_auto_grid(const nvfp4kv_cache &c, int group, cudaError_t *status) {
     int grid = 0;
@@ -1132,9 +1222,10 @@ cudaError_t launch_decode(const nvfp4kv_cache &c, const void *q, int batch, int 
     float *casc_acc = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(casc_ml) +
                                                 align256(sizeof(float2) * (size_t)csplits * batch * num_q_heads));
     const int skip = shared_pages ? shared_len : 0;
-
-    {
-        int64_t max_tokens = (int64_t)max_pages * c.page_size;
+    int64_t max_tokens = (int64_t)max_pages * c.page_size;
+    // A small batch is planned in every decode CTA; otherwise by the plan kernel.
+    const bool plan_in_cta = decode_plans_in_cta(batch, shared_pages != nullptr);
+    if (!plan_in_cta) {
         int skip_arg = skip;
         void *pargs[] = {&seq_lens, &batch, &max_tokens, &prefix, &err, &skip_arg};
         e = launch_pdl(reinterpret_cast<const void *>(&plan_kernel), 1, 1024, 0, stream, pargs);
@@ -1161,6 +1252,7 @@ cudaError_t launch_decode(const nvfp4kv_cache &c, const void *q, int batch, int 
     a.block_table = block_table;
     a.seq_lens = seq_lens;
     a.chunk_prefix = prefix;
+    a.plan_in_cta = plan_in_cta ? 1 : 0;
     a.score_log2 = (float)((double)sm_scale * (double)c.k_global_scale * 1.4426950408889634);
     a.gv = c.v_global_scale;
     a.out = static_cast<__nv_bfloat16 *>(out);
@@ -1178,8 +1270,10 @@ cudaError_t launch_decode(const nvfp4kv_cache &c, const void *q, int batch, int 
     a.pool_w = static_cast<uint8_t *>(c.pool);
     a.skip = skip;
     a.after_shared = shared_pages ? 1 : 0;
-    int smem = 0;
-    const void *fn = select_kernel(c.dtype, nt, &smem);
+    int smem_max = 0;
+    const void *fn = select_kernel(c.dtype, nt, &smem_max);
+    const int smem = c.dtype == NVFP4KV_DTYPE_NVFP4 ? Smem<0>::bytes(batch, plan_in_cta)
+                                                    : Smem<1>::bytes(batch, plan_in_cta);
     void *args[] = {&a};
     if (before && (e = cudaEventRecord(before, stream)) != cudaSuccess) return e;
     e = launch_pdl(fn, (unsigned)grid, kThreads, (size_t)smem, stream, args);
@@ -1192,7 +1286,9 @@ cudaError_t launch_decode(const nvfp4kv_cache &c, const void *q, int batch, int 
     r.Hkv = c.num_kv_heads;
     r.G = G;
     r.grid = grid;
-    r.chunk_prefix = prefix;
+    r.chunk_prefix = plan_in_cta ? nullptr : prefix;
+    r.seq_lens = seq_lens;
+    r.max_tokens = max_tokens;
     r.part_acc = part_acc;
     r.part_ml = part_ml;
     r.casc_ml = shared_pages ? casc_ml : nullptr;

@@ -21,6 +21,10 @@ cudaError_t launch_prefix_dequant(const nvfp4kv_cache &c, const int32_t *block_t
 // Number of decode CTAs an auto split uses (SM count x resident CTAs per SM).
 int decode_auto_grid(const nvfp4kv_cache &c, int group, cudaError_t *status);
 
+// Whether a decode call plans its split inside the decode CTAs (a small batch
+// without a shared prefix) instead of launching the plan kernel first.
+bool decode_plans_in_cta(int batch, bool shared_prefix);
+
 // Workspace bytes for a decode call with `grid` CTAs.
 size_t decode_workspace_bytes(const nvfp4kv_cache &c, int batch, int num_q_heads, int grid);
 

@@ -144,8 +144,11 @@ def test_paged_extend_and_launch_count_arguments(m):
     assert lib.nvfp4_extend_attention_paged(d, *bad) == -1
     bad = list(args); bad[8] = 0                                 # no requests: nothing to do
     assert lib.nvfp4_extend_attention_paged(d, *bad) == 0
-    # launch count: plan + decode + reduction, plus the shared-prefix kernel for a cascade call
-    assert lib.nvfp4kv_decode_launch_count(d, 4, 8, 0, 0) == 3
+    # launch count: decode + reduction for a batch of up to 96 (planned in the decode CTAs), the plan
+    # kernel as well for a larger one, and the shared-prefix kernel for a cascade call (planned by the plan kernel)
+    assert lib.nvfp4kv_decode_launch_count(d, 4, 8, 0, 0) == 2
+    assert lib.nvfp4kv_decode_launch_count(d, 96, 8, 0, 0) == 2
+    assert lib.nvfp4kv_decode_launch_count(d, 97, 8, 0, 0) == 3
     assert lib.nvfp4kv_decode_launch_count(d, 4, 8, 0, 128) == 4
     assert lib.nvfp4kv_decode_launch_count(d, 0, 8, 0, 0) == 0
     assert lib.nvfp4kv_decode_launch_count(d, 4, 3, 0, 0) == 0

@@ -52,6 +52,29 @@ def test_split_count_does_not_change_the_result_beyond_tolerance(m, splits):
     check_attention(out, ref, "splits=%d" % splits, spread=spread)
 
 
+# Batches of up to 96 sequences are planned inside every decode CTA (two
+# sequences per thread of the 64-thread CTA, the reduction scanning seq_lens in
+# each warp), larger ones by the plan kernel: both sides of the threshold, with
+# ragged and empty sequences, and the launch count of each.
+@pytest.mark.parametrize("B", [1, 33, 95, 96, 97, 160])
+def test_batch_planned_in_cta_and_by_plan_kernel(m, B):
+    rng = np.random.default_rng(700 + B)
+    lens = [int(x) for x in rng.integers(1, 400, size=B)]
+    if B > 1:
+        lens[B // 2] = 0
+    w = workloads.make_decode("plan%d" % B, 700 + B, lens, 16, 2, 32)
+    cache, pool = fill_both(w, m)
+    assert m.decode_launch_count(cache, B, 16) == (2 if B <= 96 else 3)
+    out, ref, spread = decode_both(w, m, cache, pool)
+    check_attention(out, ref, "B=%d" % B, spread=spread)
+    assert m.check_device_errors() == 0
+    # a length beyond the block table is clamped and flagged either way
+    sl = w.seq_lens.clone()
+    sl[B - 1] = w.block_table.shape[1] * 32 + 5
+    m.paged_decode_attention(cache, w.q("cuda"), w.block_table.cuda(), sl.cuda())
+    assert m.check_device_errors() == -4
+
+
 def test_channel_outliers_long_sequence(m):
     w = workloads.make_decode("c", 6, [20000, 7], 40, 8, 64, recipe=workloads.ValueRecipe(channel_lognormal=True))
     cache, pool = fill_both(w, m)
