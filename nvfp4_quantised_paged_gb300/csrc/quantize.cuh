@@ -11,12 +11,25 @@
 
 namespace nvfp4kv {
 
-// Round a float to 13 significant bits (half-way cases away from zero); exact
-// values with <= 13 bits are unchanged.
-__device__ __forceinline__ float snap13(float y) {
-    uint32_t b = __float_as_uint(y);
-    b = (b + 0x400u) & ~0x7ffu;
-    return __uint_as_float(b);
+// (hi, lo) floats -> f16x2, each rounded to nearest-even (11 significant
+// bits; beyond the FP16 range: infinity).
+__device__ __forceinline__ uint32_t f32x2_to_f16x2_rn(float hi, float lo) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Four f16x2 -> one word of eight E2M1 codes (element 2i in the low nibble of
+// byte i), each rounded to nearest-even and saturated (infinity -> 6).
+__device__ __forceinline__ uint32_t f16x2x4_to_e2m1x8(uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    uint32_t r;
+    asm("{ .reg .b8 p, q, s, t;\n"
+        "  cvt.rn.satfinite.e2m1x2.f16x2 p, %1; cvt.rn.satfinite.e2m1x2.f16x2 q, %2;\n"
+        "  cvt.rn.satfinite.e2m1x2.f16x2 s, %3; cvt.rn.satfinite.e2m1x2.f16x2 t, %4;\n"
+        "  mov.b32 %0, {p, q, s, t}; }"
+        : "=r"(r)
+        : "r"(a), "r"(b), "r"(c), "r"(d));
+    return r;
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -163,11 +176,14 @@ __device__ __forceinline__ void quantize_block16(const uint4 &a, const uint4 &b,
         }
     } else if (kUnitScale) {
         const float r = rcp_approx(sd);
+        uint32_t h[8];
 #pragma unroll
         for (int i = 0; i < 8; i++) {
             const float2 y = mul2(make_float2(bf16_lo(w[i]), bf16_hi(w[i])), r);
-            packed[i / 4] |= f32x2_to_e2m1x2(snap13(y.y), snap13(y.x)) << (8 * (i % 4));
+            h[i] = f32x2_to_f16x2_rn(y.y, y.x);
         }
+        packed[0] = f16x2x4_to_e2m1x8(h[0], h[1], h[2], h[3]);
+        packed[1] = f16x2x4_to_e2m1x8(h[4], h[5], h[6], h[7]);
     } else {
         const float xs = tiny ? kTinyRescale : 1.0f;
 #pragma unroll

@@ -20,14 +20,17 @@
 // For g = 1 the kernel forms q as amax * fl32(1/6): the FP32 results differ
 // from the quotient for some amax, but the E4M3 scale never does (all 32,640
 // finite non-negative BF16 values checked on the host).  It forms y_i as
-// x_i * rcp(scale) with the hardware's approximate reciprocal and then rounds
-// y_i to 13 significant bits.  x_i has at most 8 significant bits and the
-// scale at most 4, so every exact quotient that is not exactly an E2M1
-// rounding midpoint lies more than 2^-8 (relative) away from every midpoint,
-// far outside the ~2^-22 error of the reciprocal product; an exact midpoint
-// has at most 3 significant bits and the 13-bit rounding lands on it exactly.
-// Hence the codes equal those of the exactly rounded quotient (the GPU tests
-// check every BF16 value against every scale).  For g != 1 the codes are the
+// x_i * rcp(scale) with the hardware's approximate reciprocal, rounds y_i to
+// FP16 (11 significant bits) and converts that to E2M1.  x_i has at most 8
+// significant bits and the scale at most 4, so every exact quotient that is
+// not exactly an E2M1 rounding midpoint lies more than 2^-8 (relative) away
+// from every midpoint, far outside the ~2^-22 error of the reciprocal product
+// plus the 2^-11 of the FP16 rounding, which therefore neither crosses a
+// midpoint nor lands on one; an exact midpoint has at most 3 significant bits
+// and the FP16 rounding lands on it exactly (quotients beyond the FP16 range
+// become infinity, which saturates to 6 like the quotient itself).  Hence the
+// codes equal those of the exactly rounded quotient (the GPU tests check every
+// BF16 value against every scale).  For g != 1 the codes are the
 // exact roundings too (quantize.cuh: an FP32 estimate, then exact midpoint
 // checks by fused multiply-add).
 #include "common.cuh"
