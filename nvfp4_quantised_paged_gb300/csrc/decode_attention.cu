@@ -10,24 +10,30 @@
 // GB300 design (not the page's SM120 kernel):
 //   * Work split.  The KV of every (sequence, kv_head) pair is cut into
 //     64-token chunks; all chunks of all pairs form one flat range that is cut
-//     into `grid` equal contiguous pieces, one per CTA (grid = SM count x
-//     resident CTAs for an auto split), so every CTA streams the same number
-//     of bytes whatever the mix of sequence lengths.  The two warps of a CTA
-//     take alternate chunks of its range and each leaves one (max, sum, acc)
-//     partial per pair it touched; a separate log-sum-exp reduction kernel
-//     merges the partials of a pair and normalises.
-//   * Staging.  The CTA's warps share a ring of three chunk stages: the warp
-//     that used a stage refills it (lane 0, one 1-D bulk (TMA) copy of 9,216
-//     contiguous bytes for NVFP4 when pages hold >= 64 tokens, else one copy
-//     per page, completed on the stage's mbarrier) with the chunk three
+//     into `grid` equal contiguous pieces, one per warp pair (grid = SM count x
+//     resident warp pairs for an auto split), so every warp pair streams the
+//     same number of bytes whatever the mix of sequence lengths.  The two
+//     warps of a pair take alternate chunks of its range and each leaves one
+//     (max, sum, acc) partial per sequence-head pair it touched; a separate
+//     log-sum-exp reduction kernel merges the partials of a pair and
+//     normalises.
+//   * One CTA per SM holds all its warp pairs (eight for NVFP4 with up to 8
+//     heads per group, four otherwise; 16 warps of 128 registers).  Eight
+//     CTAs of one warp pair each did the same work with the same code 2%
+//     slower: the SM's warp schedulers favour the warps of the CTAs placed on
+//     it first, so those ranges finished first (in four tiers, ~80 us apart
+//     on the 32K workload) and the SM ran its last stretch with few warps.
+//   * Staging.  The warps of a pair share a ring of three chunk stages: the
+//     warp that used a stage refills it (lane 0, one 1-D bulk (TMA) copy of
+//     9,216 contiguous bytes for NVFP4 when pages hold >= 64 tokens, else one
+//     copy per page, completed on the stage's mbarrier) with the chunk three
 //     places ahead, which belongs to the other warp, and publishes the chunk
 //     index so that a warp never waits on a barrier phase that belongs to an
 //     earlier use of the stage.  The lanes resolve the sources of the next
-//     8-32 refills (one page each) well ahead of their copies.  Eight CTAs
-//     (16 warps, 128 registers each) per SM hold ~220 KB of ring; the data of
-//     a chunk has always landed when its warp gets to it.  Every wait is
-//     bounded and reports a timeout in the device error word instead of
-//     spinning forever.
+//     8-32 refills (one page each) well ahead of their copies.  The eight
+//     rings of an SM hold ~220 KB; the data of a chunk has always landed when
+//     its warp gets to it.  Every wait is bounded and reports a timeout in the
+//     device error word instead of spinning forever.
 //   * The four 16-token groups of a chunk are processed together, step by
 //     step, so their conversions and products interleave and the per-stage
 //     bookkeeping is paid once per 64 tokens.
@@ -95,17 +101,17 @@ constexpr int kPlanInCta = 96;
 // mbarriers, the mask of groups each stage holds, the index of the chunk last
 // issued into each stage, an abort flag and, for a batch planned in the CTA,
 // the chunk prefix (B + 1 entries).
-template <int DTYPE>
+template <int DTYPE, int NT>
 struct Smem {
+    static constexpr int kSubs = DTYPE == NVFP4KV_DTYPE_NVFP4 && NT == 1 ? 8 : 4;  // warp pairs per CTA
     static constexpr int kStage = kGroups * Group<DTYPE>::kBytes;
     static constexpr int kBars = kSlots * kStage;           // u64 full[kSlots]
     static constexpr int kFlags = kBars + kSlots * 8;       // int valid[kSlots]
     static constexpr int kSeq = kFlags + kSlots * 4;        // int seq[kSlots]
     static constexpr int kAbort = kSeq + kSlots * 4;        // int abort
-    static constexpr int kPrefix = (kAbort + 4 + 15) & ~15;  // u32 prefix[B + 1] (planned in the CTA)
-    static constexpr int kTotal = kAbort + 4;               // without the prefix
-    static constexpr int kMax = kPrefix + 4 * (kPlanInCta + 1);
-    static int bytes(int B, bool in_cta) { return in_cta ? kPrefix + 4 * (B + 1) : kTotal; }
+    static constexpr int kSub = (kAbort + 4 + 127) & ~127;  // one warp pair's region (offsets above within it)
+    static constexpr int kPrefixBytes = (4 * (kPlanInCta + 1) + 127) & ~127;  // u32 prefix[B + 1] at offset 0
+    static constexpr int kMax = kPrefixBytes + kSubs * kSub;
 };
 
 struct DecodeArgs {
@@ -156,7 +162,7 @@ template <int DTYPE>
 __device__ __forceinline__ int64_t chunk_prefix_at(const DecodeArgs &a, int i) {
     if (a.plan_in_cta) {
         extern __shared__ __align__(128) uint8_t smem[];
-        return reinterpret_cast<const uint32_t *>(smem + Smem<DTYPE>::kPrefix)[i];
+        return reinterpret_cast<const uint32_t *>(smem)[i];
     }
     return a.chunk_prefix[i];
 }
@@ -673,10 +679,15 @@ __device__ __forceinline__ void fused_append(const DecodeArgs &a, int64_t u0, in
 // refills it with unit i + kSlots.  Each warp keeps its own (max, sum, acc)
 // per pair and leaves its own partial.
 template <int DTYPE, int NT>
-__global__ void __launch_bounds__(kThreads, DTYPE == NVFP4KV_DTYPE_NVFP4 && NT == 1 ? 8 : 4) decode_kernel(DecodeArgs a) {
-    using S = Smem<DTYPE>;
-    extern __shared__ __align__(128) uint8_t smem[];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+__global__ void __launch_bounds__(kThreads * Smem<DTYPE, NT>::kSubs, 1) decode_kernel(DecodeArgs a) {
+    using S = Smem<DTYPE, NT>;
+    extern __shared__ __align__(128) uint8_t smem_all[];
+    // kSubs warp pairs per CTA, each with its own ring and its own range of
+    // units (as a CTA of two warps would have): sub-CTA sub of CTA blockIdx.x
+    // is unit range c = blockIdx.x * kSubs + sub of the split.
+    const int sub = threadIdx.x / kThreads;
+    const int tid = threadIdx.x % kThreads, lane = tid & 31, warp = tid >> 5;
+    uint8_t *smem = smem_all + S::kPrefixBytes + sub * S::kSub;
     // chunk_prefix comes from the plan kernel, or, for a batch planned in the
     // CTA, from this CTA's own scan of seq_lens below.  Behind the
     // shared-prefix kernel, this grid starts only once every CTA of that
@@ -691,16 +702,17 @@ __global__ void __launch_bounds__(kThreads, DTYPE == NVFP4KV_DTYPE_NVFP4 && NT =
     // complete: it reads chunk_prefix (or seq_lens) before its own wait.
     pdl_launch_dependents();
 
-    if (a.plan_in_cta) {  // exclusive scan of the chunk counts, B <= 2 * kThreads
-        uint32_t *sp = reinterpret_cast<uint32_t *>(smem + S::kPrefix);
-        uint32_t *wsum = reinterpret_cast<uint32_t *>(smem);  // scratch: no copy has been issued into the ring yet
+    if (a.plan_in_cta) {  // exclusive scan of the chunk counts, B <= 2 * kThreads (the first warp pair's threads)
+        uint32_t *sp = reinterpret_cast<uint32_t *>(smem_all);
+        uint32_t *wsum = reinterpret_cast<uint32_t *>(smem_all + S::kPrefixBytes);  // scratch: no copy issued yet
         const int64_t max_tokens = (int64_t)a.max_pages * a.P;
         const int b0 = 2 * tid, b1 = b0 + 1;
         uint32_t c0 = 0, c1 = 0;
         if (b0 < a.B) c0 = (uint32_t)seq_chunks(a.seq_lens[b0], max_tokens, 0);
         if (b1 < a.B) c1 = (uint32_t)seq_chunks(a.seq_lens[b1], max_tokens, 0);
-        if (blockIdx.x == 0 && ((b0 < a.B && (a.seq_lens[b0] < 0 || (int64_t)a.seq_lens[b0] > max_tokens)) ||
-                                (b1 < a.B && (a.seq_lens[b1] < 0 || (int64_t)a.seq_lens[b1] > max_tokens))))
+        if (sub == 0 && blockIdx.x == 0 &&
+            ((b0 < a.B && (a.seq_lens[b0] < 0 || (int64_t)a.seq_lens[b0] > max_tokens)) ||
+             (b1 < a.B && (a.seq_lens[b1] < 0 || (int64_t)a.seq_lens[b1] > max_tokens))))
             flag_error(a.err, kErrSeqLen);
         uint32_t incl = c0 + c1;
 #pragma unroll
@@ -708,23 +720,23 @@ __global__ void __launch_bounds__(kThreads, DTYPE == NVFP4KV_DTYPE_NVFP4 && NT =
             const uint32_t y = __shfl_up_sync(0xffffffffu, incl, x);
             if (lane >= x) incl += y;
         }
-        if (lane == 31) wsum[warp] = incl;
+        if (sub == 0 && lane == 31) wsum[warp] = incl;
         __syncthreads();
         if (warp > 0) incl += wsum[0];
         const uint32_t excl = incl - c0 - c1;
-        if (b0 < a.B) sp[b0] = excl;
-        if (b1 < a.B) sp[b1] = excl + c0;
-        if (tid == kThreads - 1) sp[a.B] = incl;
+        if (sub == 0) {
+            if (b0 < a.B) sp[b0] = excl;
+            if (b1 < a.B) sp[b1] = excl + c0;
+            if (tid == kThreads - 1) sp[a.B] = incl;
+        }
         __syncthreads();
     }
 
     const int64_t U = (int64_t)a.Hkv * chunk_prefix_at<DTYPE>(a, a.B);
-    const int64_t c = blockIdx.x;
-    const int64_t u0 = c * U / a.grid, u1 = (c + 1) * U / a.grid;
-    if (u0 >= u1) {
-        if (a.after_shared) pdl_wait();
-        return;
-    }
+    const int64_t c = (int64_t)blockIdx.x * S::kSubs + sub;
+    const int64_t u0 = c < a.grid ? c * U / a.grid : U, u1 = c < a.grid ? (c + 1) * U / a.grid : U;
+    // a warp pair with no units (possible when grid > U, or past the grid in
+    // the last CTA) skips to the end, where the CTA meets again
     const int nstages = (int)(u1 - u0);
 
     uint8_t *ring = smem;
@@ -742,7 +754,7 @@ __global__ void __launch_bounds__(kThreads, DTYPE == NVFP4KV_DTYPE_NVFP4 && NT =
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (a.k_new) {
+    if (a.k_new && nstages > 0) {
         fused_append<DTYPE>(a, u0, u1, tid);
         fence_proxy_async_global();  // the stores above before this CTA's bulk reads of the same rows
     }
@@ -786,11 +798,11 @@ __global__ void __launch_bounds__(kThreads, DTYPE == NVFP4KV_DTYPE_NVFP4 && NT =
 
     uint32_t qf[NT][8][2];
     float fac[NT][2], m_run[NT][2], o[NT][9][4];
-    int64_t acc_pair = -1;  // pair whose partial this warp is accumulating
+    int acc_pair = -1;  // pair (b * Hkv + kv, below 2^31) whose partial this warp is accumulating
     bool aborted = false;
 
     // this warp's partial of pair `pair`: (max, sum, acc)
-    auto write_partial = [&](int64_t pair) {
+    auto write_partial = [&](int pair) {
         const int g = lane >> 2, cq = lane & 3;
         const int64_t pidx = (c + pair) * kWarps + warp;
 #pragma unroll
@@ -819,7 +831,7 @@ __global__ void __launch_bounds__(kThreads, DTYPE == NVFP4KV_DTYPE_NVFP4 && NT =
             cur = nxt;
             nxt = part_src<DTYPE>(a, u0, nstages, refill_unit(k + upb + my_unit), my_part);
         }
-        const int64_t pair = (int64_t)cc.b * a.Hkv + cc.kv;
+        const int pair = cc.b * a.Hkv + cc.kv;
         if (pair != acc_pair) {  // this warp starts on a new (sequence, kv_head)
             if (acc_pair >= 0) write_partial(acc_pair);
             acc_pair = pair;
@@ -1134,15 +1146,27 @@ const void *kernel_fn() {
     return reinterpret_cast<const void *>(&decode_kernel<DTYPE, NT>);
 }
 
-// smem_bytes: the most the kernel is ever launched with (a batch planned in the CTA).
-const void *select_kernel(int dtype, int nt, int *smem_bytes) {
+// smem_bytes: the dynamic shared memory of every launch; subs: warp pairs per CTA.
+const void *select_kernel(int dtype, int nt, int *smem_bytes, int *subs = nullptr) {
+    int dummy = 0;
+    int &n = subs ? *subs : dummy;
     if (dtype == NVFP4KV_DTYPE_NVFP4) {
-        *smem_bytes = Smem<0>::kMax;
-        if (nt == 1) return kernel_fn<0, 1>();
+        if (nt == 1) {
+            *smem_bytes = Smem<0, 1>::kMax;
+            n = Smem<0, 1>::kSubs;
+            return kernel_fn<0, 1>();
+        }
+        *smem_bytes = Smem<0, 2>::kMax;
+        n = Smem<0, 2>::kSubs;
         return kernel_fn<0, 2>();
     }
-    *smem_bytes = Smem<1>::kMax;
-    if (nt == 1) return kernel_fn<1, 1>();
+    if (nt == 1) {
+        *smem_bytes = Smem<1, 1>::kMax;
+        n = Smem<1, 1>::kSubs;
+        return kernel_fn<1, 1>();
+    }
+    *smem_bytes = Smem<1, 2>::kMax;
+    n = Smem<1, 2>::kSubs;
     return kernel_fn<1, 2>();
 }
 
@@ -1157,8 +1181,8 @@ cudaError_t prepare_kernel(int dtype, int nt, int *grid_out) {
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(g_mu);
-    int smem = 0;
-    const void *fn = select_kernel(dtype, nt, &smem);
+    int smem = 0, subs = 1;
+    const void *fn = select_kernel(dtype, nt, &smem, &subs);
     if (!g_attr_set[dev][dtype][nt - 1]) {
         e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
@@ -1168,9 +1192,9 @@ cudaError_t prepare_kernel(int dtype, int nt, int *grid_out) {
         int sms = 0, per_sm = 0;
         e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThreads, smem);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThreads * subs, smem);
         if (e != cudaSuccess) return e;
-        g_auto_grid[dev][dtype][nt - 1] = sms * (per_sm > 0 ? per_sm : 1);
+        g_auto_grid[dev][dtype][nt - 1] = sms * (per_sm > 0 ? per_sm : 1) * subs;
     }
     if (grid_out) *grid_out = g_auto_grid[dev][dtype][nt - 1];
     return cudaSuccess;
@@ -1270,13 +1294,11 @@ cudaError_t launch_decode(const nvfp4kv_cache &c, const void *q, int batch, int 
     a.pool_w = static_cast<uint8_t *>(c.pool);
     a.skip = skip;
     a.after_shared = shared_pages ? 1 : 0;
-    int smem_max = 0;
-    const void *fn = select_kernel(c.dtype, nt, &smem_max);
-    const int smem = c.dtype == NVFP4KV_DTYPE_NVFP4 ? Smem<0>::bytes(batch, plan_in_cta)
-                                                    : Smem<1>::bytes(batch, plan_in_cta);
+    int smem = 0, subs = 1;
+    const void *fn = select_kernel(c.dtype, nt, &smem, &subs);
     void *args[] = {&a};
     if (before && (e = cudaEventRecord(before, stream)) != cudaSuccess) return e;
-    e = launch_pdl(fn, (unsigned)grid, kThreads, (size_t)smem, stream, args);
+    e = launch_pdl(fn, (unsigned)ceil_div64(grid, subs), kThreads * subs, (size_t)smem, stream, args);
     if (e != cudaSuccess) return e;
     if (after && (e = cudaEventRecord(after, stream)) != cudaSuccess) return e;
 
