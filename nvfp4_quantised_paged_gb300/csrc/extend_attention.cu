@@ -64,8 +64,16 @@ constexpr int kQRows = 128;                    // rows per query tile (one TMEM 
 constexpr int kCtaRows = kWGs * kQRows;
 constexpr int kSoftThreads = kWGs * kQRows;
 constexpr int kEThreads = kSoftThreads + 32;   // + the load / MMA warp
-constexpr int kDqThreads = 96;                 // paged prefix: three warps expanding NVFP4 tiles
+constexpr int kDqThreads = 224;                // paged prefix: seven warps expanding NVFP4 tiles
 constexpr int kEThreadsPaged = kEThreads + kDqThreads;
+// The paged instantiation is launched with 512 threads at 128 registers each;
+// the two softmax warpgroups then take 152 and the other two (the load / MMA
+// warp and the seven expanding warps) give back down to 104: 8 warps x 32 x
+// 152 + 8 warps x 32 x 104 = 65,536, exactly the registers the CTA holds.
+constexpr int kSoftRegs = 152, kOtherRegs = 104;
+static_assert(kEThreadsPaged == 512 && (kSoftThreads / 32) * kSoftRegs + (kEThreadsPaged - kSoftThreads) / 32 * kOtherRegs ==
+                                           (kEThreadsPaged / 32) * 128,
+              "register split of the paged instantiation must add up to its launch");
 constexpr int kKeys = 128;                     // keys per K/V tile
 constexpr int kQBytes = kQRows * 256;          // a query tile: 2 column blocks of [128][64] BF16
 constexpr int kKVBlock = kKeys * 128;          // one column block of a K or V tile (one TMA box)
@@ -291,360 +299,370 @@ __global__ void __launch_bounds__(kPaged ? kEThreadsPaged : kEThreads, 1)
     tc_fence_after();
     const uint32_t tmem = tmem_base;
 
-    if (warp == kSoftThreads / 32) {
-        // ---------------- load / MMA thread
-        if (lane == 0) {
-            constexpr uint32_t idesc_s = idesc_bf16_f32(128, kKeys, false);
-            constexpr uint32_t idesc_o = idesc_bf16_f32(128, kHeadDim, true);
-            auto mma_s = [&](int w, int s) {  // S_w = Q_w K(slot s)^T over head_dim, 16 at a time
-                const uint32_t sQ = sbase + kOffQ + w * kQBytes, sK = sbase + kOffK + s * kKVTile;
+    // The register split of the paged instantiation is taken per warpgroup at
+    // one instruction each (setmaxnreg is aligned over a warpgroup): the load /
+    // MMA warp and the expanding warps give registers back, the softmax
+    // warpgroups take them.
+    if (warp >= kSoftThreads / 32) {
+        if (kPaged) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kOtherRegs));
+        if (warp == kSoftThreads / 32) {
+            // ---------------- load / MMA thread
+            if (lane == 0) {
+                constexpr uint32_t idesc_s = idesc_bf16_f32(128, kKeys, false);
+                constexpr uint32_t idesc_o = idesc_bf16_f32(128, kHeadDim, true);
+                auto mma_s = [&](int w, int s) {  // S_w = Q_w K(slot s)^T over head_dim, 16 at a time
+                    const uint32_t sQ = sbase + kOffQ + w * kQBytes, sK = sbase + kOffK + s * kKVTile;
 #pragma unroll
-                for (int kk = 0; kk < 8; kk++) {
-                    const uint32_t blk = (uint32_t)(kk >> 2), sub = (uint32_t)(kk & 3) * 32;
-                    tc_mma_bf16(tmem + 128u * w, smem_desc_sw128(sQ + blk * (kQRows * 128) + sub, 16, 1024),
-                                smem_desc_sw128(sK + blk * kKVBlock + sub, 16, 1024), idesc_s, kk > 0);
-                }
-                tc_commit(&s_done[w]);
-            };
-            auto mma_pv = [&](int w, int j, int s) {  // O_w += P_w V(slot s) over the tile's 128 keys
-                const uint32_t sV = sbase + kOffV + s * kKVTile;
-#pragma unroll
-                for (int kk = 0; kk < 8; kk++)  // P from TMEM: 8 columns = 16 keys
-                    tc_mma_bf16_tmem_a(tmem + kColO + 128u * w, tmem + 128u * w + kk * 8,
-                                       smem_desc_sw128(sV + kk * 16 * 128, kKVBlock, 1024), idesc_o,
-                                       (j > 0 || kk > 0) ? 1u : 0u);
-                tc_commit(&pv_done[w]);
-            };
-            // Issue whatever is ready, for either query tile, so that the tensor core
-            // always holds the next product of one tile while the other's softmax runs:
-            //   S_w(t) once K(t) has landed and O_w += P_w(t - 1) V(t - 1) is complete;
-            //   O_w += P_w(t) V(t) once P_w(t) is stored and V(t) has landed;
-            //   K(t) into slot t % 2 once both S(t - 2) are done (their P V issued);
-            //   V(t) into slot t % 2 once both P(t - 2) V(t - 2) are complete.
-            // Each barrier is polled only where it cannot be two phases ahead.
-            // Phase of the barrier that completes tile t in slot t % 2: tile t is
-            // the (t / 2)-th of its slot; with a paged prefix, chunk tiles count
-            // from the first chunk tile (prefix tiles complete k_dq / v_dq instead).
-            auto kv_phase = [&](int t) { return (uint32_t)((((kPaged && t >= nt_pre) ? t - nt_pre : t) >> 1) & 1); };
-            int tw[kWGs] = {0, 0};                 // next tile of query tile w
-            bool at_pv[kWGs] = {false, false};     // its next product is P V (else S)
-            int pv_seen[kWGs] = {0, 0};            // its P V of tiles < pv_seen are known complete
-            int k_next = nt > 1 ? 2 : 1, v_next = k_next;  // next K / V tiles to request
-            bool ok = true;
-            uint32_t idle = 0;
-            for (;;) {
-                bool progress = false, finished = true;
-#pragma unroll
-                for (int w = 0; w < kWGs; w++) {
-                    const int t = tw[w];
-                    if (w >= nwg || t >= nt) continue;
-                    finished = false;
-                    if (!at_pv[w]) {
-                        if (t > 0 && pv_seen[w] < t) {
-                            if (!mbar_test_wait(&pv_done[w], (uint32_t)((t - 1) & 1))) continue;
-                            pv_seen[w] = t;
-                        }
-                        uint64_t *kb = kPaged && t < nt_pre ? &k_dq[t & 1] : &k_full[t & 1];
-                        if (!mbar_test_wait(kb, kv_phase(t))) continue;
-                        tc_fence_after();
-                        mma_s(w, t & 1);
-                        at_pv[w] = true;
-                    } else {
-                        if (!mbar_test_wait(&p_full[w], (uint32_t)(t & 1))) continue;
-                        uint64_t *vb = kPaged && t < nt_pre ? &v_dq[t & 1] : &v_full[t & 1];
-                        if (!mbar_test_wait(vb, kv_phase(t))) continue;
-                        tc_fence_after();
-                        mma_pv(w, t, t & 1);
-                        at_pv[w] = false;
-                        tw[w] = t + 1;
+                    for (int kk = 0; kk < 8; kk++) {
+                        const uint32_t blk = (uint32_t)(kk >> 2), sub = (uint32_t)(kk & 3) * 32;
+                        tc_mma_bf16(tmem + 128u * w, smem_desc_sw128(sQ + blk * (kQRows * 128) + sub, 16, 1024),
+                                    smem_desc_sw128(sK + blk * kKVBlock + sub, 16, 1024), idesc_s, kk > 0);
                     }
-                    progress = true;
+                    tc_commit(&s_done[w]);
+                };
+                auto mma_pv = [&](int w, int j, int s) {  // O_w += P_w V(slot s) over the tile's 128 keys
+                    const uint32_t sV = sbase + kOffV + s * kKVTile;
+#pragma unroll
+                    for (int kk = 0; kk < 8; kk++)  // P from TMEM: 8 columns = 16 keys
+                        tc_mma_bf16_tmem_a(tmem + kColO + 128u * w, tmem + 128u * w + kk * 8,
+                                           smem_desc_sw128(sV + kk * 16 * 128, kKVBlock, 1024), idesc_o,
+                                           (j > 0 || kk > 0) ? 1u : 0u);
+                    tc_commit(&pv_done[w]);
+                };
+                // Issue whatever is ready, for either query tile, so that the tensor core
+                // always holds the next product of one tile while the other's softmax runs:
+                //   S_w(t) once K(t) has landed and O_w += P_w(t - 1) V(t - 1) is complete;
+                //   O_w += P_w(t) V(t) once P_w(t) is stored and V(t) has landed;
+                //   K(t) into slot t % 2 once both S(t - 2) are done (their P V issued);
+                //   V(t) into slot t % 2 once both P(t - 2) V(t - 2) are complete.
+                // Each barrier is polled only where it cannot be two phases ahead.
+                // Phase of the barrier that completes tile t in slot t % 2: tile t is
+                // the (t / 2)-th of its slot; with a paged prefix, chunk tiles count
+                // from the first chunk tile (prefix tiles complete k_dq / v_dq instead).
+                auto kv_phase = [&](int t) { return (uint32_t)((((kPaged && t >= nt_pre) ? t - nt_pre : t) >> 1) & 1); };
+                int tw[kWGs] = {0, 0};                 // next tile of query tile w
+                bool at_pv[kWGs] = {false, false};     // its next product is P V (else S)
+                int pv_seen[kWGs] = {0, 0};            // its P V of tiles < pv_seen are known complete
+                int k_next = nt > 1 ? 2 : 1, v_next = k_next;  // next K / V tiles to request
+                bool ok = true;
+                uint32_t idle = 0;
+                for (;;) {
+                    bool progress = false, finished = true;
+#pragma unroll
+                    for (int w = 0; w < kWGs; w++) {
+                        const int t = tw[w];
+                        if (w >= nwg || t >= nt) continue;
+                        finished = false;
+                        if (!at_pv[w]) {
+                            if (t > 0 && pv_seen[w] < t) {
+                                if (!mbar_test_wait(&pv_done[w], (uint32_t)((t - 1) & 1))) continue;
+                                pv_seen[w] = t;
+                            }
+                            uint64_t *kb = kPaged && t < nt_pre ? &k_dq[t & 1] : &k_full[t & 1];
+                            if (!mbar_test_wait(kb, kv_phase(t))) continue;
+                            tc_fence_after();
+                            mma_s(w, t & 1);
+                            at_pv[w] = true;
+                        } else {
+                            if (!mbar_test_wait(&p_full[w], (uint32_t)(t & 1))) continue;
+                            uint64_t *vb = kPaged && t < nt_pre ? &v_dq[t & 1] : &v_full[t & 1];
+                            if (!mbar_test_wait(vb, kv_phase(t))) continue;
+                            tc_fence_after();
+                            mma_pv(w, t, t & 1);
+                            at_pv[w] = false;
+                            tw[w] = t + 1;
+                        }
+                        progress = true;
+                    }
+                    if (finished) break;
+                    int min_tw = tw[0], min_seen = pv_seen[0];
+                    if (nwg > 1) {
+                        min_tw = min(min_tw, tw[1]);
+                        min_seen = min(min_seen, pv_seen[1]);
+                    }
+                    if (k_next < nt && min_tw >= k_next - 1) {
+                        load_k(k_next, k_next & 1);
+                        k_next++;
+                        progress = true;
+                    }
+                    if (v_next < nt && min_seen >= v_next - 1) {
+                        load_v(v_next, v_next & 1);
+                        v_next++;
+                        progress = true;
+                    }
+                    if (progress) {  // polls without sleeping: a sleep here lands on the critical path
+                        idle = 0;
+                    } else if (++idle > kWaitLimitE || *abort_flag) {
+                        ok = false;
+                        break;
+                    }
                 }
-                if (finished) break;
-                int min_tw = tw[0], min_seen = pv_seen[0];
-                if (nwg > 1) {
-                    min_tw = min(min_tw, tw[1]);
-                    min_seen = min(min_seen, pv_seen[1]);
+                if (!ok) {
+                    *abort_flag = 1;
+                    flag_error(a.err, kErrTimeout);
+                    // no copy or MMA may still be running when the CTA frees its memory
+                    for (int t = max(kPaged ? nt_pre : 0, k_next - 2); t < k_next; t++)  // tensor copies only
+                        mbar_wait_bounded(&k_full[t & 1], kv_phase(t), kWaitLimitE, nullptr);
+                    for (int t = max(kPaged ? nt_pre : 0, v_next - 2); t < v_next; t++)
+                        mbar_wait_bounded(&v_full[t & 1], kv_phase(t), kWaitLimitE, nullptr);
+                    tc_commit(drain);
+                    mbar_wait_bounded(drain, 0, kWaitLimitE, nullptr);
                 }
-                if (k_next < nt && min_tw >= k_next - 1) {
-                    load_k(k_next, k_next & 1);
-                    k_next++;
-                    progress = true;
+            }
+            __syncwarp();
+        } else if (kPaged) {
+            // ---------------- paged prefix: expand tile j's K (then V) from the NVFP4
+            // pages into the BF16 operand layout of the slot, once it may be written
+            const int dt = tid - kEThreads;  // 0 .. kDqThreads - 1
+            const int32_t *bt = a.block_table + (int64_t)r * a.max_pages;
+            constexpr int kBlocks = kKeys * 8;  // 16-value blocks of one K (or V) tile
+            constexpr int kPer = (kBlocks + kDqThreads - 1) / kDqThreads;
+            // Tile j's eight 16-token groups are bulk-copied in halves (K codes and
+            // scales, V codes and scales: 1,152 B each) into raw stages by lanes 0..7
+            // of the first dequantising warp as soon as a stage is free: the K halves
+            // one tile ahead, the V halves two.  Groups past the prefix are not copied
+            // (those keys are written as zeros); a group of an invalid page is
+            // zero-filled and flagged.
+            auto issue_raw = [&](int j, int which, uint8_t *dst, uint64_t *bar) {  // the first dequantising warp
+                const int g = lane, tok = j * kKeys + 16 * g;
+                int32_t pg = -1;
+                if (g < 8 && tok < np) {
+                    pg = __ldg(bt + (tok >> a.log2P));
+                    if (pg < 0 || pg >= a.num_pages) {
+                        flag_error(a.err, kErrPage);
+                        uint4 *z = reinterpret_cast<uint4 *>(dst + g * kHalfGroup);
+                        for (int i = 0; i < kHalfGroup / 16; i++) z[i] = make_uint4(0u, 0u, 0u, 0u);
+                        pg = -1;
+                    }
                 }
-                if (v_next < nt && min_seen >= v_next - 1) {
-                    load_v(v_next, v_next & 1);
-                    v_next++;
-                    progress = true;
+                const unsigned copies = __popc(__ballot_sync(0xffffffffu, pg >= 0));
+                __syncwarp();
+                if (lane == 0) mbar_arrive_expect_tx(bar, copies * kHalfGroup);
+                __syncwarp();
+                if (pg >= 0)
+                    bulk_g2s(dst + g * kHalfGroup,
+                             a.pool + ((int64_t)pg * a.Hkv + kv) * a.slab + ((tok & (a.P - 1)) >> 4) * kGroupBytes +
+                                 which * kHalfGroup,
+                             kHalfGroup, bar);
+            };
+            uint8_t *rawk = smem + kOffRawK, *rawv = smem + kOffRawV;
+            const bool issuer = warp == kEThreads / 32;
+            // tiles whose halves were requested / seen landed (for the drain after an abort)
+            int k_req = 0, k_seen = 0, v_req = 0, v_seen = 0;
+            if (issuer) {
+                for (int j = 0; j < 2 && j < nt_pre; j++) issue_raw(j, 1, rawv + j * kRawHalf, &rawv_full[j]);
+                v_req = nt_pre < 2 ? nt_pre : 2;
+                if (nt_pre > 0) {
+                    issue_raw(0, 0, rawk, rawk_full);
+                    k_req = 1;
                 }
-                if (progress) {  // polls without sleeping: a sleep here lands on the critical path
-                    idle = 0;
-                } else if (++idle > kWaitLimitE || *abort_flag) {
-                    ok = false;
-                    break;
+            }
+            bool ok = true;
+            for (int j = 0; ok && j < nt_pre; j++) {
+                const int s = j & 1;
+                for (int which = 0; which < 2; which++) {
+                    uint64_t *landed = which ? &rawv_full[s] : rawk_full;
+                    const uint32_t lph = (uint32_t)((which ? j >> 1 : j) & 1);
+                    ok = __all_sync(0xffffffffu, spin_wait(landed, lph, abort_flag));
+                    if (!ok) break;
+                    if (which) v_seen = j + 1;
+                    else k_seen = j + 1;
+                    ok = __all_sync(0xffffffffu,
+                                    spin_wait(which ? &v_go[s] : &k_go[s], (uint32_t)((j >> 1) & 1), abort_flag));
+                    if (!ok) break;
+                    const uint8_t *src = which ? rawv + s * kRawHalf : rawk;
+                    uint8_t *tile = smem + (which ? kOffV : kOffK) + s * kKVTile;
+                    const float g = which ? a.gv : a.gk;
+                    auto expand = [&](auto unit) {  // unit: g = 1, chosen once per tile (the general form is long)
+#pragma unroll 1
+                        for (int i = 0; i < kPer; i++) {
+                            const int b = dt + i * kDqThreads;
+                            if (b >= kBlocks) continue;
+                            const int key = b >> 3, blk = b & 7, tok = j * kKeys + key;
+                            uint32_t o[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+                            if (tok < np) {
+                                const uint8_t *grp = src + (key >> 4) * kHalfGroup;  // codes [16][64] then scales
+                                const int rr = key & 15;
+                                const uint2 codes = *reinterpret_cast<const uint2 *>(grp + rr * 64 + blk * 8);
+                                const uint32_t sb = grp[1024 + (which ? blk * 16 + rr : rr * 8 + blk)];
+                                nvfp4_block_to_bf16<decltype(unit)::value>(codes, sb, g, o);
+                            }
+                            uint8_t *cb = tile + (blk >> 2) * kKVBlock;  // column block of head_dim 64 (blk / 4) ..
+                            *reinterpret_cast<uint4 *>(cb + sw128_off(key, (blk & 3) * 2)) =
+                                make_uint4(o[0], o[1], o[2], o[3]);
+                            *reinterpret_cast<uint4 *>(cb + sw128_off(key, (blk & 3) * 2 + 1)) =
+                                make_uint4(o[4], o[5], o[6], o[7]);
+                        }
+                    };
+                    if (g == 1.0f)
+                        expand(std::true_type{});
+                    else
+                        expand(std::false_type{});
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the tile for the tensor core
+                    mbar_arrive(which ? &v_dq[s] : &k_dq[s]);
+                    // the raw half is read: the tile after next (K) or the next (V) may land in it
+                    mbar_arrive(which ? &rawv_free[s] : rawk_free);
+                    const int jn = which ? j + 2 : j + 1;
+                    if (issuer && jn < nt_pre) {
+                        ok = __all_sync(0xffffffffu, spin_wait(which ? &rawv_free[s] : rawk_free, lph, abort_flag));
+                        if (!ok) break;
+                        if (which) {
+                            issue_raw(jn, 1, rawv + s * kRawHalf, &rawv_full[s]);
+                            v_req = jn + 1;
+                        } else {
+                            issue_raw(jn, 0, rawk, rawk_full);
+                            k_req = jn + 1;
+                        }
+                    }
                 }
+            }
+            if (issuer) {  // no copy may still be writing when the CTA frees its memory
+                for (int j = k_seen; j < k_req; j++) mbar_wait_bounded(rawk_full, (uint32_t)(j & 1), kWaitLimitE, nullptr);
+                for (int j = v_seen; j < v_req; j++)
+                    mbar_wait_bounded(&rawv_full[j & 1], (uint32_t)((j >> 1) & 1), kWaitLimitE, nullptr);
             }
             if (!ok) {
                 *abort_flag = 1;
-                flag_error(a.err, kErrTimeout);
-                // no copy or MMA may still be running when the CTA frees its memory
-                for (int t = max(kPaged ? nt_pre : 0, k_next - 2); t < k_next; t++)  // tensor copies only
-                    mbar_wait_bounded(&k_full[t & 1], kv_phase(t), kWaitLimitE, nullptr);
-                for (int t = max(kPaged ? nt_pre : 0, v_next - 2); t < v_next; t++)
-                    mbar_wait_bounded(&v_full[t & 1], kv_phase(t), kWaitLimitE, nullptr);
-                tc_commit(drain);
-                mbar_wait_bounded(drain, 0, kWaitLimitE, nullptr);
+                if (lane == 0) flag_error(a.err, kErrTimeout);
             }
         }
-        __syncwarp();
-    } else if (kPaged && warp > kSoftThreads / 32) {
-        // ---------------- paged prefix: expand tile j's K (then V) from the NVFP4
-        // pages into the BF16 operand layout of the slot, once it may be written
-        const int dt = tid - kEThreads;  // 0 .. kDqThreads - 1
-        const int32_t *bt = a.block_table + (int64_t)r * a.max_pages;
-        constexpr int kBlocks = kKeys * 8;  // 16-value blocks of one K (or V) tile
-        constexpr int kPer = (kBlocks + kDqThreads - 1) / kDqThreads;
-        // Tile j's eight 16-token groups are bulk-copied in halves (K codes and
-        // scales, V codes and scales: 1,152 B each) into raw stages by lanes 0..7
-        // of the first dequantising warp as soon as a stage is free: the K halves
-        // one tile ahead, the V halves two.  Groups past the prefix are not copied
-        // (those keys are written as zeros); a group of an invalid page is
-        // zero-filled and flagged.
-        auto issue_raw = [&](int j, int which, uint8_t *dst, uint64_t *bar) {  // the first dequantising warp
-            const int g = lane, tok = j * kKeys + 16 * g;
-            int32_t pg = -1;
-            if (g < 8 && tok < np) {
-                pg = __ldg(bt + (tok >> a.log2P));
-                if (pg < 0 || pg >= a.num_pages) {
-                    flag_error(a.err, kErrPage);
-                    uint4 *z = reinterpret_cast<uint4 *>(dst + g * kHalfGroup);
-                    for (int i = 0; i < kHalfGroup / 16; i++) z[i] = make_uint4(0u, 0u, 0u, 0u);
-                    pg = -1;
-                }
-            }
-            const unsigned copies = __popc(__ballot_sync(0xffffffffu, pg >= 0));
-            __syncwarp();
-            if (lane == 0) mbar_arrive_expect_tx(bar, copies * kHalfGroup);
-            __syncwarp();
-            if (pg >= 0)
-                bulk_g2s(dst + g * kHalfGroup,
-                         a.pool + ((int64_t)pg * a.Hkv + kv) * a.slab + ((tok & (a.P - 1)) >> 4) * kGroupBytes +
-                             which * kHalfGroup,
-                         kHalfGroup, bar);
-        };
-        uint8_t *rawk = smem + kOffRawK, *rawv = smem + kOffRawV;
-        const bool issuer = warp == kEThreads / 32;
-        // tiles whose halves were requested / seen landed (for the drain after an abort)
-        int k_req = 0, k_seen = 0, v_req = 0, v_seen = 0;
-        if (issuer) {
-            for (int j = 0; j < 2 && j < nt_pre; j++) issue_raw(j, 1, rawv + j * kRawHalf, &rawv_full[j]);
-            v_req = nt_pre < 2 ? nt_pre : 2;
-            if (nt_pre > 0) {
-                issue_raw(0, 0, rawk, rawk_full);
-                k_req = 1;
-            }
-        }
-        bool ok = true;
-        for (int j = 0; ok && j < nt_pre; j++) {
-            const int s = j & 1;
-            for (int which = 0; which < 2; which++) {
-                uint64_t *landed = which ? &rawv_full[s] : rawk_full;
-                const uint32_t lph = (uint32_t)((which ? j >> 1 : j) & 1);
-                ok = __all_sync(0xffffffffu, spin_wait(landed, lph, abort_flag));
+    } else {
+        if (kPaged) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftRegs));
+        if ((tid >> 7) < nwg) {
+            // ---------------- softmax of this thread's query row
+            const int w = tid >> 7;
+            const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;  // this warp's TMEM lanes
+            const uint32_t colS = 128u * w, colO = kColO + 128u * w;
+            const int R = row0 + w * kQRows + (tid & 127);
+            const bool row_ok = R < rows;
+            const int token = row_ok ? R / a.G : 0;
+            float m_run = kNegInfE, l_run = 0.f;
+            bool ok = true;
+            for (int j = 0; j < nt; j++) {
+                // S_w(j) done; its commit also covers O_w += P_w(j - 1) V(j - 1)
+                ok = __all_sync(0xffffffffu, mbar_wait_bounded(&s_done[w], (uint32_t)(j & 1), kWaitLimitE, abort_flag));
                 if (!ok) break;
-                if (which) v_seen = j + 1;
-                else k_seen = j + 1;
-                ok = __all_sync(0xffffffffu,
-                                spin_wait(which ? &v_go[s] : &k_go[s], (uint32_t)((j >> 1) & 1), abort_flag));
-                if (!ok) break;
-                const uint8_t *src = which ? rawv + s * kRawHalf : rawk;
-                uint8_t *tile = smem + (which ? kOffV : kOffK) + s * kKVTile;
-                const float g = which ? a.gv : a.gk;
-                auto expand = [&](auto unit) {  // unit: g = 1, chosen once per tile (the general form is long)
+                tc_fence_after();
+                const bool pre = j < nt_pre;
+                const int base = pre ? j * kKeys : (j - nt_pre) * kKeys;
+                const int visible = (pre ? np : token + 1) - base;   // keys [0, visible) of the tile are seen
+                const bool edge = __any_sync(0xffffffffu, visible < kKeys);  // mask on edge tiles only
+                // the row's 64 scores of half h (masked scores are -inf)
+                auto load_half = [&](int h, float (&sc)[64]) {
+                    uint32_t sr[2][32];
+                    tc_ld32(tmem + lane_base + colS + 64 * h, sr[0]);
+                    tc_ld32(tmem + lane_base + colS + 64 * h + 32, sr[1]);
+                    tc_wait_ld();
 #pragma unroll
-                    for (int i = 0; i < kPer; i++) {
-                        const int b = dt + i * kDqThreads;
-                        if (b >= kBlocks) continue;
-                        const int key = b >> 3, blk = b & 7, tok = j * kKeys + key;
-                        uint32_t o[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
-                        if (tok < np) {
-                            const uint8_t *grp = src + (key >> 4) * kHalfGroup;  // codes [16][64] then scales
-                            const int rr = key & 15;
-                            const uint2 codes = *reinterpret_cast<const uint2 *>(grp + rr * 64 + blk * 8);
-                            const uint32_t sb = grp[1024 + (which ? blk * 16 + rr : rr * 8 + blk)];
-                            nvfp4_block_to_bf16<decltype(unit)::value>(codes, sb, g, o);
-                        }
-                        uint8_t *cb = tile + (blk >> 2) * kKVBlock;  // column block of head_dim 64 (blk / 4) ..
-                        *reinterpret_cast<uint4 *>(cb + sw128_off(key, (blk & 3) * 2)) =
-                            make_uint4(o[0], o[1], o[2], o[3]);
-                        *reinterpret_cast<uint4 *>(cb + sw128_off(key, (blk & 3) * 2 + 1)) =
-                            make_uint4(o[4], o[5], o[6], o[7]);
+                    for (int c = 0; c < 64; c++) sc[c] = __uint_as_float(sr[c >> 5][c & 31]);
+                    if (edge) {
+#pragma unroll
+                        for (int c = 0; c < 64; c++)
+                            if (64 * h + c >= visible) sc[c] = kNegInfE;
                     }
                 };
-                if (g == 1.0f)
-                    expand(std::true_type{});
-                else
-                    expand(std::false_type{});
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the tile for the tensor core
-                mbar_arrive(which ? &v_dq[s] : &k_dq[s]);
-                // the raw half is read: the tile after next (K) or the next (V) may land in it
-                mbar_arrive(which ? &rawv_free[s] : rawk_free);
-                const int jn = which ? j + 2 : j + 1;
-                if (issuer && jn < nt_pre) {
-                    ok = __all_sync(0xffffffffu, spin_wait(which ? &rawv_free[s] : rawk_free, lph, abort_flag));
-                    if (!ok) break;
-                    if (which) {
-                        issue_raw(jn, 1, rawv + s * kRawHalf, &rawv_full[s]);
-                        v_req = jn + 1;
-                    } else {
-                        issue_raw(jn, 0, rawk, rawk_full);
-                        k_req = jn + 1;
+                // P = 2^(s * scale - m) of one half, rounded to BF16 pairs; ls += the rounded values
+                auto make_p = [&](const float (&sc)[64], float neg_m, uint32_t (&pw)[32], float (&ls)[4]) {
+#pragma unroll
+                    for (int c = 0; c < 32; c++) {
+                        const float2 e = fma2(make_float2(sc[2 * c], sc[2 * c + 1]), a.score_log2, neg_m);
+                        const __nv_bfloat162 pr = __floats2bfloat162_rn(ex2(e.x), ex2(e.y));
+                        pw[c] = *reinterpret_cast<const uint32_t *>(&pr);
+                        add_bf16x2(ls[2 * (c & 1)], ls[2 * (c & 1) + 1], pw[c]);
                     }
-                }
-            }
-        }
-        if (issuer) {  // no copy may still be writing when the CTA frees its memory
-            for (int j = k_seen; j < k_req; j++) mbar_wait_bounded(rawk_full, (uint32_t)(j & 1), kWaitLimitE, nullptr);
-            for (int j = v_seen; j < v_req; j++)
-                mbar_wait_bounded(&rawv_full[j & 1], (uint32_t)((j >> 1) & 1), kWaitLimitE, nullptr);
-        }
-        if (!ok) {
-            *abort_flag = 1;
-            if (lane == 0) flag_error(a.err, kErrTimeout);
-        }
-    } else if ((tid >> 7) < nwg) {
-        // ---------------- softmax of this thread's query row
-        const int w = tid >> 7;
-        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;  // this warp's TMEM lanes
-        const uint32_t colS = 128u * w, colO = kColO + 128u * w;
-        const int R = row0 + w * kQRows + (tid & 127);
-        const bool row_ok = R < rows;
-        const int token = row_ok ? R / a.G : 0;
-        float m_run = kNegInfE, l_run = 0.f;
-        bool ok = true;
-        for (int j = 0; j < nt; j++) {
-            // S_w(j) done; its commit also covers O_w += P_w(j - 1) V(j - 1)
-            ok = __all_sync(0xffffffffu, mbar_wait_bounded(&s_done[w], (uint32_t)(j & 1), kWaitLimitE, abort_flag));
-            if (!ok) break;
-            tc_fence_after();
-            const bool pre = j < nt_pre;
-            const int base = pre ? j * kKeys : (j - nt_pre) * kKeys;
-            const int visible = (pre ? np : token + 1) - base;   // keys [0, visible) of the tile are seen
-            const bool edge = __any_sync(0xffffffffu, visible < kKeys);  // mask on edge tiles only
-            // the row's 64 scores of half h (masked scores are -inf)
-            auto load_half = [&](int h, float (&sc)[64]) {
-                uint32_t sr[2][32];
-                tc_ld32(tmem + lane_base + colS + 64 * h, sr[0]);
-                tc_ld32(tmem + lane_base + colS + 64 * h + 32, sr[1]);
-                tc_wait_ld();
+                };
+                auto half_max = [&](const float (&sc)[64]) {
+                    float m8[8];
 #pragma unroll
-                for (int c = 0; c < 64; c++) sc[c] = __uint_as_float(sr[c >> 5][c & 31]);
-                if (edge) {
+                    for (int e = 0; e < 8; e++) m8[e] = max3(sc[e], sc[8 + e], sc[16 + e]);
 #pragma unroll
-                    for (int c = 0; c < 64; c++)
-                        if (64 * h + c >= visible) sc[c] = kNegInfE;
-                }
-            };
-            // P = 2^(s * scale - m) of one half, rounded to BF16 pairs; ls += the rounded values
-            auto make_p = [&](const float (&sc)[64], float neg_m, uint32_t (&pw)[32], float (&ls)[4]) {
+                    for (int e = 0; e < 8; e++) m8[e] = max3(m8[e], sc[24 + e], sc[32 + e]);
 #pragma unroll
-                for (int c = 0; c < 32; c++) {
-                    const float2 e = fma2(make_float2(sc[2 * c], sc[2 * c + 1]), a.score_log2, neg_m);
-                    const __nv_bfloat162 pr = __floats2bfloat162_rn(ex2(e.x), ex2(e.y));
-                    pw[c] = *reinterpret_cast<const uint32_t *>(&pr);
-                    add_bf16x2(ls[2 * (c & 1)], ls[2 * (c & 1) + 1], pw[c]);
-                }
-            };
-            auto half_max = [&](const float (&sc)[64]) {
-                float m8[8];
+                    for (int e = 0; e < 8; e++) m8[e] = max3(m8[e], sc[40 + e], sc[48 + e]);
 #pragma unroll
-                for (int e = 0; e < 8; e++) m8[e] = max3(sc[e], sc[8 + e], sc[16 + e]);
-#pragma unroll
-                for (int e = 0; e < 8; e++) m8[e] = max3(m8[e], sc[24 + e], sc[32 + e]);
-#pragma unroll
-                for (int e = 0; e < 8; e++) m8[e] = max3(m8[e], sc[40 + e], sc[48 + e]);
-#pragma unroll
-                for (int e = 0; e < 8; e++) m8[e] = fmaxf(m8[e], sc[56 + e]);
-                return max3(max3(m8[0], m8[1], m8[2]), max3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
-            };
-            // One pass with the running max as it stands (the lazy rescale lets it
-            // lag the true max by up to 2^8): P of half 0 stays in registers until
-            // half 1 shows whether the max must move; only then does it go over the
-            // scores in TMEM.  If it must (the first tile, rarely later), O and the
-            // row sum are rescaled and P is formed again from the scores in TMEM.
-            uint32_t pw0[32], pw1[32];
-            float ls[4] = {0.f, 0.f, 0.f, 0.f};
-            float smax;
-            {
-                float sc[64];
-                load_half(0, sc);
-                smax = half_max(sc);
-                make_p(sc, -m_run, pw0, ls);
-                load_half(1, sc);
-                smax = fmaxf(smax, half_max(sc));
-                const float mx = smax * a.score_log2;  // the scale is positive
-                const bool need = mx > m_run + kRescale;
-                if (!__any_sync(0xffffffffu, need)) {
-                    make_p(sc, -m_run, pw1, ls);
-                } else {
-                    const float m_new = need ? fmaxf(m_run, mx) : m_run;
-                    const float alpha = need ? (m_run == kNegInfE ? 0.f : ex2(m_run - m_new)) : 1.f;
-                    if (j > 0) {  // O_w holds tiles 0 .. j - 1 (complete): rescale this warp's rows
-#pragma unroll
-                        for (int cblk = 0; cblk < 4; cblk++) {
-                            uint32_t ov[32];
-                            tc_ld32(tmem + lane_base + colO + 32 * cblk, ov);
-                            tc_wait_ld();
-#pragma unroll
-                            for (int e = 0; e < 32; e++) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-                            tc_st32(tmem + lane_base + colO + 32 * cblk, ov);
-                        }
-                        tc_wait_st();
-                    }
-                    l_run *= alpha;
-                    m_run = m_new;
-                    ls[0] = ls[1] = ls[2] = ls[3] = 0.f;
-                    make_p(sc, -m_run, pw1, ls);
+                    for (int e = 0; e < 8; e++) m8[e] = fmaxf(m8[e], sc[56 + e]);
+                    return max3(max3(m8[0], m8[1], m8[2]), max3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
+                };
+                // One pass with the running max as it stands (the lazy rescale lets it
+                // lag the true max by up to 2^8): P of half 0 stays in registers until
+                // half 1 shows whether the max must move; only then does it go over the
+                // scores in TMEM.  If it must (the first tile, rarely later), O and the
+                // row sum are rescaled and P is formed again from the scores in TMEM.
+                uint32_t pw0[32], pw1[32];
+                float ls[4] = {0.f, 0.f, 0.f, 0.f};
+                float smax;
+                {
+                    float sc[64];
                     load_half(0, sc);
+                    smax = half_max(sc);
                     make_p(sc, -m_run, pw0, ls);
-                }
-            }
-            l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-            tc_st32(tmem + lane_base + colS, pw0);       // over scores 0 .. 31 (read already)
-            tc_st32(tmem + lane_base + colS + 32, pw1);  // over scores 32 .. 63
-            tc_wait_st();
-            tc_fence_before();
-            mbar_arrive(&p_full[w]);
-        }
-        // O_w is complete after O_w += P_w(nt - 1) V(nt - 1); the previous one is
-        // done already (S_w(nt - 1) waited for it), so one parity wait suffices
-        if (ok)
-            ok = __all_sync(0xffffffffu,
-                            mbar_wait_bounded(&pv_done[w], (uint32_t)((nt - 1) & 1), kWaitLimitE, abort_flag));
-        if (!ok) {
-            *abort_flag = 1;
-            if (lane == 0) flag_error(a.err, kErrTimeout);
-        } else {
-            // ---- O / l -> BF16 row of the output
-            tc_fence_after();
-            const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-            uint4 *dst =
-                reinterpret_cast<uint4 *>(a.out + (((int64_t)q0 + token) * a.Hq + kv * a.G + R % a.G) * kHeadDim);
+                    load_half(1, sc);
+                    smax = fmaxf(smax, half_max(sc));
+                    const float mx = smax * a.score_log2;  // the scale is positive
+                    const bool need = mx > m_run + kRescale;
+                    if (!__any_sync(0xffffffffu, need)) {
+                        make_p(sc, -m_run, pw1, ls);
+                    } else {
+                        const float m_new = need ? fmaxf(m_run, mx) : m_run;
+                        const float alpha = need ? (m_run == kNegInfE ? 0.f : ex2(m_run - m_new)) : 1.f;
+                        if (j > 0) {  // O_w holds tiles 0 .. j - 1 (complete): rescale this warp's rows
 #pragma unroll
-            for (int cblk = 0; cblk < 4; cblk++) {
-                uint32_t ov[32];
-                tc_ld32(tmem + lane_base + colO + 32 * cblk, ov);
-                tc_wait_ld();
-                if (row_ok) {
+                            for (int cblk = 0; cblk < 4; cblk++) {
+                                uint32_t ov[32];
+                                tc_ld32(tmem + lane_base + colO + 32 * cblk, ov);
+                                tc_wait_ld();
 #pragma unroll
-                    for (int q4 = 0; q4 < 4; q4++) {
-                        uint32_t wv[4];
-#pragma unroll
-                        for (int e = 0; e < 4; e++) {
-                            const __nv_bfloat162 hv = __floats2bfloat162_rn(
-                                __uint_as_float(ov[8 * q4 + 2 * e]) * inv, __uint_as_float(ov[8 * q4 + 2 * e + 1]) * inv);
-                            wv[e] = *reinterpret_cast<const uint32_t *>(&hv);
+                                for (int e = 0; e < 32; e++) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+                                tc_st32(tmem + lane_base + colO + 32 * cblk, ov);
+                            }
+                            tc_wait_st();
                         }
-                        dst[4 * cblk + q4] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+                        l_run *= alpha;
+                        m_run = m_new;
+                        ls[0] = ls[1] = ls[2] = ls[3] = 0.f;
+                        make_p(sc, -m_run, pw1, ls);
+                        load_half(0, sc);
+                        make_p(sc, -m_run, pw0, ls);
+                    }
+                }
+                l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+                tc_st32(tmem + lane_base + colS, pw0);       // over scores 0 .. 31 (read already)
+                tc_st32(tmem + lane_base + colS + 32, pw1);  // over scores 32 .. 63
+                tc_wait_st();
+                tc_fence_before();
+                mbar_arrive(&p_full[w]);
+            }
+            // O_w is complete after O_w += P_w(nt - 1) V(nt - 1); the previous one is
+            // done already (S_w(nt - 1) waited for it), so one parity wait suffices
+            if (ok)
+                ok = __all_sync(0xffffffffu,
+                                mbar_wait_bounded(&pv_done[w], (uint32_t)((nt - 1) & 1), kWaitLimitE, abort_flag));
+            if (!ok) {
+                *abort_flag = 1;
+                if (lane == 0) flag_error(a.err, kErrTimeout);
+            } else {
+                // ---- O / l -> BF16 row of the output
+                tc_fence_after();
+                const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+                uint4 *dst =
+                    reinterpret_cast<uint4 *>(a.out + (((int64_t)q0 + token) * a.Hq + kv * a.G + R % a.G) * kHeadDim);
+#pragma unroll
+                for (int cblk = 0; cblk < 4; cblk++) {
+                    uint32_t ov[32];
+                    tc_ld32(tmem + lane_base + colO + 32 * cblk, ov);
+                    tc_wait_ld();
+                    if (row_ok) {
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; q4++) {
+                            uint32_t wv[4];
+#pragma unroll
+                            for (int e = 0; e < 4; e++) {
+                                const __nv_bfloat162 hv = __floats2bfloat162_rn(
+                                    __uint_as_float(ov[8 * q4 + 2 * e]) * inv, __uint_as_float(ov[8 * q4 + 2 * e + 1]) * inv);
+                                wv[e] = *reinterpret_cast<const uint32_t *>(&hv);
+                            }
+                            dst[4 * cblk + q4] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+                        }
                     }
                 }
             }
