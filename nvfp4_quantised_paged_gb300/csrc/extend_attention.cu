@@ -41,7 +41,7 @@
 //
 // Two instantiations: the prefix as BF16 workspace rows loaded by TMA
 // (extend_kernel<false>), or read from the NVFP4 pages of the cache
-// (extend_kernel<true>): three more warps then bulk-copy each prefix tile's
+// (extend_kernel<true>): seven more warps then bulk-copy each prefix tile's
 // NVFP4 groups into raw shared-memory stages and expand them into the K / V
 // slots in BF16 (as the prefix dequant kernel would), so the result is the
 // same bit for bit and no workspace is written.  Every wait is bounded; a
