@@ -670,7 +670,7 @@ __device__ __noinline__ void fused_append(const DecodeArgs &a, int64_t u0, int64
         const uint4 *src = (which ? a.v_new : a.k_new) + (int64_t)b * a.new_stride16 + kv * (kHeadDim / 8) + blk * 2;
         uint8_t *slab = a.pool_w + ((int64_t)pg * a.Hkv + kv) * a.slab;
         if (a.unit_scale)
-            store_block<true, true>(slab, a.dtype, t & (a.P - 1), which, blk, src, 1.0f);
+            store_block<true>(slab, a.dtype, t & (a.P - 1), which, blk, src, 1.0f);
         else
             store_block<false>(slab, a.dtype, t & (a.P - 1), which, blk, src, which ? a.gv_q : a.gk_q);
     }

@@ -11,14 +11,6 @@
 
 namespace nvfp4kv {
 
-// Round a float to 13 significant bits (half-way cases away from zero); exact
-// values with <= 13 bits are unchanged.
-__device__ __forceinline__ float snap13(float y) {
-    uint32_t b = __float_as_uint(y);
-    b = (b + 0x400u) & ~0x7ffu;
-    return __uint_as_float(b);
-}
-
 // (hi, lo) floats -> f16x2, each rounded to nearest-even (11 significant
 // bits; beyond the FP16 range: infinity).
 __device__ __forceinline__ uint32_t f32x2_to_f16x2_rn(float hi, float lo) {
@@ -156,15 +148,7 @@ __device__ __forceinline__ uint32_t bf16_of_product(float p, float g) {
     return (uint32_t)f | sign;
 }
 
-// kSnap13 (unit scale only): the quotients x * rcp(scale) are rounded to 13
-// significant bits by integer operations and converted from FP32 instead of
-// being rounded to FP16 and converted from that; both land exactly on every
-// E2M1 midpoint and cross none (the quotient of a BF16 value by an E4M3 scale
-// is a midpoint or more than 2^-8 away from all of them), so the codes are the
-// same.  The decode kernel's fused append uses it: that kernel runs at its
-// register cap, and with this form its allocation keeps the main loop free of
-// local-memory reloads.
-template <bool kUnitScale, bool kSnap13 = false>
+template <bool kUnitScale>
 __device__ __forceinline__ void quantize_block16(const uint4 &a, const uint4 &b, float g, uint2 &codes,
                                                  uint32_t &scale_byte) {
     const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
@@ -189,13 +173,6 @@ __device__ __forceinline__ void quantize_block16(const uint4 &a, const uint4 &b,
             const uint32_t lo_neg = (w[i] >> 15) & 1u, hi_neg = w[i] >> 31;
             const uint32_t byte = (lo_neg << 3) | (hi_neg << 7);
             packed[i / 4] |= byte << (8 * (i % 4));
-        }
-    } else if (kUnitScale && kSnap13) {
-        const float r = rcp_approx(sd);
-#pragma unroll
-        for (int i = 0; i < 8; i++) {
-            const float2 y = mul2(make_float2(bf16_lo(w[i]), bf16_hi(w[i])), r);
-            packed[i / 4] |= f32x2_to_e2m1x2(snap13(y.y), snap13(y.x)) << (8 * (i % 4));
         }
     } else if (kUnitScale) {
         const float r = rcp_approx(sd);
@@ -256,13 +233,13 @@ __device__ __forceinline__ void nvfp4_block_to_bf16(uint2 codes, uint32_t sbyte,
 // of the (page, h) slab.  NVFP4 slabs are 16-token groups of 2304 bytes
 // (K codes | K scales | V codes | V scales [8][16]); FP8 slabs are groups of
 // 4096 bytes (K codes [16][128] | V codes [16][128]).
-template <bool kUnitScale, bool kSnap13 = false>
+template <bool kUnitScale>
 __device__ __forceinline__ void store_block_values(uint8_t *slab_base, int dtype, int r, int which, int blk,
                                                    const uint4 &x0, const uint4 &x1, float g) {
     if (dtype == NVFP4KV_DTYPE_NVFP4) {
         uint2 codes;
         uint32_t sbyte;
-        quantize_block16<kUnitScale, kSnap13>(x0, x1, g, codes, sbyte);
+        quantize_block16<kUnitScale>(x0, x1, g, codes, sbyte);
         uint8_t *grp = slab_base + (r >> 4) * 2304;
         const int rr = r & 15;
         *reinterpret_cast<uint2 *>(grp + (which ? 1152 : 0) + rr * 64 + blk * 8) = codes;
@@ -294,11 +271,11 @@ __device__ __forceinline__ void store_block_values(uint8_t *slab_base, int dtype
 }
 
 // The same, loading the 16 values from src[0..1] first.
-template <bool kUnitScale, bool kSnap13 = false>
+template <bool kUnitScale>
 __device__ __forceinline__ void store_block(uint8_t *slab_base, int dtype, int r, int which, int blk,
                                             const uint4 *src, float g) {
     const uint4 x0 = __ldg(src), x1 = __ldg(src + 1);
-    store_block_values<kUnitScale, kSnap13>(slab_base, dtype, r, which, blk, x0, x1, g);
+    store_block_values<kUnitScale>(slab_base, dtype, r, which, blk, x0, x1, g);
 }
 
 }  // namespace nvfp4kv
