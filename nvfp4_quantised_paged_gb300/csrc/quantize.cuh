@@ -228,14 +228,28 @@ __device__ __forceinline__ void nvfp4_block_to_bf16(uint2 codes, uint32_t sbyte,
     for (int i = 0; i < 8; i++) o[i] = f16x2_to_bf16x2_scaled<kUnit>(hmul2(f[i], s2), g);
 }
 
+// L2 policy "evict last" (all of a request's lines), for st_u8_policy.
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ void st_u8_policy(uint8_t *p, uint32_t v, uint64_t policy) {
+    asm volatile("st.global.L2::cache_hint.u8 [%0], %1, %2;" ::"l"(p), "h"((unsigned short)v), "l"(policy) : "memory");
+}
+
 // Quantise block `blk` (0..7) of K (which = 0) or V (which = 1) of one
 // head_dim row -- the 16 BF16 values at src[0..1] -- and store it at row `r`
 // of the (page, h) slab.  NVFP4 slabs are 16-token groups of 2304 bytes
 // (K codes | K scales | V codes | V scales [8][16]); FP8 slabs are groups of
-// 4096 bytes (K codes [16][128] | V codes [16][128]).
-template <bool kUnitScale>
+// 4096 bytes (K codes [16][128] | V codes [16][128]).  kScalePolicy: the scale
+// byte is stored with the L2 policy `policy` (a 32-byte sector of scales holds
+// bytes of four (K) or sixteen (V) tokens, so a token alone writes it partly).
+template <bool kUnitScale, bool kScalePolicy = false>
 __device__ __forceinline__ void store_block_values(uint8_t *slab_base, int dtype, int r, int which, int blk,
-                                                   const uint4 &x0, const uint4 &x1, float g) {
+                                                   const uint4 &x0, const uint4 &x1, float g,
+                                                   uint64_t policy = 0) {
     if (dtype == NVFP4KV_DTYPE_NVFP4) {
         uint2 codes;
         uint32_t sbyte;
@@ -243,7 +257,11 @@ __device__ __forceinline__ void store_block_values(uint8_t *slab_base, int dtype
         uint8_t *grp = slab_base + (r >> 4) * 2304;
         const int rr = r & 15;
         *reinterpret_cast<uint2 *>(grp + (which ? 1152 : 0) + rr * 64 + blk * 8) = codes;
-        grp[which ? 2176 + blk * 16 + rr : 1024 + rr * 8 + blk] = (uint8_t)sbyte;
+        uint8_t *sdst = grp + (which ? 2176 + blk * 16 + rr : 1024 + rr * 8 + blk);
+        if (kScalePolicy)
+            st_u8_policy(sdst, sbyte, policy);
+        else
+            *sdst = (uint8_t)sbyte;
     } else {
         const uint32_t w[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
         uint32_t out[4];

@@ -73,6 +73,12 @@ __global__ void __launch_bounds__(256) append_kernel(AppendArgs a) {
     const uint32_t items = (uint32_t)(a.num_tokens * a.Hkv * 16);
     const uint32_t n = gridDim.x * blockDim.x;
     const uint32_t id0 = blockIdx.x * blockDim.x + threadIdx.x;
+    // Scale bytes are stored "evict last" in L2: with scattered slots the other
+    // tokens of a scale sector arrive at random times in the call, and a sector
+    // evicted partly written costs a read of the rest from DRAM.  On 65,536
+    // tokens x 8 heads into random slots of a 2,048-page pool, 66 -> 61.5 us
+    // (57.5 against 55.6 us with page-ordered slots).
+    const uint64_t scale_policy = l2_policy_evict_last();
     uint4 x0[kBlocksPerThread], x1[kBlocksPerThread];
     int64_t slot[kBlocksPerThread];
 #pragma unroll
@@ -104,8 +110,9 @@ __global__ void __launch_bounds__(256) append_kernel(AppendArgs a) {
             continue;
         }
         const int64_t page = slot[j] >> a.log2P;
-        store_block_values<kUnitScale>(a.pool + (page * a.Hkv + h) * a.slab, a.dtype, (int)(slot[j] & (a.P - 1)),
-                                       which, blk, x0[j], x1[j], which ? a.gv : a.gk);
+        store_block_values<kUnitScale, true>(a.pool + (page * a.Hkv + h) * a.slab, a.dtype,
+                                             (int)(slot[j] & (a.P - 1)), which, blk, x0[j], x1[j],
+                                             which ? a.gv : a.gk, scale_policy);
     }
 }
 
