@@ -36,6 +36,12 @@
  *     is skipped (never dereferenced) and recorded in a per-device error word
  *     that nvfp4kv_check_device_errors() reports.  No kernel traps or asserts.
  *   - head_dim is 128.  page_size P is 16, 32, 64 or 128 tokens.
+ *   - Per device, the library keeps the device addresses of its own
+ *     __device__ variables (the error word, the no-alloc scratch array) and
+ *     kernel attributes it has set, from the first call on that device.  They
+ *     belong to the device's primary context: after cudaDeviceReset (or any
+ *     teardown of the primary context) the library must not be called again
+ *     in that process.
  *
  * Pool layout, one slab per (page, kv_head), slabs ordered page-major:
  *   pool = uint8[num_pages][num_kv_heads][slab_bytes]
