@@ -9,10 +9,12 @@ units run in parallel threads).
     in the same launch (the 64 new rows bit-exact too);
   * 1M long-context decode (batch 2 x 1,048,576, 40 q / 8 kv, channel factors),
     automatic split;
+  * the 32K workload over the FP8-E4M3 comparison cache, automatic split;
   * agent mix: the 128 decode sequences (3.2K-160K tokens sharing a 3,200-token
     prefix) through plain and cascade decode; the 8 extend requests' prefix
     dequant bit-exact, their extend attention on all 8 x 512 chunk rows over the
-    oracle's own workspace, and the chunks' appends bit-exact;
+    oracle's own workspace, the paged-prefix extend bit-identical to it, and the
+    chunks' appends bit-exact;
   * quantise-append of 65,536 tokens x 8 kv heads through a random slot mapping
     into 64-token pages: the whole 151 MB pool bit-exact.
 """
@@ -45,8 +47,9 @@ def pool_exec():
         yield ex
 
 
-def fill(m, w, device="cuda"):
-    cache = m.PagedCache(w.num_pages, w.page_size, w.num_kv_heads, device=device)
+def fill(m, w, device="cuda", dtype=None):
+    cache = m.PagedCache(w.num_pages, w.page_size, w.num_kv_heads, device=device,
+                         dtype=m.DTYPE_NVFP4 if dtype is None else dtype)
     if w.shared_prefix_tokens:
         pk, pv = w.prefix_kv(device)
         m.quantize_append(cache, pk, pv, w.slots(0, 0, w.shared_prefix_tokens).to(device))
@@ -71,7 +74,7 @@ def rows_mask(local_slots, pool):
     return mask
 
 
-def oracle_decode_all(ex, w, q, seqs, new_kv=None, window=3):
+def oracle_decode_all(ex, w, q, seqs, new_kv=None, window=3, dtype=oracle.DTYPE_NVFP4):
     """fp64 attention (and spread) of every (sequence, kv head) unit of the
     sequences `seqs`, each computed by the oracle from sequence b's BF16 K/V as
     drawn on the GPU (the product's own inputs).  new_kv = (k_new, v_new)
@@ -83,7 +86,7 @@ def oracle_decode_all(ex, w, q, seqs, new_kv=None, window=3):
     pending = []
 
     def unit(i, kv, kb, vb, qg):
-        return i, kv, oracle.sequence_attention(qg, kb, vb, w.sm_scale, spread=True)
+        return i, kv, oracle.sequence_attention(qg, kb, vb, w.sm_scale, dtype=dtype, spread=True)
 
     def drain(keep):
         while len(pending) > keep:
@@ -129,6 +132,21 @@ def test_decode_32k_full_output_of_the_bench_call(m, pool_exec):
 
     ref, spread = oracle_decode_all(pool_exec, w, q, list(range(B)), new_kv=(new_k, new_v))
     check_attention(out, ref, "32K full output (fused append + decode, auto split)", spread=spread)
+
+
+def test_decode_32k_fp8_cache_full_output(m, pool_exec):
+    """The FP8-E4M3 comparison cache at the 32K workload, through the call the
+    bench times for it (paged_decode_attention, automatic split): every unit."""
+    w = workloads.decode_32k()
+    cache = fill(m, w, dtype=m.DTYPE_FP8_E4M3)
+    q = w.q("cuda")
+    out = m.paged_decode_attention(cache, q, w.block_table.cuda(), w.seq_lens.cuda(), w.sm_scale)
+    torch.cuda.synchronize()
+    assert m.check_device_errors() == 0
+    del cache
+    torch.cuda.empty_cache()
+    ref, spread = oracle_decode_all(pool_exec, w, q, list(range(w.batch)), dtype=oracle.DTYPE_FP8)
+    check_attention(out, ref, "32K FP8 cache full output (auto split)", spread=spread)
 
 
 def test_decode_1m_full_output(m, pool_exec):
@@ -197,8 +215,13 @@ def test_agent_mix_full_output(m, pool_exec):
     L = mix.chunk_tokens
     cu_q = torch.arange(0, L * (len(rows) + 1), L, dtype=torch.int32)
     ext = m.extend_attention(qs, kw, vw, cu.cuda(), kn, vn, cu_q.cuda(), L, w.sm_scale)
+    # the same extends with the prefix read from the NVFP4 pages inside the kernel: identical
+    paged = m.extend_attention_paged(cache, qs, w.block_table[rows].contiguous().cuda(), pl.cuda(), kn, vn,
+                                     cu_q.cuda(), L, w.sm_scale)
     torch.cuda.synchronize()
     assert m.check_device_errors() == 0
+    assert torch.equal(paged, ext), "paged-prefix extend differs from dequant + extend"
+    del paged
     eref, espread = oracle.extend_attention(bits(qs), rk, rv, cu.numpy(), bits(kn), bits(vn), cu_q.numpy(),
                                             w.sm_scale, nthreads=THREADS, spread=True)
     check_attention(ext, eref, "agent mix extend, all 8 x 512 rows", eps=EPS_BF16_P, spread=espread)
