@@ -9,7 +9,7 @@ units run in parallel threads).
     in the same launch (the 64 new rows bit-exact too);
   * 1M long-context decode (batch 2 x 1,048,576, 40 q / 8 kv, channel factors),
     automatic split;
-  * the 32K workload over the FP8-E4M3 comparison cache, automatic split;
+  * the 32K and 1M workloads over the FP8-E4M3 comparison cache, automatic split;
   * agent mix: the 128 decode sequences (3.2K-160K tokens sharing a 3,200-token
     prefix) through plain and cascade decode; the 8 extend requests' prefix
     dequant bit-exact, their extend attention on all 8 x 512 chunk rows over the
@@ -160,6 +160,20 @@ def test_decode_1m_full_output(m, pool_exec):
     torch.cuda.empty_cache()
     ref, spread = oracle_decode_all(pool_exec, w, q, [0, 1], window=1)
     check_attention(out, ref, "1M full output (auto split)", spread=spread)
+
+
+def test_decode_1m_fp8_cache_full_output(m, pool_exec):
+    """The FP8-E4M3 comparison cache at the 1M workload (4.3 GB of FP8 KV): every unit."""
+    w = workloads.decode_1m()
+    cache = fill(m, w, dtype=m.DTYPE_FP8_E4M3)
+    q = w.q("cuda")
+    out = m.paged_decode_attention(cache, q, w.block_table.cuda(), w.seq_lens.cuda(), w.sm_scale)
+    torch.cuda.synchronize()
+    assert m.check_device_errors() == 0
+    del cache
+    torch.cuda.empty_cache()
+    ref, spread = oracle_decode_all(pool_exec, w, q, [0, 1], window=1, dtype=oracle.DTYPE_FP8)
+    check_attention(out, ref, "1M FP8 cache full output (auto split)", spread=spread)
 
 
 def test_agent_mix_full_output(m, pool_exec):
