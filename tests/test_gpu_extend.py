@@ -55,6 +55,7 @@ def _case(m, prefix_lens, chunk_lens, Hq, Hkv, seed, max_q_len=None):
     ([77, 5], [0, 130], 8, 1),
     ([127, 256, 257, 0], [129, 64, 255, 1], 32, 8),
     ([128, 383], [96, 33], 16, 2),
+    ([200, 1030], [40, 9], 32, 2),          # G = 16: a 128-row query tile holds 8 chunk tokens
 ])
 def test_extend_matches_oracle(m, prefix_lens, chunk_lens, Hq, Hkv):
     out, (ref, spread) = _case(m, prefix_lens, chunk_lens, Hq, Hkv, sum(prefix_lens) + sum(chunk_lens) + Hq)
@@ -121,6 +122,7 @@ def _paged_case(m, lens, chunk, Hq, Hkv, P, seed, gk=1.0, gv=1.0):
     ([0, 1, 127, 129, 300], [17, 64, 255, 5, 1], 16, 2, 16),
     ([1000, 257], [96, 200], 40, 8, 128),
     ([63, 2048], [300, 7], 8, 1, 32),
+    ([513, 90], [33, 260], 32, 2, 64),
 ])
 def test_paged_extend_equals_dequant_then_extend(m, lens, chunk, Hq, Hkv, P):
     """The prefix expanded inside the kernel gives the same BF16 operands, in the

@@ -1,7 +1,8 @@
 """The fused decode step (new token appended in the decode launch) against the
 two-call path it replaces (quantise-append of the token, then decode): the
 pools must be bit-identical and the outputs identical, over NVFP4 and FP8
-caches, tensor scales, page sizes 16 and 64, tokens landing on a page's first
+caches, tensor scales, page sizes 16 to 128, groups of 1, 4 and 16 query heads
+(both N-tile instances of each cache format), tokens landing on a page's first
 row, single-token and empty sequences, many sequence ends per CTA, strided
 token rows, explicit split counts, and a bad block-table entry; plus the
 fused result against the fp64 oracle."""
@@ -49,14 +50,17 @@ def _two_calls(m, w, cache, new_k, new_v, q, num_splits=0):
     return m.paged_decode_attention(cache, q, w.block_table.cuda(), lens.cuda(), w.sm_scale, num_splits=num_splits)
 
 
-@pytest.mark.parametrize("dtype,gk,gv,P,lens,splits", [
-    (0, 1.0, 1.0, 64, [3000, 1, 64, 65, 0, 700, 129], 0),
-    (0, 0.7, 2.5, 16, [17, 16, 33, 1000, 2], 0),
-    (1, 1.0, 1.0, 64, [513, 64, 1], 0),
-    (0, 1.0, 1.0, 32, [5000, 33, 97], 7),
+@pytest.mark.parametrize("dtype,gk,gv,P,lens,splits,Hq,Hkv", [
+    (0, 1.0, 1.0, 64, [3000, 1, 64, 65, 0, 700, 129], 0, 32, 8),
+    (0, 0.7, 2.5, 16, [17, 16, 33, 1000, 2], 0, 32, 8),
+    (1, 1.0, 1.0, 64, [513, 64, 1], 0, 32, 8),
+    (0, 1.0, 1.0, 32, [5000, 33, 97], 7, 32, 8),
+    (0, 1.0, 1.0, 128, [129, 2000, 1, 128], 0, 32, 2),    # G = 16: the two-N-tile instance
+    (1, 0.5, 4.0, 64, [700, 65, 3], 0, 32, 2),            # FP8, G = 16, tensor scales
+    (0, 1.0, 1.0, 64, [900, 64, 2], 0, 8, 8),             # G = 1
 ])
-def test_fused_equals_append_then_decode(m, dtype, gk, gv, P, lens, splits):
-    w = workloads.make_decode("fused", 41 + P, lens, 32, 8, P, recipe=workloads.ValueRecipe(outlier_p=0.003))
+def test_fused_equals_append_then_decode(m, dtype, gk, gv, P, lens, splits, Hq, Hkv):
+    w = workloads.make_decode("fused", 41 + P, lens, Hq, Hkv, P, recipe=workloads.ValueRecipe(outlier_p=0.003))
     (c_fused, c_two), new_k, new_v = _prepare(m, w, dtype, gk, gv, 41)
     q = w.q("cuda")
     out_f = m.paged_decode_attention_append(c_fused, new_k, new_v, q, w.block_table.cuda(), w.seq_lens.cuda(),
